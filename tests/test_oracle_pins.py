@@ -1,0 +1,457 @@
+"""Pins for the CPU oracle: each test ties it to something other than itself.
+
+Sources: values the pages print (the worked dispatch/combine example, Table 1,
+Figure 2), closed forms, special cases that reduce to simpler formulas,
+invariants of the method, and brute force on tiny inputs.
+"""
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+from moe_decode_layer_fp32_gb300 import synth
+
+LN3 = math.log(3.0)
+
+
+def load(golden_dir, name):
+    with open(os.path.join(golden_dir, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------------------
+# SiLU closed forms
+# ---------------------------------------------------------------------------
+
+
+def test_silu_closed_forms():
+    assert O.silu(0.0) == 0.0
+    # sigmoid(ln 3) = 3/4
+    assert O.silu(LN3) == pytest.approx(0.75 * LN3, rel=1e-15)
+    # sigmoid(-ln 3) = 1/4
+    assert O.silu(-LN3) == pytest.approx(-0.25 * LN3, rel=1e-15)
+    z = np.linspace(-8, 8, 33)
+    # SiLU(-z) = SiLU(z) - z
+    np.testing.assert_allclose(O.silu(-z), O.silu(z) - z, atol=1e-14)
+    # large z: SiLU(z) -> z
+    assert O.silu(60.0) == pytest.approx(60.0, rel=1e-15)
+
+
+def test_bf16_decode_exact():
+    vals = torch.tensor([1.0, -2.5, 0.0078125, 3.0e38, -1.0e-30], dtype=torch.float32)
+    b = vals.to(torch.bfloat16)
+    dec = O.to_f64(b)
+    np.testing.assert_array_equal(dec, b.to(torch.float32).double().numpy())
+    assert O.to_f64(torch.tensor([1.0], dtype=torch.bfloat16))[0] == 1.0
+
+
+# ---------------------------------------------------------------------------
+# The pages' worked 4-token / 4-expert top-2 example
+# ---------------------------------------------------------------------------
+
+
+def worked_example(golden):
+    T = n = d = 4
+    wr = np.full((n, d), -10.0)
+    name = {"E1": 0, "E2": 1, "E3": 2, "E4": 3}
+    for t, tok in enumerate(["T1", "T2", "T3", "T4"]):
+        for ex, w in golden["choices"][tok]:
+            wr[name[ex], t] = math.log(w)
+    x = np.eye(T, d)
+    return x, wr
+
+
+def test_worked_example_routing(golden_dir):
+    gd = load(golden_dir, "dispatch_combine_4tok_4exp_top2.json")
+    x, wr = worked_example(gd)
+    idx, p, _ = O.route(x, wr, k=2)
+    np.testing.assert_array_equal(idx, np.array(gd["expected_idx"]))
+    np.testing.assert_allclose(p, np.array(gd["expected_w"]), rtol=1e-12)
+
+
+def test_worked_example_dispatch(golden_dir):
+    gd = load(golden_dir, "dispatch_combine_4tok_4exp_top2.json")
+    idx = np.array(gd["expected_idx"], np.int32)
+    w = np.array(gd["expected_w"])
+    D = O.dispatch(idx, w, n=4, g=1)
+    np.testing.assert_array_equal(D["exp_count"], gd["expected_exp_count"])
+    np.testing.assert_array_equal(D["exp_off"], gd["expected_exp_off"])
+    np.testing.assert_array_equal(D["asg_tok"], gd["expected_asg_tok"])
+    np.testing.assert_array_equal(D["asg_slot"], gd["expected_asg_slot"])
+    np.testing.assert_array_equal(D["tok_asg"], gd["expected_tok_asg"])
+    D2 = O.dispatch(idx, w, n=4, g=2)
+    dg = gd["departments_g2"]
+    np.testing.assert_array_equal(D2["dept_tok"], dg["expected_dept_tok"])
+    np.testing.assert_array_equal(D2["dept_off"], dg["expected_dept_off"])
+    np.testing.assert_allclose(D2["dept_w"], dg["expected_dept_w"], rtol=1e-15)
+
+
+def test_worked_example_combine(golden_dir):
+    gd = load(golden_dir, "dispatch_combine_4tok_4exp_top2.json")
+    x, wr = worked_example(gd)
+    n, I, d = 4, 2, 4
+    wg = np.full((n, I, d), LN3)
+    wu = np.zeros((n, I, d))
+    wd = np.zeros((n, I, d))
+    for e in range(n):
+        for i in range(I):
+            for t in range(d):
+                wu[e, i, t] = (e + 1) * (i + 1) * (t + 1)
+            wd[e, i, (e + i) % 4] = 1.0
+    idx, p, _ = O.route(x, wr, k=2)
+    y = O.vanilla_layer(x, idx, p, wg, wu, wd)
+    expected = 0.75 * LN3 * np.array(gd["expected_y_over_three_quarters_ln3"])
+    np.testing.assert_allclose(y, expected, rtol=1e-13, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# Routing: brute force and special cases
+# ---------------------------------------------------------------------------
+
+
+def test_topk_matches_rank_definition():
+    rng = np.random.default_rng(7)
+    for trial in range(200):
+        n = int(rng.choice([4, 8, 16]))
+        k = int(rng.integers(1, n + 1))
+        T = int(rng.integers(1, 6))
+        d = int(rng.choice([8, 16]))
+        x = rng.standard_normal((T, d))
+        wr = rng.standard_normal((n, d)) * 0.3
+        if trial % 3 == 0:                     # force exact ties
+            wr[n // 2] = wr[0]
+            if n > 3:
+                wr[n - 1] = wr[1]
+        bias = rng.standard_normal(n) * 0.1 if trial % 2 else None
+        idx, p, info = O.route(x, wr, k, bias=bias)
+        key = info["key32"]
+        for t in range(T):
+            for r, e in enumerate(idx[t]):
+                # rank of e = number of experts strictly ahead of it
+                ahead = sum(1 for f in range(n)
+                            if key[t, f] > key[t, e] or (key[t, f] == key[t, e] and f < e))
+                assert ahead == r
+            assert p[t].sum() == pytest.approx(1.0, abs=1e-14)       # I4
+
+
+def test_topk_softmax_uses_unbiased_logits():
+    # bias moves the selection but not the weights
+    x = np.array([[1.0, 0.0]])
+    wr = np.array([[2.0, 0.0], [1.0, 0.0], [0.5, 0.0]])
+    bias = np.array([-5.0, 0.0, 0.0], np.float32)
+    idx, p, _ = O.route(x, wr, 2, bias=bias)
+    assert list(idx[0]) == [1, 2]
+    e1, e2 = math.exp(1.0), math.exp(0.5)
+    np.testing.assert_allclose(p[0], [e1 / (e1 + e2), e2 / (e1 + e2)], rtol=1e-14)
+
+
+def test_equal_logits_give_uniform_weights():
+    x = np.ones((3, 8))
+    wr = np.zeros((16, 8))
+    idx, p, _ = O.route(x, wr, 4, scale=2.0)
+    np.testing.assert_array_equal(idx, np.tile(np.arange(4), (3, 1)))   # I5
+    np.testing.assert_allclose(p, np.full((3, 4), 0.5), rtol=1e-15)    # scale/k
+
+
+def test_k_equals_n_routes_everything():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((2, 8))
+    wr = rng.standard_normal((5, 8))
+    idx, p, _ = O.route(x, wr, 5)
+    for t in range(2):
+        assert sorted(idx[t]) == list(range(5))
+        l = wr @ x[t]
+        np.testing.assert_allclose(p[t], np.exp(l[idx[t]]) / np.exp(l).sum(), rtol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# Dense brute force vs the gathered per-token evaluation
+# ---------------------------------------------------------------------------
+
+
+def dense_layer(x, gate_matrix, wg, wu, wd):
+    """All experts on all tokens, masked afterwards by the gate matrix."""
+    G = np.einsum("eid,td->eti", wg, x)
+    U = np.einsum("eid,td->eti", wu, x)
+    H = G / (1.0 + np.exp(-G)) * U
+    Y = np.einsum("eti,eid->etd", H, wd)
+    return np.einsum("te,etd->td", gate_matrix, Y)
+
+
+def test_vanilla_matches_dense_bruteforce():
+    rng = np.random.default_rng(11)
+    for trial in range(200):
+        d = int(rng.choice([8, 16]))
+        n = int(rng.choice([4, 8]))
+        k = int(rng.integers(1, 4))
+        T = int(rng.integers(1, 9))
+        I = 4
+        x = rng.standard_normal((T, d))
+        wr = rng.standard_normal((n, d)) * 0.5
+        wg, wu, wd = (rng.standard_normal((n, I, d)) * 0.3 for _ in range(3))
+        idx, p, _ = O.route(x, wr, k)
+        Gm = np.zeros((T, n))
+        for t in range(T):
+            for s in range(k):
+                Gm[t, idx[t, s]] = p[t, s]
+        y = O.vanilla_layer(x, idx, p, wg, wu, wd)
+        np.testing.assert_allclose(y, dense_layer(x, Gm, wg, wu, wd), rtol=1e-11, atol=1e-12)
+
+
+def test_shared_expert_added_with_weight_one():
+    rng = np.random.default_rng(5)
+    T, d, n, I, k = 3, 8, 4, 4, 2
+    x = rng.standard_normal((T, d))
+    wr = rng.standard_normal((n, d))
+    wg, wu, wd = (rng.standard_normal((n, I, d)) for _ in range(3))
+    sg, su, sd = (rng.standard_normal((6, d)) for _ in range(3))
+    idx, p, _ = O.route(x, wr, k)
+    y0 = O.vanilla_layer(x, idx, p, wg, wu, wd)
+    y1 = O.vanilla_layer(x, idx, p, wg, wu, wd, shared=(sg, su, sd))
+    # the shared expert is the only expert of a 1-expert, top-1 layer (weight 1)
+    ys = O.vanilla_layer(x, np.zeros((T, 1), np.int32), np.ones((T, 1)),
+                         sg[None], su[None], sd[None])
+    np.testing.assert_allclose(y1 - y0, ys, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# DeaMoE form C invariants
+# ---------------------------------------------------------------------------
+
+
+def rand_formc(rng, T=5, d=16, n=8, g=4, I_sh=8, I_pr=4, k=3):
+    x = rng.standard_normal((T, d))
+    wr = rng.standard_normal((n, d)) * 0.5
+    m = n // g
+    dept = [rng.standard_normal((m, I_sh, d)) * 0.3 for _ in range(3)]
+    priv = [rng.standard_normal((n, I_pr, d)) * 0.3 for _ in range(3)]
+    return x, wr, dept, priv
+
+
+def test_formc_g1_no_private_is_vanilla():
+    rng = np.random.default_rng(21)
+    x, wr, dept, _ = rand_formc(rng, n=8, g=1, I_sh=8)
+    idx, p, _ = O.route(x, wr, 3)
+    y_dea = O.deamoe_layer_c(x, idx, p, 1, *dept)
+    y_van = O.vanilla_layer(x, idx, p, *dept)
+    np.testing.assert_array_equal(y_dea, y_van)                           # I1
+
+
+def test_formc_zero_private_reduces_to_department_ffn():
+    """Zero private weights: y_t = sum_j omega_{t,j} FFN_j(x_t), the two-stage
+    grouping of DeaMoE §3.2 applied to the department backbones."""
+    rng = np.random.default_rng(22)
+    for g in (2, 4):
+        x, wr, dept, priv = rand_formc(rng, g=g)
+        zero = [np.zeros_like(w) for w in priv]
+        idx, p, _ = O.route(x, wr, 3)
+        y = O.deamoe_layer_c(x, idx, p, g, *dept, *zero)
+        D = O.dispatch(idx, p, n=8, g=g)
+        ref = np.zeros_like(y)
+        m = 8 // g
+        for j in range(m):
+            for pos in range(D["dept_off"][j], D["dept_off"][j + 1]):
+                t = D["dept_tok"][pos]
+                ref[t] += D["dept_w"][pos] * O.swiglu_expert(x[t], dept[0][j], dept[1][j], dept[2][j])
+        np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)          # I2
+
+
+def test_formc_equals_vanilla_with_materialised_weights():
+    rng = np.random.default_rng(23)
+    g, n = 4, 8
+    x, wr, dept, priv = rand_formc(rng, g=g, n=n)
+    idx, p, _ = O.route(x, wr, 3)
+    y = O.deamoe_layer_c(x, idx, p, g, *dept, *priv)
+    # materialise: expert e = rows of department e//g (np.repeat) over its private rows
+    mats = [np.concatenate([np.repeat(dept[a], g, axis=0), priv[a]], axis=1) for a in range(3)]
+    y_ref = O.vanilla_layer(x, idx, p, *mats)
+    np.testing.assert_allclose(y, y_ref, rtol=1e-12, atol=1e-12)            # I3
+
+
+def test_layer_token_permutation_equivariance():
+    rng = np.random.default_rng(24)
+    x, wr, dept, priv = rand_formc(rng, T=6)
+    perm = rng.permutation(6)
+    idx, p, _ = O.route(x, wr, 3)
+    y = O.deamoe_layer_c(x, idx, p, 4, *dept, *priv)
+    idx2, p2, _ = O.route(x[perm], wr, 3)
+    y2 = O.deamoe_layer_c(x[perm], idx2, p2, 4, *dept, *priv)
+    np.testing.assert_allclose(y2, y[perm], rtol=1e-13, atol=1e-13)        # I6
+
+
+def test_dispatch_lists_are_a_partition():
+    rng = np.random.default_rng(25)
+    for trial in range(100):
+        n, g = 16, int(rng.choice([1, 2, 4, 8]))
+        T, k = int(rng.integers(1, 20)), int(rng.integers(1, 6))
+        idx = np.stack([rng.permutation(n)[:k] for _ in range(T)]).astype(np.int32)
+        p = rng.random((T, k))
+        D = O.dispatch(idx, p, n, g)
+        # every (token, slot) appears once, grouped by expert, tokens ascending
+        seen = set()
+        for e in range(n):
+            toks = D["asg_tok"][D["exp_off"][e]:D["exp_off"][e + 1]]
+            assert list(toks) == sorted(toks)
+            for pos in range(D["exp_off"][e], D["exp_off"][e + 1]):
+                t, s = int(D["asg_tok"][pos]), int(D["asg_slot"][pos])
+                assert idx[t, s] == e and D["tok_asg"][t, s] == pos
+                seen.add((t, s))
+        assert len(seen) == T * k
+        if g > 1:
+            for j in range(n // g):
+                toks = list(D["dept_tok"][D["dept_off"][j]:D["dept_off"][j + 1]])
+                want = sorted({t for t in range(T) for s in range(k) if idx[t, s] // g == j})
+                assert toks == want
+
+
+# ---------------------------------------------------------------------------
+# DeaMoE form P (eq. 4)
+# ---------------------------------------------------------------------------
+
+
+def test_formp_zero_A_gives_zero():
+    rng = np.random.default_rng(31)
+    h, r = 6, 4
+    W = [rng.standard_normal((r, h)) for _ in range(3)]
+    Z = np.zeros((r, r))
+    out = O.deamoe_expert_p(rng.standard_normal(h), *W, Z, Z, Z)
+    np.testing.assert_array_equal(out, np.zeros(h))
+
+
+def test_formp_identity_A_closed_form():
+    """Identity init (DeaMoE §3.4): with A = I each expert reduces to
+    W_d^T SiLU(SiLU(SiLU(W_g x)) * SiLU(W_u x))."""
+    rng = np.random.default_rng(32)
+    h, r = 6, 4
+    wg, wu, wd = (rng.standard_normal((r, h)) for _ in range(3))
+    x = rng.standard_normal(h)
+    Id = np.eye(r)
+    out = O.deamoe_expert_p(x, wg, wu, wd, Id, Id, Id)
+    s = lambda z: z / (1 + np.exp(-z))
+    ref = wd.T @ s(s(s(wg @ x)) * s(wu @ x))
+    np.testing.assert_allclose(out, ref, rtol=1e-14)
+
+
+def test_formp_hand_example():
+    """h = r = 2, worked by hand so every SiLU argument is 0 or ln 3:
+    W_g x = [ln3, 0] -> sigma -> [3/4 ln3, 0] -> A_g (4/3) -> [ln3, 0] -> SiLU -> [3/4 ln3, 0];
+    W_u x = [0, ln3] -> sigma -> [0, 3/4 ln3] -> A_u (swap) -> [3/4 ln3, 0];
+    product [9/16 ln3^2, 0] -> A_d^T -> [ln3, 0] -> sigma -> [3/4 ln3, 0];
+    W_d^T [3/4 ln3, 0] = 3/4 ln3 * W_d[0, :] = [3/2 ln3, -3/4 ln3]."""
+    x = np.array([LN3, 0.0])
+    wg = np.array([[1.0, 0.0], [0.0, 1.0]])
+    ag = np.array([[4.0 / 3.0, 0.0], [0.0, 1.0]])
+    wu = np.array([[0.0, 1.0], [1.0, 0.0]])
+    au = np.array([[0.0, 1.0], [1.0, 0.0]])
+    c = 1.0 / (0.5625 * LN3)
+    ad = np.array([[c, 0.0], [7.0, 1.0]])      # A_d^T [a, 0] = [c a, 0]; A_d [a, 0] would not be
+    wd = np.array([[2.0, -1.0], [5.0, 7.0]])   # W_d^T picks row 0; W_d would not
+    out = O.deamoe_expert_p(x, wg, wu, wd, ag, au, ad)
+    np.testing.assert_allclose(out, [1.5 * LN3, -0.75 * LN3], rtol=1e-14)
+
+
+def test_formp_layer_combines_per_eq3():
+    rng = np.random.default_rng(33)
+    T, h, r, n, g, k = 3, 6, 4, 8, 4, 2
+    x = rng.standard_normal((T, h))
+    wr = rng.standard_normal((n, h))
+    W = [rng.standard_normal((n // g, r, h)) for _ in range(3)]
+    A = [rng.standard_normal((n, r, r)) * 0.5 for _ in range(3)]
+    idx, p, _ = O.route(x, wr, k)
+    y = O.deamoe_layer_p(x, idx, p, g, *W, *A)
+    # Two-stage reading (DeaMoE §3.2): O^j = W_d^T sum_i p_i Z^{j,i}
+    ref = np.zeros_like(y)
+    s = lambda z: z / (1 + np.exp(-z))
+    for t in range(T):
+        by_dept = {}
+        for q in range(k):
+            e = idx[t, q]
+            j = e // g
+            Xg, Xu = s(W[0][j] @ x[t]), s(W[1][j] @ x[t])
+            Y = s(A[0][e] @ Xg) * (A[1][e] @ Xu)
+            by_dept[j] = by_dept.get(j, 0) + p[t, q] * s(A[2][e].T @ Y)
+        for j, Zs in by_dept.items():
+            ref[t] += W[2][j].T @ Zs
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# Table 1 and Figure 2
+# ---------------------------------------------------------------------------
+
+
+def test_table1_ratios(golden_dir):
+    gd = load(golden_dir, "table1_fig2.json")
+    for name, r in gd["rows"].items():
+        fl, pa = O.table1_ratios(r["h"], r["r"], r["n_base"], r["k_base"], r["m"], r["n"],
+                                 r["k_dept"], r["k"])
+        assert round(pa, 3) == pytest.approx(r["params"], abs=1e-3 + 1e-9), name
+        if r["flops"] is not None:
+            assert round(fl, 3) == pytest.approx(r["flops"], abs=1e-3 + 1e-9), name
+
+
+def test_figure2_dsv3_loading_bounds(golden_dir):
+    gd = load(golden_dir, "table1_fig2.json")
+    r = gd["rows"]["DeepSeek-V3"]
+    f = gd["figure2_dsv3"]
+    for with_router in (False, True):
+        ratios = [100 * O.loading_ratio_formp(r["h"], r["r"], r["n_base"], r["k_base"], r["n"],
+                                              r["m"], r["k"], T, with_router)
+                  for T in range(f["batch_range"][0], f["batch_range"][1] + 1)]
+        assert min(ratios) == pytest.approx(f["min_percent"], abs=f["tolerance_pp"])
+        assert max(ratios) == pytest.approx(f["max_percent"], abs=f["tolerance_pp"])
+    # the non-monotonic shape the figure describes: falls, then rises toward 1
+    rt = [O.loading_ratio_formp(7168, 2048, 256, 8, 864, 8, 10, T) for T in (1, 16, 512)]
+    assert rt[1] < rt[0] and rt[1] < rt[2] and rt[2] < 1.0
+
+
+def test_expected_active_counts_monte_carlo():
+    """E[A_e], E[A_d] closed forms against the oracle's dispatch counts for
+    uniform k-of-n routing (10^4 trials)."""
+    rng = np.random.default_rng(41)
+    n, k, g, T = 64, 8, 8, 4
+    trials = 10000
+    Ae = np.empty(trials)
+    Ad = np.empty(trials)
+    for i in range(trials):
+        idx = np.stack([rng.choice(n, k, replace=False) for _ in range(T)]).astype(np.int32)
+        occupied = np.zeros(n, bool)
+        occupied[idx.ravel()] = True
+        Ae[i] = occupied.sum()
+        Ad[i] = len(set(int(e) // g for e in idx.ravel()))
+    # 4-sigma bands on the sample means
+    assert abs(Ae.mean() - O.expected_active_experts(n, k, T)) < 4 * Ae.std() / math.sqrt(trials)
+    assert abs(Ad.mean() - O.expected_active_depts(n, k, g, T)) < 4 * Ad.std() / math.sqrt(trials)
+    # and the oracle's dispatch agrees with the direct count on a sample
+    for i in range(50):
+        idx = np.stack([rng.choice(n, k, replace=False) for _ in range(T)]).astype(np.int32)
+        D = O.dispatch(idx, np.ones((T, k)), n, g)
+        assert len(D["active_experts"]) == len(set(idx.ravel()))
+        assert len(D["active_depts"]) == len(set(int(e) // g for e in idx.ravel()))
+
+
+def test_unique_bytes_matches_touched_tensors():
+    """The closed-form byte count equals the bytes of the weight slices the
+    literal evaluation touches (router + shared + active units)."""
+    shape = synth.TINY_DEAMOE
+    L = synth.make_layer(shape, seed=0)
+    x = synth.hidden(4, shape.d, seed=0)
+    idx, p, _ = O.route(x, L["router"], shape.k)
+    D = O.dispatch(idx, p, shape.n, shape.g)
+    touched = L["router"].numel() * L["router"].element_size()
+    for j in D["active_depts"]:
+        touched += sum(L[key][int(j)].numel() * L[key].element_size() for key in ("dgate", "dup", "ddown"))
+    for e in D["active_experts"]:
+        touched += sum(L[key][int(e)].numel() * L[key].element_size() for key in ("pgate", "pup", "pdown"))
+    U = O.unique_bytes_deamoe_c(shape.d, shape.n, shape.I_sh, shape.I_pr, 0,
+                                len(D["active_depts"]), len(D["active_experts"]), 4)
+    assert U == touched
+    # vanilla with a shared expert, bf16
+    Uv = O.unique_bytes_vanilla(2048, 128, 768, 256, 10, 2)
+    assert Uv == 4 * 2048 * 128 + 2 * 3 * 2048 * (10 * 768 + 256)
