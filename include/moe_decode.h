@@ -1,0 +1,276 @@
+/*
+ * moe_decode.h -- C ABI of the GB300 (sm_103a) MoE / DeaMoE small-batch decode layer.
+ *
+ * The layer (vanilla top-k SwiGLU MoE with an optional always-on shared expert,
+ * and the DeaMoE department variant) is split into the steps the pages describe:
+ * routing, dispatch, expert FFN, combine.  Each step is one entry point; the
+ * *_layer_forward calls chain them with fewer launches.
+ *
+ * Sources:
+ *   [DeaMoE]  "DeaMoE: Efficient MoE Structure for Fast Small-Batch Decoding":
+ *             §2.1 eqs. (1)-(3), §3.1-3.2 (departments, two-stage routing).
+ *   [DSMoE]   "DeepSeekMoE Guide: Fine-Grained Experts & Dynamic Routing":
+ *             "Mathematical Formulation of the DeepSeekMoE Forward Pass".
+ *   [MoE-inf] "MoE inference engineering, clearly explained": "How a batch
+ *             becomes expert-specific matrices", "Local MoE execution pipeline".
+ *
+ * Conventions (all entry points):
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, unless a
+ *     parameter says "host".  The library never allocates, frees or
+ *     synchronises inside a step; all scratch lives in the caller's workspace.
+ *   - Every step is asynchronous on the given stream (a cudaStream_t passed as
+ *     void*; NULL = legacy default stream) and may be captured in a CUDA graph.
+ *   - Activations, router weights, routing weights and outputs are fp32.
+ *     Expert weights are fp32 or bf16 (MOE_DTYPE_*), row-major.
+ *   - Weight layout (per unit: an expert, a department backbone, a private
+ *     block or the shared expert): gate, up and down are each [rows, d]
+ *     row-major.  Gate/up rows are the rows of W_gate / W_up; the down tensor
+ *     holds W_down in the paper's [hffn, h] shape and is applied transposed
+ *     ([DeaMoE] §2.1).  Stacked tensors are [units, rows, d].
+ *   - Pointers must be 16-byte aligned; d must be a multiple of 8 and every
+ *     intermediate size a multiple of 16.
+ *   - Return value: MOE_OK or a negative MOE_ERR_* code; nothing is launched
+ *     when the host-side checks fail.  moe_last_error() gives a message
+ *     (thread-local).  Device-side checks (an expert index out of range, a
+ *     token choosing an expert twice, a wait that timed out) write a code into
+ *     the workspace status word, read with moe_read_status().
+ */
+#ifndef MOE_DECODE_H
+#define MOE_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK               0
+#define MOE_ERR_INVALID_ARG (-1)  /* null pointer, bad size, misalignment    */
+#define MOE_ERR_UNSUPPORTED (-2)  /* valid but outside what the kernels take */
+#define MOE_ERR_WORKSPACE   (-3)  /* workspace smaller than required         */
+#define MOE_ERR_CUDA        (-4)  /* a CUDA runtime call failed              */
+#define MOE_ERR_TIMEOUT     (-5)  /* device status: a bounded wait expired   */
+#define MOE_ERR_DEVICE      (-6)  /* device status: bad routing input        */
+
+#define MOE_DTYPE_F32  0
+#define MOE_DTYPE_BF16 1
+
+/* Output modes of the FFN steps. */
+#define MOE_OUT_ROWS  0  /* one unweighted row per (unit, token); moe_combine sums them */
+#define MOE_OUT_ACCUM 1  /* routing weights applied in the epilogue, added into y[T,d]   */
+
+/* Library version (major*10000 + minor*100 + patch). */
+int moe_version(void);
+
+/* Message for the last failed call on this thread ("" if none). */
+const char* moe_last_error(void);
+
+/* ------------------------------------------------------------------------- */
+/* Workspace                                                                 */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Byte offsets of the workspace arrays for a (T, n, k, experts_per_dept) step.
+ * The dispatch lists follow [MoE-inf] "How a batch becomes expert-specific
+ * matrices" (group the T*k assignments by expert, keep each token id and an
+ * inverse map for the combine) and the department token sets X^j of [DeaMoE]
+ * §3.2.  Canonical order everywhere: ascending expert (department) id, then
+ * ascending token id.
+ *
+ *   status    int32[4]   [0] first device error code (0 = none)
+ *   counts    int32[4]   [0] active experts A_e, [1] active departments A_d
+ *   logits    float[T*n] router logits (scratch of moe_route_topk)
+ *   exp_count int32[n]   assignments per expert
+ *   exp_off   int32[n+1] exclusive prefix sum of exp_count
+ *   asg_tok   int32[T*k] token of each assignment (expert-sorted)
+ *   asg_slot  int32[T*k] top-k slot of each assignment
+ *   asg_w     float[T*k] routing weight of each assignment
+ *   tok_asg   int32[T*k] inverse map: (token, slot) -> assignment position
+ *   act_exp   int32[n]   active experts, ascending (first A_e valid)
+ *   dept_count int32[m]  tokens per department (m = n / experts_per_dept)
+ *   dept_off  int32[m+1] exclusive prefix sum of dept_count
+ *   dept_tok  int32[T*min(k,m)] tokens of each department (X^j), each once
+ *   dept_w    float[T*min(k,m)] sum of the token's routing weights inside X^j
+ *   tok_dpos  int32[T*m] (token, department) -> position in dept_tok, or -1
+ *   act_dept  int32[m]   active departments, ascending (first A_d valid)
+ *   sync      uint32[4]  internal counters (kept at zero between calls)
+ * The department arrays are present only when experts_per_dept > 1.
+ */
+typedef struct moe_ws_layout {
+    size_t total;
+    size_t status, counts, logits;
+    size_t exp_count, exp_off, asg_tok, asg_slot, asg_w, tok_asg, act_exp;
+    size_t dept_count, dept_off, dept_tok, dept_w, tok_dpos, act_dept;
+    size_t sync;
+} moe_ws_layout;
+
+/* Required workspace bytes; 0 on invalid arguments.  T, n, k as for routing;
+ * experts_per_dept = g (1 for a vanilla layer; n % g == 0). */
+size_t moe_workspace_bytes(int T, int n, int k, int experts_per_dept);
+
+/* Fill *out (host) with the layout above.  MOE_ERR_INVALID_ARG on bad sizes. */
+int moe_workspace_layout(int T, int n, int k, int experts_per_dept, moe_ws_layout* out);
+
+/* Zero a workspace once before its first use (enqueued on stream). The library
+ * leaves its internal counters at zero after every call, so one init serves
+ * any number of steps on that workspace. */
+int moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Copy the status word and the active counts to the host (synchronises the
+ * stream).  host_status: int32[1], host_counts: int32[2] (A_e, A_d); either may
+ * be NULL.  Off the timed path. */
+int moe_read_status(const void* ws, size_t ws_bytes, int32_t* host_status,
+                    int32_t* host_counts, void* stream);
+
+/* ------------------------------------------------------------------------- */
+/* Step 1: router GEMV + top-k + routing weights                             */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * [DeaMoE] §2.1 eq. (2) S(x) = TopK(W_r x, k) and the weights of eq. (3);
+ * [DSMoE] routing-bias form: the bias takes part in the selection only.
+ *   x        float[T, d]   hidden states
+ *   w_router float[n, d]   router rows (row e = expert e)
+ *   bias     float[n] or NULL  selection-only bias b_e
+ *   scale    routing-weight scale (1.0 = plain softmax)
+ *   topk_idx int32[T, k]   out: experts by descending (logit + bias); equal
+ *                          keys -> lower expert index first
+ *   topk_w   float[T, k]   out: scale * softmax over the k selected UNBIASED
+ *                          logits
+ *   ws       workspace (logits scratch + a counter)
+ * Limits: 1 <= T <= 128, 1 <= k <= min(n, 32), n <= 1024, d % 8 == 0.
+ */
+int moe_route_topk(const float* x, const float* w_router, const float* bias,
+                   int T, int d, int n, int k, float scale,
+                   int32_t* topk_idx, float* topk_w,
+                   void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------- */
+/* Step 2: dispatch (two-level index lists, built on the device)             */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Build the expert and department lists of the workspace from (topk_idx,
+ * topk_w), with no host round trip.  Expert e belongs to department
+ * e / experts_per_dept; a department's token weight is the sum of the token's
+ * routing weights over the department's selected experts, in slot order.
+ * experts_per_dept = 1 builds only the expert lists (vanilla layer).
+ * Device errors (index outside [0,n), a token repeating an expert) set the
+ * status word to MOE_ERR_DEVICE.
+ */
+int moe_dispatch(const int32_t* topk_idx, const float* topk_w, int T, int n, int k,
+                 int experts_per_dept, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------- */
+/* Step 3: expert FFN                                                        */
+/* ------------------------------------------------------------------------- */
+
+/* Rows needed by MOE_OUT_ROWS: T*k assignment rows, then T*min(k,m) department
+ * rows (DeaMoE only), then T shared-expert rows (if has_shared).  Each row is
+ * float[d].  Returns -1 on invalid arguments. */
+int64_t moe_rows_count(int T, int n, int k, int experts_per_dept, int has_shared);
+
+/*
+ * Vanilla expert FFN of [DeaMoE] eq. (1) for every active expert over its
+ * gathered tokens, plus the shared expert of [DSMoE] (weight 1, all tokens)
+ * when I_s > 0.  Reads the dispatch lists from ws.
+ *   w_gate, w_up, w_down  [n, I, d] (dtype)
+ *   s_gate, s_up, s_down  [I_s, d] or NULL when I_s == 0
+ *   out_mode MOE_OUT_ROWS:  out = rows[moe_rows_count, d], overwritten; row
+ *            p (< T*k) is expert asg's unweighted output for assignment p;
+ *            shared rows start at T*k.
+ *   out_mode MOE_OUT_ACCUM: out = y[T, d]; y[t] += sum_s w[t,s] FFN_e(x_t)
+ *            (+ FFN_shared(x_t)).  The caller zeroes y beforehand.
+ */
+int moe_ffn_vanilla(const float* x, int T, int d, int n, int k, int I, int dtype,
+                    const void* w_gate, const void* w_up, const void* w_down,
+                    int I_s, const void* s_gate, const void* s_up, const void* s_down,
+                    const void* ws, size_t ws_bytes, int out_mode, float* out,
+                    void* stream);
+
+/*
+ * DeaMoE FFN, form C: expert i of department j = i / g has the intermediate
+ * [department j's I_sh shared rows ; expert i's I_pr private rows].  Following
+ * the two-stage routing of [DeaMoE] §3.2, each active department's backbone
+ * runs once over its token set X^j (rows weighted by the department token
+ * weight), and each active expert's private rows run over its own tokens.
+ *   dept_gate, dept_up, dept_down  [m, I_sh, d]
+ *   priv_gate, priv_up, priv_down  [n, I_pr, d] (NULL allowed when I_pr == 0)
+ *   s_gate, s_up, s_down           [I_s, d] or NULL when I_s == 0
+ *   out_mode as for moe_ffn_vanilla: ROWS puts private rows at assignment
+ *   positions, department rows at T*k + dept position, shared rows after.
+ * experts_per_dept = 1 is allowed: each department is then one expert whose
+ * intermediate is [I_sh rows ; I_pr rows], i.e. a vanilla layer with
+ * I = I_sh + I_pr, and there are no department rows.
+ */
+int deamoe_ffn(const float* x, int T, int d, int n, int k, int experts_per_dept,
+               int I_sh, int I_pr, int dtype,
+               const void* dept_gate, const void* dept_up, const void* dept_down,
+               const void* priv_gate, const void* priv_up, const void* priv_down,
+               int I_s, const void* s_gate, const void* s_up, const void* s_down,
+               const void* ws, size_t ws_bytes, int out_mode, float* out,
+               void* stream);
+
+/* ------------------------------------------------------------------------- */
+/* Step 4: combine                                                           */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * [MoE-inf] combine: return every row to its token through the inverse map and
+ * add it with its routing weight ([DeaMoE] eq. (3)).  For token t, in this
+ * fixed order: slots s = 0..k-1 (weight topk_w[t,s]), then its departments in
+ * ascending id (department weight), then its shared-expert row (weight 1).
+ *   rows float[moe_rows_count(...), d] from an FFN step in MOE_OUT_ROWS mode
+ *   y    float[T, d], overwritten
+ */
+int moe_combine(const float* rows, int T, int d, int n, int k, int experts_per_dept,
+                int has_shared, const void* ws, size_t ws_bytes, float* y,
+                void* stream);
+
+/* ------------------------------------------------------------------------- */
+/* Whole layer                                                               */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * route -> dispatch -> FFN (MOE_OUT_ACCUM) with the routing and dispatch fused
+ * in one kernel that also zeroes y, and the FFN launched as its programmatic
+ * dependent.  topk_idx / topk_w receive the routing like moe_route_topk.
+ */
+int moe_layer_forward(const float* x, int T, int d, int n, int k, float scale,
+                      const float* w_router, const float* bias,
+                      int I, int dtype, const void* w_gate, const void* w_up,
+                      const void* w_down, int I_s, const void* s_gate,
+                      const void* s_up, const void* s_down,
+                      void* ws, size_t ws_bytes, int32_t* topk_idx, float* topk_w,
+                      float* y, void* stream);
+
+int deamoe_layer_forward(const float* x, int T, int d, int n, int k, float scale,
+                         const float* w_router, const float* bias,
+                         int experts_per_dept, int I_sh, int I_pr, int dtype,
+                         const void* dept_gate, const void* dept_up, const void* dept_down,
+                         const void* priv_gate, const void* priv_up, const void* priv_down,
+                         int I_s, const void* s_gate, const void* s_up, const void* s_down,
+                         void* ws, size_t ws_bytes, int32_t* topk_idx, float* topk_w,
+                         float* y, void* stream);
+
+/* ------------------------------------------------------------------------- */
+/* Byte accounting (host only)                                               */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Weight bytes one step must read at least once ("unique weight bytes"): the
+ * fp32 router, the shared expert, and each active unit's three matrices once.
+ *   vanilla: 4*d*n + bw*3*d*(A_e*I + I_s)
+ *   DeaMoE:  4*d*n + bw*3*d*(A_d*I_sh + A_e*I_pr + I_s)
+ * where bw = 2 (bf16) or 4 (fp32).  Returns -1 on invalid arguments.
+ */
+int64_t moe_unique_weight_bytes_vanilla(int d, int n, int I, int I_s, int dtype, int A_e);
+int64_t moe_unique_weight_bytes_deamoe(int d, int n, int I_sh, int I_pr, int I_s,
+                                       int dtype, int A_d, int A_e);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_DECODE_H */

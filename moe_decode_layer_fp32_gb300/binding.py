@@ -1,0 +1,243 @@
+"""ctypes binding of ``libmoe_gb300.so``: argument marshalling only.
+
+Every function has the name of the C entry point it calls (see
+``include/moe_decode.h``).  Tensors are passed as device pointers, sizes are
+read from their shapes, and the stream is torch's current CUDA stream.  No
+step of the layer runs here; a missing library raises instead of falling back.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_gb300.so")
+
+MOE_OK = 0
+MOE_DTYPE_F32 = 0
+MOE_DTYPE_BF16 = 1
+MOE_OUT_ROWS = 0
+MOE_OUT_ACCUM = 1
+
+ERRORS = {-1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_WORKSPACE",
+          -4: "MOE_ERR_CUDA", -5: "MOE_ERR_TIMEOUT", -6: "MOE_ERR_DEVICE"}
+
+WS_FIELDS = ("total", "status", "counts", "logits", "exp_count", "exp_off", "asg_tok",
+             "asg_slot", "asg_w", "tok_asg", "act_exp", "dept_count", "dept_off", "dept_tok",
+             "dept_w", "tok_dpos", "act_dept", "sync")
+
+
+class WsLayout(C.Structure):
+    _fields_ = [(f, C.c_size_t) for f in WS_FIELDS]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} failed: {ERRORS.get(code, code)}: {msg}")
+        self.code = code
+
+
+_lib = None
+
+_P, _I, _F, _SZ, _I64 = C.c_void_p, C.c_int, C.c_float, C.c_size_t, C.c_int64
+
+_SIGS = {
+    "moe_version": (_I, []),
+    "moe_last_error": (C.c_char_p, []),
+    "moe_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "moe_workspace_layout": (_I, [_I, _I, _I, _I, C.POINTER(WsLayout)]),
+    "moe_workspace_init": (_I, [_P, _SZ, _P]),
+    "moe_read_status": (_I, [_P, _SZ, C.POINTER(C.c_int32), C.POINTER(C.c_int32), _P]),
+    "moe_route_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _SZ, _P]),
+    "moe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _P, _SZ, _P]),
+    "moe_rows_count": (_I64, [_I, _I, _I, _I, _I]),
+    "moe_ffn_vanilla": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P,
+                             _P, _SZ, _I, _P, _P]),
+    "deamoe_ffn": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I,
+                        _P, _P, _P, _P, _SZ, _I, _P, _P]),
+    "moe_combine": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _SZ, _P, _P]),
+    "moe_layer_forward": (_I, [_P, _I, _I, _I, _I, _F, _P, _P, _I, _I, _P, _P, _P, _I,
+                               _P, _P, _P, _P, _SZ, _P, _P, _P, _P]),
+    "deamoe_layer_forward": (_I, [_P, _I, _I, _I, _I, _F, _P, _P, _I, _I, _I, _I, _P, _P,
+                                  _P, _P, _P, _P, _I, _P, _P, _P, _P, _SZ, _P, _P, _P, _P]),
+    "moe_unique_weight_bytes_vanilla": (_I64, [_I, _I, _I, _I, _I, _I]),
+    "moe_unique_weight_bytes_deamoe": (_I64, [_I, _I, _I, _I, _I, _I, _I, _I]),
+}
+
+
+def lib() -> C.CDLL:
+    """Load the native library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"native library not built: {LIB_PATH} "
+                              "(run __graft_entry__.build())")
+        L = C.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def exported_symbols():
+    return tuple(_SIGS)
+
+
+def _check(fn: str, rc: int):
+    if rc != MOE_OK:
+        raise MoeError(fn, rc, lib().moe_last_error().decode())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _dtype_code(t) -> int:
+    if t.dtype == torch.bfloat16:
+        return MOE_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return MOE_DTYPE_F32
+    raise ValueError(f"unsupported weight dtype {t.dtype}")
+
+
+# ---------------------------------------------------------------- workspace
+
+
+def moe_workspace_bytes(T: int, n: int, k: int, experts_per_dept: int = 1) -> int:
+    b = lib().moe_workspace_bytes(T, n, k, experts_per_dept)
+    if b == 0:
+        raise MoeError("moe_workspace_bytes", -1, "invalid sizes")
+    return b
+
+
+def moe_workspace_layout(T: int, n: int, k: int, experts_per_dept: int = 1) -> dict:
+    L = WsLayout()
+    _check("moe_workspace_layout", lib().moe_workspace_layout(T, n, k, experts_per_dept, C.byref(L)))
+    return {f: getattr(L, f) for f in WS_FIELDS}
+
+
+def new_workspace(T: int, n: int, k: int, experts_per_dept: int = 1, device="cuda") -> torch.Tensor:
+    """Allocate (torch) and zero (library kernel) a workspace."""
+    ws = torch.empty(moe_workspace_bytes(T, n, k, experts_per_dept), dtype=torch.uint8, device=device)
+    moe_workspace_init(ws)
+    return ws
+
+
+def moe_workspace_init(ws: torch.Tensor):
+    _check("moe_workspace_init", lib().moe_workspace_init(_ptr(ws), ws.numel(), _stream()))
+
+
+def moe_read_status(ws: torch.Tensor):
+    """(status, A_e, A_d) -- synchronises the current stream."""
+    st = (C.c_int32 * 1)()
+    cnt = (C.c_int32 * 2)()
+    _check("moe_read_status", lib().moe_read_status(_ptr(ws), ws.numel(), st, cnt, _stream()))
+    return int(st[0]), int(cnt[0]), int(cnt[1])
+
+
+# ---------------------------------------------------------------- steps
+
+
+def moe_route_topk(x, w_router, bias, k: int, scale: float, topk_idx, topk_w, ws):
+    T, d = x.shape
+    n = w_router.shape[0]
+    _check("moe_route_topk", lib().moe_route_topk(
+        _ptr(x), _ptr(w_router), _ptr(bias), T, d, n, k, scale, _ptr(topk_idx), _ptr(topk_w),
+        _ptr(ws), ws.numel(), _stream()))
+
+
+def moe_dispatch(topk_idx, topk_w, n: int, experts_per_dept: int, ws):
+    T, k = topk_idx.shape
+    _check("moe_dispatch", lib().moe_dispatch(
+        _ptr(topk_idx), _ptr(topk_w), T, n, k, experts_per_dept, _ptr(ws), ws.numel(), _stream()))
+
+
+def moe_rows_count(T: int, n: int, k: int, experts_per_dept: int, has_shared: bool) -> int:
+    r = lib().moe_rows_count(T, n, k, experts_per_dept, 1 if has_shared else 0)
+    if r < 0:
+        raise MoeError("moe_rows_count", -1, "invalid sizes")
+    return r
+
+
+def moe_ffn_vanilla(x, k: int, w_gate, w_up, w_down, shared, ws, out_mode: int, out):
+    """``shared`` = (s_gate, s_up, s_down) or None."""
+    T, d = x.shape
+    n, I, _ = w_gate.shape
+    sg, su, sd = shared if shared is not None else (None, None, None)
+    I_s = sg.shape[0] if sg is not None else 0
+    _check("moe_ffn_vanilla", lib().moe_ffn_vanilla(
+        _ptr(x), T, d, n, k, I, _dtype_code(w_gate), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
+        I_s, _ptr(sg), _ptr(su), _ptr(sd), _ptr(ws), ws.numel(), out_mode, _ptr(out), _stream()))
+
+
+def deamoe_ffn(x, k: int, experts_per_dept: int, dept, priv, shared, ws, out_mode: int, out):
+    """``dept`` = (gate, up, down) [m, I_sh, d]; ``priv`` = (gate, up, down)
+    [n, I_pr, d] or None; ``shared`` = (gate, up, down) [I_s, d] or None."""
+    T, d = x.shape
+    m, I_sh, _ = dept[0].shape
+    n = m * experts_per_dept
+    pg, pu, pd = priv if priv is not None else (None, None, None)
+    I_pr = pg.shape[1] if pg is not None else 0
+    sg, su, sd = shared if shared is not None else (None, None, None)
+    I_s = sg.shape[0] if sg is not None else 0
+    _check("deamoe_ffn", lib().deamoe_ffn(
+        _ptr(x), T, d, n, k, experts_per_dept, I_sh, I_pr, _dtype_code(dept[0]),
+        _ptr(dept[0]), _ptr(dept[1]), _ptr(dept[2]), _ptr(pg), _ptr(pu), _ptr(pd),
+        I_s, _ptr(sg), _ptr(su), _ptr(sd), _ptr(ws), ws.numel(), out_mode, _ptr(out), _stream()))
+
+
+def moe_combine(rows, T: int, n: int, k: int, experts_per_dept: int, has_shared: bool, ws, y):
+    d = rows.shape[1]
+    _check("moe_combine", lib().moe_combine(
+        _ptr(rows), T, d, n, k, experts_per_dept, 1 if has_shared else 0, _ptr(ws), ws.numel(),
+        _ptr(y), _stream()))
+
+
+def moe_layer_forward(x, k: int, scale: float, w_router, bias, w_gate, w_up, w_down, shared,
+                      ws, topk_idx, topk_w, y):
+    T, d = x.shape
+    n, I, _ = w_gate.shape
+    sg, su, sd = shared if shared is not None else (None, None, None)
+    I_s = sg.shape[0] if sg is not None else 0
+    _check("moe_layer_forward", lib().moe_layer_forward(
+        _ptr(x), T, d, n, k, scale, _ptr(w_router), _ptr(bias), I, _dtype_code(w_gate),
+        _ptr(w_gate), _ptr(w_up), _ptr(w_down), I_s, _ptr(sg), _ptr(su), _ptr(sd),
+        _ptr(ws), ws.numel(), _ptr(topk_idx), _ptr(topk_w), _ptr(y), _stream()))
+
+
+def deamoe_layer_forward(x, k: int, scale: float, w_router, bias, experts_per_dept: int, dept,
+                         priv, shared, ws, topk_idx, topk_w, y):
+    T, d = x.shape
+    n = w_router.shape[0]
+    I_sh = dept[0].shape[1]
+    pg, pu, pd = priv if priv is not None else (None, None, None)
+    I_pr = pg.shape[1] if pg is not None else 0
+    sg, su, sd = shared if shared is not None else (None, None, None)
+    I_s = sg.shape[0] if sg is not None else 0
+    _check("deamoe_layer_forward", lib().deamoe_layer_forward(
+        _ptr(x), T, d, n, k, scale, _ptr(w_router), _ptr(bias), experts_per_dept, I_sh, I_pr,
+        _dtype_code(dept[0]), _ptr(dept[0]), _ptr(dept[1]), _ptr(dept[2]), _ptr(pg), _ptr(pu),
+        _ptr(pd), I_s, _ptr(sg), _ptr(su), _ptr(sd), _ptr(ws), ws.numel(), _ptr(topk_idx),
+        _ptr(topk_w), _ptr(y), _stream()))
+
+
+def moe_unique_weight_bytes_vanilla(d, n, I, I_s, dtype_code, A_e) -> int:
+    return int(lib().moe_unique_weight_bytes_vanilla(d, n, I, I_s, dtype_code, A_e))
+
+
+def moe_unique_weight_bytes_deamoe(d, n, I_sh, I_pr, I_s, dtype_code, A_d, A_e) -> int:
+    return int(lib().moe_unique_weight_bytes_deamoe(d, n, I_sh, I_pr, I_s, dtype_code, A_d, A_e))

@@ -1,0 +1,450 @@
+// C ABI of the decode layer: host-side argument checks, workspace layout and
+// kernel launches.  See include/moe_decode.h for the contract of each call.
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "../../include/moe_decode.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+    return fail(MOE_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+// Widest hidden size the streaming FFN covers: 15 consumer warps x 2 chunks x 8 columns.
+constexpr int kMaxHidden = 15 * 32 * 2 * 8;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool layout_of(int T, int n, int k, int g, moe_ws_layout* L) {
+    if (T < 1 || T > moe::kMaxT || n < 1 || n > moe::kMaxN || k < 1 || k > n ||
+        k > moe::kMaxK || g < 1 || n % g != 0)
+        return false;
+    const int m = g > 1 ? n / g : 0;
+    const int dk = g > 1 ? T * (k < m ? k : m) : 0;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes, 256);
+        return o;
+    };
+    L->status = take(4 * sizeof(int32_t));
+    L->counts = take(4 * sizeof(int32_t));
+    L->logits = take((size_t)T * n * sizeof(float));
+    L->exp_count = take((size_t)n * sizeof(int32_t));
+    L->exp_off = take((size_t)(n + 1) * sizeof(int32_t));
+    L->asg_tok = take((size_t)T * k * sizeof(int32_t));
+    L->asg_slot = take((size_t)T * k * sizeof(int32_t));
+    L->asg_w = take((size_t)T * k * sizeof(float));
+    L->tok_asg = take((size_t)T * k * sizeof(int32_t));
+    L->act_exp = take((size_t)n * sizeof(int32_t));
+    L->dept_count = take((size_t)m * sizeof(int32_t));
+    L->dept_off = take((size_t)(m + 1) * sizeof(int32_t));
+    L->dept_tok = take((size_t)dk * sizeof(int32_t));
+    L->dept_w = take((size_t)dk * sizeof(float));
+    L->tok_dpos = take((size_t)T * m * sizeof(int32_t));
+    L->act_dept = take((size_t)m * sizeof(int32_t));
+    L->sync = take(4 * sizeof(uint32_t));
+    L->total = off;
+    return true;
+}
+
+moe::WsPtrs resolve(const void* ws, const moe_ws_layout& L) {
+    char* b = static_cast<char*>(const_cast<void*>(ws));
+    moe::WsPtrs p;
+    p.status = reinterpret_cast<int32_t*>(b + L.status);
+    p.counts = reinterpret_cast<int32_t*>(b + L.counts);
+    p.logits = reinterpret_cast<float*>(b + L.logits);
+    p.exp_count = reinterpret_cast<int32_t*>(b + L.exp_count);
+    p.exp_off = reinterpret_cast<int32_t*>(b + L.exp_off);
+    p.asg_tok = reinterpret_cast<int32_t*>(b + L.asg_tok);
+    p.asg_slot = reinterpret_cast<int32_t*>(b + L.asg_slot);
+    p.asg_w = reinterpret_cast<float*>(b + L.asg_w);
+    p.tok_asg = reinterpret_cast<int32_t*>(b + L.tok_asg);
+    p.act_exp = reinterpret_cast<int32_t*>(b + L.act_exp);
+    p.dept_count = reinterpret_cast<int32_t*>(b + L.dept_count);
+    p.dept_off = reinterpret_cast<int32_t*>(b + L.dept_off);
+    p.dept_tok = reinterpret_cast<int32_t*>(b + L.dept_tok);
+    p.dept_w = reinterpret_cast<float*>(b + L.dept_w);
+    p.tok_dpos = reinterpret_cast<int32_t*>(b + L.tok_dpos);
+    p.act_dept = reinterpret_cast<int32_t*>(b + L.act_dept);
+    p.sync = reinterpret_cast<uint32_t*>(b + L.sync);
+    return p;
+}
+
+// Workspace check shared by every step.
+int check_ws(const void* ws, size_t ws_bytes, int T, int n, int k, int g, moe_ws_layout* L,
+             const char* who) {
+    if (!layout_of(T, n, k, g, L))
+        return fail(MOE_ERR_INVALID_ARG,
+                    "%s: need 1<=T<=%d, 1<=n<=%d, 1<=k<=min(n,%d), g>=1, n%%g==0 "
+                    "(T=%d n=%d k=%d g=%d)",
+                    who, moe::kMaxT, moe::kMaxN, moe::kMaxK, T, n, k, g);
+    if (!ws || !aligned16(ws)) return fail(MOE_ERR_INVALID_ARG, "%s: workspace null or unaligned", who);
+    if (ws_bytes < L->total)
+        return fail(MOE_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu required", who, ws_bytes,
+                    L->total);
+    return MOE_OK;
+}
+
+int weight_bytes(int dtype) { return dtype == MOE_DTYPE_BF16 ? 2 : dtype == MOE_DTYPE_F32 ? 4 : 0; }
+
+int check_hidden(const float* x, int d, const char* who) {
+    if (!x || !aligned16(x)) return fail(MOE_ERR_INVALID_ARG, "%s: x null or unaligned", who);
+    if (d < 8 || d % 8 != 0) return fail(MOE_ERR_INVALID_ARG, "%s: d=%d must be a positive multiple of 8", who, d);
+    return MOE_OK;
+}
+
+int check_unit(const void* g, const void* u, const void* dn, int rows, int d, int dtype,
+               const char* what, const char* who) {
+    if (rows <= 0 || rows % 16 != 0)
+        return fail(MOE_ERR_INVALID_ARG, "%s: %s rows=%d must be a positive multiple of 16", who, what, rows);
+    if (!g || !u || !dn || !aligned16(g) || !aligned16(u) || !aligned16(dn))
+        return fail(MOE_ERR_INVALID_ARG, "%s: %s weights null or unaligned", who, what);
+    if ((long long)d * weight_bytes(dtype) > 16384 || d > kMaxHidden)
+        return fail(MOE_ERR_UNSUPPORTED, "%s: d=%d exceeds the streaming kernel's %d (one row <= 16 KB)",
+                    who, d, kMaxHidden);
+    return MOE_OK;
+}
+
+int check_ffn_common(const float* x, int d, int dtype, int out_mode, const float* out,
+                     const char* who) {
+    int rc = check_hidden(x, d, who);
+    if (rc) return rc;
+    if (weight_bytes(dtype) == 0) return fail(MOE_ERR_UNSUPPORTED, "%s: dtype %d", who, dtype);
+    if (out_mode != MOE_OUT_ROWS && out_mode != MOE_OUT_ACCUM)
+        return fail(MOE_ERR_INVALID_ARG, "%s: out_mode %d", who, out_mode);
+    if (!out || !aligned16(out)) return fail(MOE_ERR_INVALID_ARG, "%s: out null or unaligned", who);
+    return MOE_OK;
+}
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+long long rows_count(int T, int n, int k, int g, int has_shared) {
+    const int m = g > 1 ? n / g : 0;
+    const long long dk = g > 1 ? (long long)T * (k < m ? k : m) : 0;
+    return (long long)T * k + dk + (has_shared ? T : 0);
+}
+
+int run_ffn(moe::FfnArgs& a, int T, int n, int k, int g, int has_shared, void* stream,
+            const char* who) {
+    a.rows_dept_base = T * k;
+    a.rows_shared_base = (int)rows_count(T, n, k, g, 0);
+    cudaError_t e;
+    if (a.out_mode == MOE_OUT_ROWS) {
+        const size_t bytes = (size_t)rows_count(T, n, k, g, has_shared) * a.d * sizeof(float);
+        e = moe::launch_zero(a.out, bytes, as_stream(stream));
+        if (e != cudaSuccess) return cuda_fail(e, who);
+    }
+    e = moe::launch_ffn(a, as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    return MOE_OK;
+}
+
+}  // namespace
+
+namespace moe {
+int device_sm_count() {
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    int sms = 1;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (dev >= 0 && dev < 64) cache[dev] = sms;
+    return sms;
+}
+}  // namespace moe
+
+extern "C" {
+
+int moe_version(void) { return 100; }
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+size_t moe_workspace_bytes(int T, int n, int k, int experts_per_dept) {
+    moe_ws_layout L;
+    return layout_of(T, n, k, experts_per_dept, &L) ? L.total : 0;
+}
+
+int moe_workspace_layout(int T, int n, int k, int experts_per_dept, moe_ws_layout* out) {
+    if (!out) return fail(MOE_ERR_INVALID_ARG, "moe_workspace_layout: out is null");
+    if (!layout_of(T, n, k, experts_per_dept, out))
+        return fail(MOE_ERR_INVALID_ARG, "moe_workspace_layout: invalid sizes");
+    return MOE_OK;
+}
+
+int moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+    if (!ws || !aligned16(ws)) return fail(MOE_ERR_INVALID_ARG, "moe_workspace_init: ws null or unaligned");
+    cudaError_t e = moe::launch_zero(ws, ws_bytes & ~size_t(15), as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "moe_workspace_init");
+    return MOE_OK;
+}
+
+int moe_read_status(const void* ws, size_t ws_bytes, int32_t* host_status, int32_t* host_counts,
+                    void* stream) {
+    if (!ws || ws_bytes < 512) return fail(MOE_ERR_INVALID_ARG, "moe_read_status: bad workspace");
+    int32_t buf[8];
+    // status at offset 0, counts at offset 256 (see layout_of)
+    cudaError_t e = cudaMemcpyAsync(buf, ws, 4 * sizeof(int32_t), cudaMemcpyDeviceToHost, as_stream(stream));
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(buf + 4, static_cast<const char*>(ws) + 256, 4 * sizeof(int32_t),
+                            cudaMemcpyDeviceToHost, as_stream(stream));
+    if (e == cudaSuccess) e = cudaStreamSynchronize(as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "moe_read_status");
+    if (host_status) host_status[0] = buf[0];
+    if (host_counts) {
+        host_counts[0] = buf[4];
+        host_counts[1] = buf[5];
+    }
+    return MOE_OK;
+}
+
+int moe_route_topk(const float* x, const float* w_router, const float* bias, int T, int d, int n,
+                   int k, float scale, int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes,
+                   void* stream) {
+    const char* who = "moe_route_topk";
+    moe_ws_layout L;
+    int rc = check_ws(ws, ws_bytes, T, n, k, 1, &L, who);
+    if (rc) return rc;
+    if ((rc = check_hidden(x, d, who))) return rc;
+    if (!w_router || !aligned16(w_router)) return fail(MOE_ERR_INVALID_ARG, "%s: w_router null or unaligned", who);
+    if (!topk_idx || !topk_w) return fail(MOE_ERR_INVALID_ARG, "%s: outputs are null", who);
+    moe::RouteArgs a = {};
+    a.x = x;
+    a.w_router = w_router;
+    a.bias = bias;
+    a.T = T; a.d = d; a.n = n; a.k = k;
+    a.scale = scale;
+    a.topk_idx = topk_idx;
+    a.topk_w = topk_w;
+    a.ws = resolve(ws, L);
+    a.fuse_dispatch = 0;
+    a.g = 1;
+    cudaError_t e = moe::launch_route(a, as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    return MOE_OK;
+}
+
+int moe_dispatch(const int32_t* topk_idx, const float* topk_w, int T, int n, int k,
+                 int experts_per_dept, void* ws, size_t ws_bytes, void* stream) {
+    const char* who = "moe_dispatch";
+    moe_ws_layout L;
+    int rc = check_ws(ws, ws_bytes, T, n, k, experts_per_dept, &L, who);
+    if (rc) return rc;
+    if (!topk_idx || !topk_w) return fail(MOE_ERR_INVALID_ARG, "%s: inputs are null", who);
+    moe::DispatchArgs a = {topk_idx, topk_w, T, n, k, experts_per_dept, resolve(ws, L)};
+    cudaError_t e = moe::launch_dispatch(a, as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    return MOE_OK;
+}
+
+int64_t moe_rows_count(int T, int n, int k, int experts_per_dept, int has_shared) {
+    moe_ws_layout L;
+    if (!layout_of(T, n, k, experts_per_dept, &L)) return -1;
+    return rows_count(T, n, k, experts_per_dept, has_shared);
+}
+
+static int setup_vanilla(moe::FfnArgs& a, const float* x, int T, int d, int n, int k, int I,
+                         int dtype, const void* w_gate, const void* w_up, const void* w_down,
+                         int I_s, const void* s_gate, const void* s_up, const void* s_down,
+                         const void* ws, size_t ws_bytes, int out_mode, float* out,
+                         const char* who) {
+    moe_ws_layout L;
+    int rc = check_ws(ws, ws_bytes, T, n, k, 1, &L, who);
+    if (rc) return rc;
+    if ((rc = check_ffn_common(x, d, dtype, out_mode, out, who))) return rc;
+    if ((rc = check_unit(w_gate, w_up, w_down, I, d, dtype, "expert", who))) return rc;
+    if (I_s < 0) return fail(MOE_ERR_INVALID_ARG, "%s: I_s < 0", who);
+    if (I_s > 0 && (rc = check_unit(s_gate, s_up, s_down, I_s, d, dtype, "shared expert", who))) return rc;
+    a = moe::FfnArgs{};
+    a.x = x;
+    a.T = T; a.d = d; a.n = n; a.k = k; a.g = 1;
+    a.dtype = dtype;
+    a.ncls = 0;
+    if (I_s > 0) a.cls[a.ncls++] = moe::UnitClass{s_gate, s_up, s_down, I_s, moe::kUnitShared};
+    a.cls[a.ncls++] = moe::UnitClass{w_gate, w_up, w_down, I, moe::kUnitExpert};
+    a.ws = resolve(ws, L);
+    a.out = out;
+    a.out_mode = out_mode;
+    a.pdl = 1;
+    return MOE_OK;
+}
+
+int moe_ffn_vanilla(const float* x, int T, int d, int n, int k, int I, int dtype,
+                    const void* w_gate, const void* w_up, const void* w_down, int I_s,
+                    const void* s_gate, const void* s_up, const void* s_down, const void* ws,
+                    size_t ws_bytes, int out_mode, float* out, void* stream) {
+    const char* who = "moe_ffn_vanilla";
+    moe::FfnArgs a;
+    int rc = setup_vanilla(a, x, T, d, n, k, I, dtype, w_gate, w_up, w_down, I_s, s_gate, s_up,
+                           s_down, ws, ws_bytes, out_mode, out, who);
+    if (rc) return rc;
+    return run_ffn(a, T, n, k, 1, I_s > 0, stream, who);
+}
+
+static int setup_deamoe(moe::FfnArgs& a, const float* x, int T, int d, int n, int k, int g,
+                        int I_sh, int I_pr, int dtype, const void* dept_gate, const void* dept_up,
+                        const void* dept_down, const void* priv_gate, const void* priv_up,
+                        const void* priv_down, int I_s, const void* s_gate, const void* s_up,
+                        const void* s_down, const void* ws, size_t ws_bytes, int out_mode,
+                        float* out, const char* who) {
+    moe_ws_layout L;
+    int rc = check_ws(ws, ws_bytes, T, n, k, g, &L, who);
+    if (rc) return rc;
+    if ((rc = check_ffn_common(x, d, dtype, out_mode, out, who))) return rc;
+    if ((rc = check_unit(dept_gate, dept_up, dept_down, I_sh, d, dtype, "department", who))) return rc;
+    if (I_pr < 0 || I_s < 0) return fail(MOE_ERR_INVALID_ARG, "%s: negative size", who);
+    if (I_pr > 0 && (rc = check_unit(priv_gate, priv_up, priv_down, I_pr, d, dtype, "private", who))) return rc;
+    if (I_s > 0 && (rc = check_unit(s_gate, s_up, s_down, I_s, d, dtype, "shared expert", who))) return rc;
+    a = moe::FfnArgs{};
+    a.x = x;
+    a.T = T; a.d = d; a.n = n; a.k = k; a.g = g;
+    a.dtype = dtype;
+    a.ncls = 0;
+    if (I_s > 0) a.cls[a.ncls++] = moe::UnitClass{s_gate, s_up, s_down, I_s, moe::kUnitShared};
+    // With one expert per department the department rows are the expert's own rows.
+    a.cls[a.ncls++] = moe::UnitClass{dept_gate, dept_up, dept_down, I_sh,
+                                     g > 1 ? moe::kUnitDept : moe::kUnitExpert};
+    if (I_pr > 0) a.cls[a.ncls++] = moe::UnitClass{priv_gate, priv_up, priv_down, I_pr, moe::kUnitExpert};
+    a.ws = resolve(ws, L);
+    a.out = out;
+    a.out_mode = out_mode;
+    a.pdl = 1;
+    return MOE_OK;
+}
+
+int deamoe_ffn(const float* x, int T, int d, int n, int k, int experts_per_dept, int I_sh,
+               int I_pr, int dtype, const void* dept_gate, const void* dept_up,
+               const void* dept_down, const void* priv_gate, const void* priv_up,
+               const void* priv_down, int I_s, const void* s_gate, const void* s_up,
+               const void* s_down, const void* ws, size_t ws_bytes, int out_mode, float* out,
+               void* stream) {
+    const char* who = "deamoe_ffn";
+    moe::FfnArgs a;
+    int rc = setup_deamoe(a, x, T, d, n, k, experts_per_dept, I_sh, I_pr, dtype, dept_gate, dept_up,
+                          dept_down, priv_gate, priv_up, priv_down, I_s, s_gate, s_up, s_down, ws,
+                          ws_bytes, out_mode, out, who);
+    if (rc) return rc;
+    return run_ffn(a, T, n, k, experts_per_dept, I_s > 0, stream, who);
+}
+
+int moe_combine(const float* rows, int T, int d, int n, int k, int experts_per_dept,
+                int has_shared, const void* ws, size_t ws_bytes, float* y, void* stream) {
+    const char* who = "moe_combine";
+    moe_ws_layout L;
+    int rc = check_ws(ws, ws_bytes, T, n, k, experts_per_dept, &L, who);
+    if (rc) return rc;
+    if (!rows || !aligned16(rows) || !y || !aligned16(y))
+        return fail(MOE_ERR_INVALID_ARG, "%s: rows / y null or unaligned", who);
+    if (d < 8 || d % 8) return fail(MOE_ERR_INVALID_ARG, "%s: d=%d must be a positive multiple of 8", who, d);
+    moe::CombineArgs a = {};
+    a.rows = rows;
+    a.T = T; a.d = d; a.k = k;
+    a.m = experts_per_dept > 1 ? n / experts_per_dept : 0;
+    a.has_shared = has_shared ? 1 : 0;
+    a.rows_dept_base = T * k;
+    a.rows_shared_base = (int)(rows_count(T, n, k, experts_per_dept, 0));
+    a.ws = resolve(ws, L);
+    a.y = y;
+    cudaError_t e = moe::launch_combine(a, as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    return MOE_OK;
+}
+
+static int layer_route(const float* x, int T, int d, int n, int k, float scale, const float* w_router,
+                       const float* bias, int g, const moe_ws_layout& L, void* ws, int32_t* topk_idx,
+                       float* topk_w, float* y, void* stream, const char* who) {
+    if (!w_router || !aligned16(w_router)) return fail(MOE_ERR_INVALID_ARG, "%s: w_router null or unaligned", who);
+    if (!topk_idx || !topk_w) return fail(MOE_ERR_INVALID_ARG, "%s: routing outputs are null", who);
+    moe::RouteArgs r = {};
+    r.x = x;
+    r.w_router = w_router;
+    r.bias = bias;
+    r.T = T; r.d = d; r.n = n; r.k = k;
+    r.scale = scale;
+    r.topk_idx = topk_idx;
+    r.topk_w = topk_w;
+    r.ws = resolve(ws, L);
+    r.fuse_dispatch = 1;
+    r.g = g;
+    r.y_zero = y;
+    r.y_elems = (long long)T * d;
+    cudaError_t e = moe::launch_route(r, as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    return MOE_OK;
+}
+
+int moe_layer_forward(const float* x, int T, int d, int n, int k, float scale,
+                      const float* w_router, const float* bias, int I, int dtype,
+                      const void* w_gate, const void* w_up, const void* w_down, int I_s,
+                      const void* s_gate, const void* s_up, const void* s_down, void* ws,
+                      size_t ws_bytes, int32_t* topk_idx, float* topk_w, float* y, void* stream) {
+    const char* who = "moe_layer_forward";
+    moe::FfnArgs a;
+    int rc = setup_vanilla(a, x, T, d, n, k, I, dtype, w_gate, w_up, w_down, I_s, s_gate, s_up,
+                           s_down, ws, ws_bytes, MOE_OUT_ACCUM, y, who);
+    if (rc) return rc;
+    moe_ws_layout L;
+    layout_of(T, n, k, 1, &L);
+    if ((rc = layer_route(x, T, d, n, k, scale, w_router, bias, 1, L, ws, topk_idx, topk_w, y, stream, who)))
+        return rc;
+    cudaError_t e = moe::launch_ffn(a, as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    return MOE_OK;
+}
+
+int deamoe_layer_forward(const float* x, int T, int d, int n, int k, float scale,
+                         const float* w_router, const float* bias, int experts_per_dept, int I_sh,
+                         int I_pr, int dtype, const void* dept_gate, const void* dept_up,
+                         const void* dept_down, const void* priv_gate, const void* priv_up,
+                         const void* priv_down, int I_s, const void* s_gate, const void* s_up,
+                         const void* s_down, void* ws, size_t ws_bytes, int32_t* topk_idx,
+                         float* topk_w, float* y, void* stream) {
+    const char* who = "deamoe_layer_forward";
+    moe::FfnArgs a;
+    int rc = setup_deamoe(a, x, T, d, n, k, experts_per_dept, I_sh, I_pr, dtype, dept_gate, dept_up,
+                          dept_down, priv_gate, priv_up, priv_down, I_s, s_gate, s_up, s_down, ws,
+                          ws_bytes, MOE_OUT_ACCUM, y, who);
+    if (rc) return rc;
+    moe_ws_layout L;
+    layout_of(T, n, k, experts_per_dept, &L);
+    if ((rc = layer_route(x, T, d, n, k, scale, w_router, bias, experts_per_dept, L, ws, topk_idx,
+                          topk_w, y, stream, who)))
+        return rc;
+    cudaError_t e = moe::launch_ffn(a, as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    return MOE_OK;
+}
+
+int64_t moe_unique_weight_bytes_vanilla(int d, int n, int I, int I_s, int dtype, int A_e) {
+    const int bw = weight_bytes(dtype);
+    if (d <= 0 || n <= 0 || I < 0 || I_s < 0 || bw == 0 || A_e < 0 || A_e > n) return -1;
+    return 4LL * d * n + (int64_t)bw * 3 * d * ((int64_t)A_e * I + I_s);
+}
+
+int64_t moe_unique_weight_bytes_deamoe(int d, int n, int I_sh, int I_pr, int I_s, int dtype,
+                                       int A_d, int A_e) {
+    const int bw = weight_bytes(dtype);
+    if (d <= 0 || n <= 0 || I_sh < 0 || I_pr < 0 || I_s < 0 || bw == 0 || A_d < 0 || A_e < 0 ||
+        A_e > n)
+        return -1;
+    return 4LL * d * n + (int64_t)bw * 3 * d * ((int64_t)A_d * I_sh + (int64_t)A_e * I_pr + I_s);
+}
+
+}  // extern "C"

@@ -1,0 +1,127 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and
+loads, exports every declared entry point, and rejects bad arguments before
+launching anything."""
+
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from tests.helpers import ensure_built
+from oracle import moe_oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def B():
+    return ensure_built()
+
+
+def declared_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if not f.endswith(".h"):
+            continue
+        text = open(os.path.join(inc, f)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, re.M):
+            if m.group(1) not in ("defined",):
+                names.append(m.group(1))
+    return names
+
+
+def test_library_exports_every_declared_symbol(B):
+    L = B.lib()
+    names = declared_functions()
+    assert len(names) >= 15
+    for name in names:
+        assert hasattr(L, name), f"{name} declared in include/ but not exported"
+    # and the binding covers every declared entry point
+    assert set(names) == set(B.exported_symbols())
+
+
+def test_version_and_error_string(B):
+    assert B.lib().moe_version() >= 100
+    assert isinstance(B.lib().moe_last_error(), bytes)
+
+
+def test_workspace_layout_is_ordered_and_aligned(B):
+    for (T, n, k, g) in [(1, 16, 2, 1), (4, 16, 2, 4), (16, 128, 8, 1), (128, 64, 8, 8), (64, 256, 8, 16)]:
+        L = B.moe_workspace_layout(T, n, k, g)
+        offs = [L[f] for f in B.WS_FIELDS[1:]]
+        assert offs == sorted(offs)
+        assert all(o % 256 == 0 for o in offs)
+        assert L["total"] == B.moe_workspace_bytes(T, n, k, g)
+        assert L["counts"] == 256  # documented position read by moe_read_status
+        assert L["total"] >= L["sync"] + 16
+
+
+@pytest.mark.parametrize("args", [(0, 16, 2, 1), (129, 16, 2, 1), (4, 16, 0, 1), (4, 16, 17, 1),
+                                  (4, 16, 33, 64), (4, 16, 2, 3), (4, 2048, 2, 1)])
+def test_workspace_rejects_bad_sizes(B, args):
+    assert B.lib().moe_workspace_bytes(*args) == 0
+    L = B.WsLayout()
+    assert B.lib().moe_workspace_layout(*args, C.byref(L)) == -1
+
+
+def test_calls_reject_null_and_small_workspace(B):
+    lib = B.lib()
+    # null workspace
+    rc = lib.moe_route_topk(None, None, None, 4, 256, 16, 2, 1.0, None, None, None, 0, None)
+    assert rc == -1 and b"workspace" in lib.moe_last_error()
+    # workspace too small (a fake aligned address; nothing is launched)
+    fake = 1 << 20
+    rc = lib.moe_dispatch(fake, fake, 4, 16, 2, 1, fake, 64, None)
+    assert rc == -3
+    # bad hidden size
+    need = lib.moe_workspace_bytes(4, 16, 2, 1)
+    rc = lib.moe_route_topk(fake, fake, None, 4, 12, 16, 2, 1.0, fake, fake, fake, need, None)
+    assert rc == -1 and b"d=12" in lib.moe_last_error()
+    # misaligned weights
+    rc = lib.moe_ffn_vanilla(fake, 4, 256, 16, 2, 64, 1, fake + 2, fake, fake, 0, None, None, None,
+                             fake, need, 1, fake, None)
+    assert rc == -1 and b"unaligned" in lib.moe_last_error()
+    # intermediate not a multiple of 16
+    rc = lib.moe_ffn_vanilla(fake, 4, 256, 16, 2, 40, 1, fake, fake, fake, 0, None, None, None,
+                             fake, need, 1, fake, None)
+    assert rc == -1
+    # unsupported dtype / out mode
+    rc = lib.moe_ffn_vanilla(fake, 4, 256, 16, 2, 64, 7, fake, fake, fake, 0, None, None, None,
+                             fake, need, 1, fake, None)
+    assert rc == -2
+    rc = lib.moe_ffn_vanilla(fake, 4, 256, 16, 2, 64, 1, fake, fake, fake, 0, None, None, None,
+                             fake, need, 5, fake, None)
+    assert rc == -1
+    # hidden size wider than the streaming kernel covers
+    rc = lib.moe_ffn_vanilla(fake, 4, 8192, 16, 2, 64, 1, fake, fake, fake, 0, None, None, None,
+                             fake, need, 1, fake, None)
+    assert rc == -2
+    # DeaMoE needs g >= 1 and n % g == 0
+    need4 = lib.moe_workspace_bytes(4, 16, 2, 4)
+    rc = lib.deamoe_ffn(fake, 4, 256, 16, 2, 0, 64, 16, 1, fake, fake, fake, fake, fake, fake, 0,
+                        None, None, None, fake, need4, 1, fake, None)
+    assert rc == -1
+    rc = lib.deamoe_ffn(fake, 4, 256, 16, 2, 3, 64, 16, 1, fake, fake, fake, fake, fake, fake, 0,
+                        None, None, None, fake, need4, 1, fake, None)
+    assert rc == -1
+
+
+def test_rows_count(B):
+    assert B.moe_rows_count(4, 16, 2, 1, False) == 8
+    assert B.moe_rows_count(4, 16, 2, 1, True) == 12
+    assert B.moe_rows_count(4, 16, 2, 4, False) == 8 + 8      # T*min(k,m) = 4*2
+    assert B.moe_rows_count(16, 64, 8, 8, True) == 128 + 128 + 16
+
+
+def test_unique_bytes_match_oracle_formula(B):
+    for (d, n, I, I_s, A_e) in [(2048, 128, 768, 0, 8), (7168, 256, 2048, 2048, 77), (256, 16, 576, 0, 3)]:
+        for code, bw in ((0, 4), (1, 2)):
+            assert B.moe_unique_weight_bytes_vanilla(d, n, I, I_s, code, A_e) == \
+                O.unique_bytes_vanilla(d, n, I, I_s, A_e, bw)
+    for (d, n, I_sh, I_pr, I_s, A_d, A_e) in [(2048, 64, 1024, 128, 0, 6, 8), (7168, 256, 1792, 256, 2048, 16, 200)]:
+        assert B.moe_unique_weight_bytes_deamoe(d, n, I_sh, I_pr, I_s, 1, A_d, A_e) == \
+            O.unique_bytes_deamoe_c(d, n, I_sh, I_pr, I_s, A_d, A_e, 2)
+    assert B.moe_unique_weight_bytes_vanilla(2048, 128, 768, 0, 9, 8) == -1
