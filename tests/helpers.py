@@ -93,14 +93,17 @@ def dispatch_lists(binding, ws, T, n, k, g):
     return out
 
 
-def assert_dispatch_equal(dev, ref, g):
+def assert_dispatch_equal(dev, ref, g, w_rtol=1e-7):
+    """Index lists bit-exact; weights within w_rtol (1e-7 when the device was
+    fed the oracle's fp32 weights, looser when it computed them itself)."""
     for key in ("exp_count", "exp_off", "asg_tok", "asg_slot", "tok_asg", "active_experts"):
         np.testing.assert_array_equal(dev[key], ref[key], err_msg=key)
-    np.testing.assert_allclose(dev["asg_w"], ref["asg_w"], rtol=1e-7, err_msg="asg_w")
+    np.testing.assert_allclose(dev["asg_w"], ref["asg_w"], rtol=w_rtol, err_msg="asg_w")
     if g > 1:
         for key in ("dept_count", "dept_off", "dept_tok", "tok_dpos", "active_depts"):
             np.testing.assert_array_equal(dev[key], ref[key], err_msg=key)
-        np.testing.assert_allclose(dev["dept_w"], ref["dept_w"], rtol=1e-6, err_msg="dept_w")
+        np.testing.assert_allclose(dev["dept_w"], ref["dept_w"], rtol=max(w_rtol, 1e-6),
+                                   err_msg="dept_w")
 
 
 def layer_tensors(shape: synth.LayerShape, seed: int, device: str):
