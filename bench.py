@@ -62,6 +62,8 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline sample budget")
+    p.add_argument("--tc-min-tokens", type=int, default=0,
+                   help="tokens per unit from which the tensor-core kernel runs (0 = library default)")
     return p.parse_args(argv)
 
 
@@ -219,6 +221,15 @@ class Workload:
             B.moe_layer_forward(x, s.k, 1.0, L["router"], L["bias"], L["gate"], L["up"], L["down"],
                                 self.shared(L), self.ws[key], self.idx[key], self.w[key], y)
 
+    def route_only(self, r, T):
+        L, key = self.layers[r], (r, T)
+        self.B.moe_route_topk(self.x[key], L["router"], L["bias"], self.shape.k, 1.0,
+                              self.idx[key], self.w[key], self.ws[key])
+
+    def dispatch_only(self, r, T):
+        key = (r, T)
+        self.B.moe_dispatch(self.idx[key], self.w[key], self.shape.n, self.g, self.ws[key])
+
     def ffn_only(self, r, T, out):
         s, B, L, key = self.shape, self.B, self.layers[r], (r, T)
         if s.I_sh > 0:
@@ -271,6 +282,7 @@ def time_graphs(graphs, order, world, device):
 def run_ours(args, rank, world, local):
     from moe_decode_layer_fp32_gb300 import binding as B
     B.lib()  # fails loudly when the native library is missing
+    B.moe_set_tc_min_tokens(args.tc_min_tokens)
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     shape = WORKLOADS[args.workload]
@@ -311,8 +323,17 @@ def run_ours(args, rank, world, local):
         t = time_graphs([gT], [0] * reps, world, device)
         us = t / (reps * R) * 1e6
         U = sum(W.unique[(r, T)] for r in range(R)) / R
+        # each stage alone (route+top-k, dispatch, expert FFN), as graphs over the replicas
+        stage_us = {}
+        scratch_T = {r: torch.zeros_like(W.y[(r, T)]) for r in range(R)}
+        for name, fn in (("route_topk", lambda T=T: [W.route_only(r, T) for r in range(R)]),
+                         ("dispatch", lambda T=T: [W.dispatch_only(r, T) for r in range(R)]),
+                         ("ffn", lambda T=T: [W.ffn_only(r, T, scratch_T[r]) for r in range(R)])):
+            gs = capture(fn)
+            time_graphs([gs], [0] * 3, world, device)
+            stage_us[name] = round(time_graphs([gs], [0] * reps, world, device) / (reps * R) * 1e6, 2)
         per_batch[str(T)] = {"us_per_layer": round(us, 2), "unique_MB": round(U / 1e6, 2),
-                             "GBps": round(U / us / 1e3, 1),
+                             "GBps": round(U / us / 1e3, 1), "stage_us": stage_us,
                              "active_experts": round(sum(W.counts[(r, T)][0] for r in range(R)) / R, 2)}
         if shape.I_sh > 0:
             per_batch[str(T)]["active_depts"] = round(sum(W.counts[(r, T)][1] for r in range(R)) / R, 2)
@@ -379,6 +400,7 @@ def run_ours(args, rank, world, local):
                    "n_experts": shape.n, "top_k": shape.k, "I": shape.I, "I_sh": shape.I_sh,
                    "I_pr": shape.I_pr, "experts_per_dept": shape.g, "I_shared": shape.I_s,
                    "batches": list(batches), "replicas": R,
+                   "tc_min_tokens": args.tc_min_tokens or "default",
                    "l2": "inputs larger than L2: consecutive steps use distinct layer replicas "
                          f"({R} replicas, >=4x L2 between reuses)",
                    "parallelism": f"replicas x{world}"},

@@ -66,6 +66,17 @@ int moe_version(void);
 /* Message for the last failed call on this thread ("" if none). */
 const char* moe_last_error(void);
 
+/*
+ * Tensor-core threshold of the FFN steps: a unit (expert, department or
+ * shared expert) whose gathered token count is at least min_tokens runs on the
+ * tcgen05 kernel, the others on the CUDA-core weight stream.  0 restores the
+ * library default (4); a value above every batch size keeps everything on the
+ * CUDA cores.  Process-wide; returns the previous setting (0 = default), or
+ * MOE_ERR_INVALID_ARG for a negative value.  The tensor-core kernel applies to
+ * bf16 weights with d % 128 == 0.
+ */
+int moe_set_tc_min_tokens(int min_tokens);
+
 /* ------------------------------------------------------------------------- */
 /* Workspace                                                                 */
 /* ------------------------------------------------------------------------- */
@@ -94,6 +105,10 @@ const char* moe_last_error(void);
  *   dept_w    float[T*min(k,m)] sum of the token's routing weights inside X^j
  *   tok_dpos  int32[T*m] (token, department) -> position in dept_tok, or -1
  *   act_dept  int32[m]   active departments, ascending (first A_d valid)
+ *   exp_units int32[n][4] per active expert q < A_e: {expert, first assignment,
+ *                        assignments, inclusive prefix over active experts of
+ *                        ceil(assignments / 4)} -- the FFN's work table
+ *   dept_units int32[m][4] the same per active department over X^j
  *   sync      uint32[4]  internal counters (kept at zero between calls)
  * The department arrays are present only when experts_per_dept > 1.
  */
@@ -102,6 +117,7 @@ typedef struct moe_ws_layout {
     size_t status, counts, logits;
     size_t exp_count, exp_off, asg_tok, asg_slot, asg_w, tok_asg, act_exp;
     size_t dept_count, dept_off, dept_tok, dept_w, tok_dpos, act_dept;
+    size_t exp_units, dept_units;
     size_t sync;
 } moe_ws_layout;
 

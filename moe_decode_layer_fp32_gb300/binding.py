@@ -13,7 +13,8 @@ import os
 
 import torch
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_gb300.so")
+LIB_PATH = os.environ.get("MOE_GB300_LIB") or os.path.join(
+    os.path.dirname(os.path.abspath(__file__)), "libmoe_gb300.so")
 
 MOE_OK = 0
 MOE_DTYPE_F32 = 0
@@ -26,7 +27,7 @@ ERRORS = {-1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_WOR
 
 WS_FIELDS = ("total", "status", "counts", "logits", "exp_count", "exp_off", "asg_tok",
              "asg_slot", "asg_w", "tok_asg", "act_exp", "dept_count", "dept_off", "dept_tok",
-             "dept_w", "tok_dpos", "act_dept", "sync")
+             "dept_w", "tok_dpos", "act_dept", "exp_units", "dept_units", "sync")
 
 
 class WsLayout(C.Structure):
@@ -45,6 +46,7 @@ _P, _I, _F, _SZ, _I64 = C.c_void_p, C.c_int, C.c_float, C.c_size_t, C.c_int64
 
 _SIGS = {
     "moe_version": (_I, []),
+    "moe_set_tc_min_tokens": (_I, [_I]),
     "moe_last_error": (C.c_char_p, []),
     "moe_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "moe_workspace_layout": (_I, [_I, _I, _I, _I, C.POINTER(WsLayout)]),
@@ -112,6 +114,13 @@ def _dtype_code(t) -> int:
     if t.dtype == torch.float32:
         return MOE_DTYPE_F32
     raise ValueError(f"unsupported weight dtype {t.dtype}")
+
+
+def moe_set_tc_min_tokens(min_tokens: int) -> int:
+    r = lib().moe_set_tc_min_tokens(min_tokens)
+    if r < 0:
+        raise MoeError("moe_set_tc_min_tokens", r, lib().moe_last_error().decode())
+    return r
 
 
 # ---------------------------------------------------------------- workspace

@@ -1,5 +1,7 @@
 // C ABI of the decode layer: host-side argument checks, workspace layout and
 // kernel launches.  See include/moe_decode.h for the contract of each call.
+#include <atomic>
+#include <climits>
 #include <cstdarg>
 #include <cstdio>
 #include <string>
@@ -27,6 +29,8 @@ int cuda_fail(cudaError_t e, const char* where) {
 
 // Widest hidden size the streaming FFN covers: 15 consumer warps x 2 chunks x 8 columns.
 constexpr int kMaxHidden = 15 * 32 * 2 * 8;
+// Widest hidden size the router kernel covers: 128 threads x 16 float4 chunks.
+constexpr int kMaxRouterHidden = 128 * 16 * 4;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -59,6 +63,8 @@ bool layout_of(int T, int n, int k, int g, moe_ws_layout* L) {
     L->dept_w = take((size_t)dk * sizeof(float));
     L->tok_dpos = take((size_t)T * m * sizeof(int32_t));
     L->act_dept = take((size_t)m * sizeof(int32_t));
+    L->exp_units = take((size_t)n * 4 * sizeof(int32_t));
+    L->dept_units = take((size_t)m * 4 * sizeof(int32_t));
     L->sync = take(4 * sizeof(uint32_t));
     L->total = off;
     return true;
@@ -83,6 +89,8 @@ moe::WsPtrs resolve(const void* ws, const moe_ws_layout& L) {
     p.dept_w = reinterpret_cast<float*>(b + L.dept_w);
     p.tok_dpos = reinterpret_cast<int32_t*>(b + L.tok_dpos);
     p.act_dept = reinterpret_cast<int32_t*>(b + L.act_dept);
+    p.exp_units = reinterpret_cast<int4*>(b + L.exp_units);
+    p.dept_units = reinterpret_cast<int4*>(b + L.dept_units);
     p.sync = reinterpret_cast<uint32_t*>(b + L.sync);
     return p;
 }
@@ -141,6 +149,49 @@ long long rows_count(int T, int n, int k, int g, int has_shared) {
     return (long long)T * k + dk + (has_shared ? T : 0);
 }
 
+// Minimum gathered tokens for a unit to run on the tensor cores (0 = default).
+std::atomic<int> g_tc_min_tokens{0};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// TMA descriptor of one [units * rows, d] bf16 weight tensor, 64 x 16 boxes, 128 B swizzle.
+bool encode_weight_map(CUtensorMap* map, const void* base, int units, int rows, int d) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)units * rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+    const cuuint32_t box[2] = {64, 16};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int tc_min_tokens() {
+    const int v = g_tc_min_tokens.load();
+    return v > 0 ? v : moe::kTcMinTokens;
+}
+
+// FFN step: the CUDA-core stream for units with few tokens and, when some unit
+// can reach the threshold, the tensor-core kernel for the others.
 int run_ffn(moe::FfnArgs& a, int T, int n, int k, int g, int has_shared, void* stream,
             const char* who) {
     a.rows_dept_base = T * k;
@@ -151,8 +202,31 @@ int run_ffn(moe::FfnArgs& a, int T, int n, int k, int g, int has_shared, void* s
         e = moe::launch_zero(a.out, bytes, as_stream(stream));
         if (e != cudaSuccess) return cuda_fail(e, who);
     }
+    const int mt = tc_min_tokens();
+    int units = 0;
+    for (int c = 0; c < a.ncls; ++c) units += moe::class_capacity(a.cls[c], a.n, a.g);
+    bool use_tc = a.dtype == MOE_DTYPE_BF16 && a.d % 128 == 0 && T >= mt &&
+                  moe::ffn_tc_smem_bytes(units) <= 227 * 1024;
+    moe::TcArgs t;
+    if (use_tc) {
+        t.f = a;
+        t.min_tokens = mt;
+        for (int c = 0; c < a.ncls && use_tc; ++c) {
+            const moe::UnitClass& uc = a.cls[c];
+            const int nu = moe::class_capacity(uc, a.n, a.g);
+            use_tc = encode_weight_map(&t.maps[c][0], uc.w_gate, nu, uc.rows, a.d) &&
+                     encode_weight_map(&t.maps[c][1], uc.w_up, nu, uc.rows, a.d) &&
+                     encode_weight_map(&t.maps[c][2], uc.w_down, nu, uc.rows, a.d);
+        }
+    }
+    a.max_tokens = use_tc ? mt - 1 : INT_MAX;
     e = moe::launch_ffn(a, as_stream(stream));
     if (e != cudaSuccess) return cuda_fail(e, who);
+    if (use_tc) {
+        t.f.max_tokens = a.max_tokens;
+        e = moe::launch_ffn_tc(t, as_stream(stream));
+        if (e != cudaSuccess) return cuda_fail(e, who);
+    }
     return MOE_OK;
 }
 
@@ -174,6 +248,11 @@ int device_sm_count() {
 extern "C" {
 
 int moe_version(void) { return 100; }
+
+int moe_set_tc_min_tokens(int min_tokens) {
+    if (min_tokens < 0) return fail(MOE_ERR_INVALID_ARG, "moe_set_tc_min_tokens: negative");
+    return g_tc_min_tokens.exchange(min_tokens);
+}
 
 const char* moe_last_error(void) { return g_last_error.c_str(); }
 
@@ -223,6 +302,8 @@ int moe_route_topk(const float* x, const float* w_router, const float* bias, int
     int rc = check_ws(ws, ws_bytes, T, n, k, 1, &L, who);
     if (rc) return rc;
     if ((rc = check_hidden(x, d, who))) return rc;
+    if (d > kMaxRouterHidden)
+        return fail(MOE_ERR_UNSUPPORTED, "%s: d=%d exceeds the router kernel's %d", who, d, kMaxRouterHidden);
     if (!w_router || !aligned16(w_router)) return fail(MOE_ERR_INVALID_ARG, "%s: w_router null or unaligned", who);
     if (!topk_idx || !topk_w) return fail(MOE_ERR_INVALID_ARG, "%s: outputs are null", who);
     moe::RouteArgs a = {};
@@ -404,9 +485,7 @@ int moe_layer_forward(const float* x, int T, int d, int n, int k, float scale,
     layout_of(T, n, k, 1, &L);
     if ((rc = layer_route(x, T, d, n, k, scale, w_router, bias, 1, L, ws, topk_idx, topk_w, y, stream, who)))
         return rc;
-    cudaError_t e = moe::launch_ffn(a, as_stream(stream));
-    if (e != cudaSuccess) return cuda_fail(e, who);
-    return MOE_OK;
+    return run_ffn(a, T, n, k, 1, I_s > 0, stream, who);
 }
 
 int deamoe_layer_forward(const float* x, int T, int d, int n, int k, float scale,
@@ -427,9 +506,7 @@ int deamoe_layer_forward(const float* x, int T, int d, int n, int k, float scale
     if ((rc = layer_route(x, T, d, n, k, scale, w_router, bias, experts_per_dept, L, ws, topk_idx,
                           topk_w, y, stream, who)))
         return rc;
-    cudaError_t e = moe::launch_ffn(a, as_stream(stream));
-    if (e != cudaSuccess) return cuda_fail(e, who);
-    return MOE_OK;
+    return run_ffn(a, T, n, k, experts_per_dept, I_s > 0, stream, who);
 }
 
 int64_t moe_unique_weight_bytes_vanilla(int d, int n, int I, int I_s, int dtype, int A_e) {

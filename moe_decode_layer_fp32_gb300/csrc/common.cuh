@@ -33,8 +33,14 @@ struct WsPtrs {
     float* dept_w;
     int32_t* tok_dpos;
     int32_t* act_dept;
+    int4* exp_units;    // per active expert: {expert, token offset, token count, group prefix}
+    int4* dept_units;   // per active department: same
     uint32_t* sync;
 };
+
+// Tokens per register group of the FFN kernels; a unit with M tokens is
+// processed as ceil(M / kGroupTokens) groups.
+constexpr int kGroupTokens = 4;
 
 __device__ __forceinline__ void set_status(int32_t* status, int code) {
     atomicCAS(reinterpret_cast<int*>(status), 0, code);
@@ -144,6 +150,29 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 v, float (&f)[8]) {
     }
 }
 
+// Two-wide fp32 fused multiply-add (sm_100+): returns a * b + c per lane pair.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    unsigned long long d;
+    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+        "mov.b64 ra, {%1, %2};\n\t"
+        "mov.b64 rb, {%3, %4};\n\t"
+        "mov.b64 rc, {%5, %6};\n\t"
+        "fma.rn.f32x2 %0, ra, rb, rc;\n\t}"
+        : "=l"(d)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
+    return r;
+}
+
+// 8 bf16 (one 16-byte word) -> 4 fp32 pairs (elements 2i, 2i+1), exact.
+__device__ __forceinline__ void unpack_bf16x8_f2(const uint4 v, float2 (&f)[4]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -188,4 +217,123 @@ __device__ int block_exclusive_scan(int* data, int len, int* warp_tmp) {
     return total;
 }
 
+// Reduce V values across the warp; afterwards the lanes whose low
+// (5 - log2 V) bits are zero hold the full sum of value index `vi`.
+template <int V>
+__device__ __forceinline__ float warp_reduce_spread(float (&v)[V], int lane, int& vi) {
+    int cnt = V;
+    vi = 0;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        if (cnt > 1) {
+            const int half = cnt >> 1;
+            const bool upper = (lane & off) != 0;
+#pragma unroll
+            for (int i = 0; i < V / 2; ++i) {
+                if (i < half) {
+                    const float send = upper ? v[i] : v[i + half];
+                    const float keep = upper ? v[i + half] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                }
+            }
+            if (upper) vi += half;
+            cnt = half;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+        }
+    }
+    return v[0];
+}
+
+
+// Exclusive prefix sums of three arrays at once (one pass, two barriers);
+// returns the three totals.  All NT threads of the block must call it.
+template <int NT>
+__device__ int3 block_exclusive_scan3(int* a0, int* a1, int* a2, int len, int3* warp_tmp) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (len + NT - 1) / NT;
+    const int b = min(len, tid * per), e = min(len, b + per);
+    int3 s = make_int3(0, 0, 0);
+    for (int i = b; i < e; ++i) {
+        s.x += a0[i];
+        s.y += a1[i];
+        s.z += a2[i];
+    }
+    int3 v = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int tx = __shfl_up_sync(0xffffffffu, v.x, o);
+        const int ty = __shfl_up_sync(0xffffffffu, v.y, o);
+        const int tz = __shfl_up_sync(0xffffffffu, v.z, o);
+        if (lane >= o) {
+            v.x += tx;
+            v.y += ty;
+            v.z += tz;
+        }
+    }
+    if (lane == 31) warp_tmp[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int3 x = lane < NT / 32 ? warp_tmp[lane] : make_int3(0, 0, 0);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int tx = __shfl_up_sync(0xffffffffu, x.x, o);
+            const int ty = __shfl_up_sync(0xffffffffu, x.y, o);
+            const int tz = __shfl_up_sync(0xffffffffu, x.z, o);
+            if (lane >= o) {
+                x.x += tx;
+                x.y += ty;
+                x.z += tz;
+            }
+        }
+        if (lane < NT / 32) warp_tmp[lane] = x;
+    }
+    __syncthreads();
+    int3 run = make_int3(v.x - s.x, v.y - s.y, v.z - s.z);
+    if (warp > 0) {
+        run.x += warp_tmp[warp - 1].x;
+        run.y += warp_tmp[warp - 1].y;
+        run.z += warp_tmp[warp - 1].z;
+    }
+    const int3 total = warp_tmp[NT / 32 - 1];
+    for (int i = b; i < e; ++i) {
+        const int c0 = a0[i], c1 = a1[i], c2 = a2[i];
+        a0[i] = run.x;
+        a1[i] = run.y;
+        a2[i] = run.z;
+        run.x += c0;
+        run.y += c1;
+        run.z += c2;
+    }
+    __syncthreads();
+    return total;
+}
+
+
+// One warp: keep the unit records {unit, first entry, entries, .} of src[0..A)
+// whose entry count lies in [lo, hi]; write them compacted to dst with .w =
+// inclusive prefix over the kept records of ceil(entries / gsize).  Returns
+// the number kept and the group total (same on every lane).
+__device__ __forceinline__ int filter_units_warp(const int4* src, int A, int lo, int hi, int gsize,
+                                                 int4* dst, int* total_groups) {
+    const int lane = threadIdx.x & 31;
+    int kept = 0, gsum = 0;
+    for (int b = 0; b < A; b += 32) {
+        const int q = b + lane;
+        const int4 r = q < A ? src[q] : make_int4(0, 0, 0, 0);
+        const bool keep = q < A && r.z >= lo && r.z <= hi;
+        int gi = keep ? (r.z + gsize - 1) / gsize : 0;
+        const unsigned bal = __ballot_sync(0xffffffffu, keep);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, gi, o);
+            if (lane >= o) gi += t;
+        }
+        if (keep) dst[kept + __popc(bal & ((1u << lane) - 1u))] = make_int4(r.x, r.y, r.z, gsum + gi);
+        kept += __popc(bal);
+        gsum += __shfl_sync(0xffffffffu, gi, 31);
+    }
+    *total_groups = gsum;
+    return kept;
+}
 }  // namespace moe

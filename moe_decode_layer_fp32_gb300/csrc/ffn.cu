@@ -11,14 +11,14 @@
 // of the department, so by linearity sum_i p_i W^T h = W^T h * sum_i p_i).
 //
 // How: the intermediate rows of all active units form one row space that is
-// split evenly over one CTA per SM.  A producer warp streams each CTA's rows
-// (gate, up, then down; every row is contiguous) from HBM into a 12-stage
+// split evenly over CPS CTAs per SM.  In each CTA a producer warp streams the
+// CTA's rows (gate, up, then down; every row is contiguous) from HBM into a
 // shared-memory ring with bulk copies (cp.async.bulk + mbarrier transaction
 // counts).  Consumer warps own fixed 8-column chunks of the hidden dimension:
-// the gate/up dot products are reduced across the warp and then across warps
-// with shared atomics, the SwiGLU is applied in shared memory, and the down
-// projection accumulates each thread's columns in registers.  The partial
-// output of the CTA's rows is added into the output with vector atomics.
+// gate/up dot products use packed fp32x2 FMAs, are reduced across the warp and
+// then across warps with shared atomics; the SwiGLU is applied in shared
+// memory; the down projection accumulates each thread's columns in registers.
+// The CTA's partial output is added into the output with vector atomics.
 #include <cuda_bf16.h>
 
 #include "../../include/moe_decode.h"
@@ -29,42 +29,44 @@ namespace moe {
 namespace {
 
 constexpr int kStageBytes = 16384;   // one ring slot
-constexpr int kStages = 12;          // 192 KB of weights in flight per SM
-constexpr int kMT = 4;               // tokens per group (register tile)
+constexpr int kRingBytesPerSM = 12 * kStageBytes;  // weights in flight per SM
+constexpr int kMT = kGroupTokens;    // tokens per group (register tile)
 constexpr int kSegMax = 256;         // rows per segment (gate/up/h buffers)
-constexpr int kMaxUnits = 1 + 2 * kMaxN;  // shared + two per-expert classes
 
 template <typename WT>
 struct WLoad;
 template <>
 struct WLoad<__nv_bfloat16> {
     static constexpr int kBytes = 2;
-    __device__ static __forceinline__ void load8(const char* p, float (&f)[8]) {
-        unpack_bf16x8(*reinterpret_cast<const uint4*>(p), f);
+    __device__ static __forceinline__ void load8(const char* p, float2 (&f)[4]) {
+        unpack_bf16x8_f2(*reinterpret_cast<const uint4*>(p), f);
     }
 };
 template <>
 struct WLoad<float> {
     static constexpr int kBytes = 4;
-    __device__ static __forceinline__ void load8(const char* p, float (&f)[8]) {
+    __device__ static __forceinline__ void load8(const char* p, float2 (&f)[4]) {
         const float4 a = reinterpret_cast<const float4*>(p)[0];
         const float4 b = reinterpret_cast<const float4*>(p)[1];
-        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+        f[0] = make_float2(a.x, a.y);
+        f[1] = make_float2(a.z, a.w);
+        f[2] = make_float2(b.x, b.y);
+        f[3] = make_float2(b.z, b.w);
     }
 };
 
-// Shared-memory carve-up (after the ring).
+// Shared-memory carve-up (after the ring).  The unit table is sized at launch.
+template <int NS>
 struct FfnSmem {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+    uint64_t full[NS];
+    uint64_t empty[NS];
     float gu[2][kSegMax * kMT];       // gate / up pre-activations of the segment
     float h[kSegMax * kMT];           // SwiGLU output (times the token weight)
-    int gpre[kMaxUnits];              // per class: inclusive prefix of groups
     int cls_units[3];
     int cls_groups[3];
-    int cls_off[3];                   // offset of the class's entries in gpre
-    int warp_tmp[32];
+    int cls_off[3];                   // offset of the class's records in `units`
+    // per unit: {weight index, first token entry, tokens, inclusive group prefix}
+    int4 units[1];
 };
 
 // A segment: rows [row0, row0+nrows) of one token group of one unit.
@@ -72,15 +74,9 @@ struct Seg {
     int cls, q, grp, row0, nrows;
 };
 
-__device__ __forceinline__ int unit_tokens(const FfnArgs& a, int cls, int q) {
-    const UnitClass& c = a.cls[cls];
-    if (c.kind == kUnitShared) return a.T;
-    if (c.kind == kUnitDept) return a.ws.dept_count[a.ws.act_dept[q]];
-    return a.ws.exp_count[a.ws.act_exp[q]];
-}
-
 // Next segment of [r, r_end) in the class / unit / group / row order.
-__device__ __forceinline__ bool next_seg(const FfnArgs& a, const FfnSmem& sm, long long& r,
+template <int NS>
+__device__ __forceinline__ bool next_seg(const FfnArgs& a, const FfnSmem<NS>& sm, long long& r,
                                          long long r_end, Seg& s) {
     if (r >= r_end) return false;
     long long base = 0;
@@ -93,15 +89,15 @@ __device__ __forceinline__ bool next_seg(const FfnArgs& a, const FfnSmem& sm, lo
     const long long rel = r - base;
     const int vg = (int)(rel / rows);
     const int rin = (int)(rel - (long long)vg * rows);
-    const int* gp = sm.gpre + sm.cls_off[c];
-    int lo = 0, hi = sm.cls_units[c] - 1;  // first q with gp[q] > vg
+    const int4* u = sm.units + sm.cls_off[c];
+    int lo = 0, hi = sm.cls_units[c] - 1;  // first q whose group prefix exceeds vg
     while (lo < hi) {
         const int mid = (lo + hi) >> 1;
-        if (gp[mid] > vg) hi = mid; else lo = mid + 1;
+        if (u[mid].w > vg) hi = mid; else lo = mid + 1;
     }
     s.cls = c;
     s.q = lo;
-    s.grp = vg - (lo > 0 ? gp[lo - 1] : 0);
+    s.grp = vg - (lo > 0 ? u[lo - 1].w : 0);
     s.row0 = rin;
     long long n = rows - rin;
     if (n > r_end - r) n = r_end - r;
@@ -111,39 +107,18 @@ __device__ __forceinline__ bool next_seg(const FfnArgs& a, const FfnSmem& sm, lo
     return true;
 }
 
-__device__ __forceinline__ int unit_weight_index(const FfnArgs& a, int cls, int q) {
-    const int kind = a.cls[cls].kind;
-    if (kind == kUnitShared) return 0;
-    if (kind == kUnitDept) return a.ws.act_dept[q];
-    return a.ws.act_exp[q];
-}
-
 // Tokens of a group: token id, weight and output row (ROWS or ACCUM mode).
-__device__ __forceinline__ int group_tokens(const FfnArgs& a, const Seg& s, int (&tok)[kMT],
-                                            float (&wt)[kMT], int (&orow)[kMT]) {
-    const int kind = a.cls[s.cls].kind;
-    int base, count;
-    if (kind == kUnitShared) {
-        base = 0;
-        count = a.T;
-    } else if (kind == kUnitDept) {
-        const int j = a.ws.act_dept[s.q];
-        base = a.ws.dept_off[j];
-        count = a.ws.dept_count[j];
-    } else {
-        const int e = a.ws.act_exp[s.q];
-        base = a.ws.exp_off[e];
-        count = a.ws.exp_count[e];
-    }
-    const int first = s.grp * kMT;
-    const int mg = min(kMT, count - first);
+__device__ __forceinline__ int group_tokens(const FfnArgs& a, const int4 rec, int kind, int grp,
+                                            int (&tok)[kMT], float (&wt)[kMT], int (&orow)[kMT]) {
+    const int first = grp * kMT;
+    const int mg = min(kMT, rec.z - first);
 #pragma unroll
     for (int i = 0; i < kMT; ++i) {
         tok[i] = 0;
         wt[i] = 0.0f;
         orow[i] = 0;
         if (i < mg) {
-            const int p = base + first + i;
+            const int p = rec.y + first + i;
             int t;
             float w;
             int row;
@@ -168,64 +143,35 @@ __device__ __forceinline__ int group_tokens(const FfnArgs& a, const Seg& s, int 
     return mg;
 }
 
-// Reduce V values across the warp; afterwards the lanes whose low
-// (5 - log2 V) bits are zero hold the full sum of value index `vi`.
-template <int V>
-__device__ __forceinline__ float warp_reduce_spread(float (&v)[V], int lane, int& vi) {
-    int cnt = V;
-    vi = 0;
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        if (cnt > 1) {
-            const int half = cnt >> 1;
-            const bool upper = (lane & off) != 0;
-#pragma unroll
-            for (int i = 0; i < V / 2; ++i) {
-                if (i < half) {
-                    const float send = upper ? v[i] : v[i + half];
-                    const float keep = upper ? v[i + half] : v[i];
-                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-                }
-            }
-            if (upper) vi += half;
-            cnt = half;
-        } else {
-            v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
-        }
-    }
-    return v[0];
-}
-
 template <typename WT, int NCW, int CH, int RMAX>
 struct Ffn {
-    static constexpr int kNT = (NCW + 1) * 32;
     static constexpr int kNC = NCW * 32;      // consumer threads
     static constexpr int kBw = WLoad<WT>::kBytes;
 
-    // One gate or up stage: nr rows of one matrix against MTC tokens.
-    template <int MTC>
+    // One gate or up stage: nr rows of one matrix against MTC tokens.  FULL:
+    // the stage holds RMAX rows (no row checks).
+    template <int MTC, bool FULL>
     __device__ static __forceinline__ void gu_stage(const char* stage, int nr, int row_bytes,
-                                                    int ctid, int nchunks,
-                                                    const float (&xr)[CH][kMT][8],
+                                                    const int (&coff)[CH], const bool (&cval)[CH],
+                                                    const float2 (&xr)[CH][kMT][4],
                                                     float* gu_rows, int mg, int lane) {
-        float acc[RMAX][MTC];
+        float2 acc[RMAX][MTC];
 #pragma unroll
         for (int r = 0; r < RMAX; ++r)
 #pragma unroll
-            for (int m = 0; m < MTC; ++m) acc[r][m] = 0.0f;
+            for (int m = 0; m < MTC; ++m) acc[r][m] = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int r = 0; r < RMAX; ++r) {
-            if (r < nr) {
+            if (FULL || r < nr) {
 #pragma unroll
                 for (int j = 0; j < CH; ++j) {
-                    const int c = ctid + j * kNC;
-                    if (c < nchunks) {
-                        float w8[8];
-                        WLoad<WT>::load8(stage + (size_t)r * row_bytes + (size_t)c * 8 * kBw, w8);
+                    if (cval[j]) {
+                        float2 w2[4];
+                        WLoad<WT>::load8(stage + (size_t)r * row_bytes + coff[j], w2);
 #pragma unroll
                         for (int m = 0; m < MTC; ++m)
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) acc[r][m] = fmaf(w8[e], xr[j][m][e], acc[r][m]);
+                            for (int e = 0; e < 4; ++e) acc[r][m] = ffma2(w2[e], xr[j][m][e], acc[r][m]);
                     }
                 }
             }
@@ -235,82 +181,133 @@ struct Ffn {
 #pragma unroll
         for (int r = 0; r < RMAX; ++r)
 #pragma unroll
-            for (int m = 0; m < MTC; ++m) v[r * MTC + m] = acc[r][m];
+            for (int m = 0; m < MTC; ++m) v[r * MTC + m] = acc[r][m].x + acc[r][m].y;
         int vi;
         const float sum = warp_reduce_spread<V>(v, lane, vi);
         if ((lane & (32 / V - 1)) == 0) {
             const int r = vi / MTC, m = vi - (vi / MTC) * MTC;
-            if (r < nr && m < mg) atomicAdd(&gu_rows[r * kMT + m], sum);
+            if ((FULL || r < nr) && m < mg) atomicAdd(&gu_rows[r * kMT + m], sum);
         }
     }
 
     // One down stage: y[col] += W_down[row, col] * h[row, token].
-    template <int MTC>
+    template <int MTC, bool FULL>
     __device__ static __forceinline__ void down_stage(const char* stage, int nr, int row_bytes,
-                                                      int ctid, int nchunks, const float* h_rows,
-                                                      float (&yacc)[CH][kMT][8]) {
+                                                      const int (&coff)[CH], const bool (&cval)[CH],
+                                                      const float* h_rows,
+                                                      float2 (&yacc)[CH][kMT][4]) {
 #pragma unroll
         for (int r = 0; r < RMAX; ++r) {
-            if (r < nr) {
+            if (FULL || r < nr) {
                 const float4 hv4 = *reinterpret_cast<const float4*>(h_rows + r * kMT);
                 const float hv[4] = {hv4.x, hv4.y, hv4.z, hv4.w};
 #pragma unroll
                 for (int j = 0; j < CH; ++j) {
-                    const int c = ctid + j * kNC;
-                    if (c < nchunks) {
-                        float w8[8];
-                        WLoad<WT>::load8(stage + (size_t)r * row_bytes + (size_t)c * 8 * kBw, w8);
+                    if (cval[j]) {
+                        float2 w2[4];
+                        WLoad<WT>::load8(stage + (size_t)r * row_bytes + coff[j], w2);
 #pragma unroll
-                        for (int m = 0; m < MTC; ++m)
+                        for (int m = 0; m < MTC; ++m) {
+                            const float2 hh = make_float2(hv[m], hv[m]);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) yacc[j][m][e] = fmaf(w8[e], hv[m], yacc[j][m][e]);
+                            for (int e = 0; e < 4; ++e) yacc[j][m][e] = ffma2(w2[e], hh, yacc[j][m][e]);
+                        }
                     }
                 }
             }
         }
     }
+
+    template <int MTC>
+    __device__ static __forceinline__ void gu_any(const char* st, int nr, int row_bytes,
+                                                  const int (&coff)[CH], const bool (&cval)[CH],
+                                                  const float2 (&xr)[CH][kMT][4], float* gr,
+                                                  int mg, int lane) {
+        if (nr == RMAX) gu_stage<MTC, true>(st, nr, row_bytes, coff, cval, xr, gr, mg, lane);
+        else gu_stage<MTC, false>(st, nr, row_bytes, coff, cval, xr, gr, mg, lane);
+    }
+    template <int MTC>
+    __device__ static __forceinline__ void down_any(const char* st, int nr, int row_bytes,
+                                                    const int (&coff)[CH], const bool (&cval)[CH],
+                                                    const float* hr, float2 (&yacc)[CH][kMT][4]) {
+        if (nr == RMAX) down_stage<MTC, true>(st, nr, row_bytes, coff, cval, hr, yacc);
+        else down_stage<MTC, false>(st, nr, row_bytes, coff, cval, hr, yacc);
+    }
 };
 
-template <typename WT, int NCW, int CH, int RMAX>
-__global__ void __launch_bounds__((NCW + 1) * 32, 1) ffn_stream_kernel(FfnArgs a) {
+template <typename WT, int NCW, int CH, int RMAX, int CPS>
+__global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs a) {
     using K = Ffn<WT, NCW, CH, RMAX>;
+    constexpr int NS = kRingBytesPerSM / kStageBytes / CPS;   // ring slots per CTA
+    constexpr int kNT = (NCW + 1) * 32;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char* ring = smem_raw;
-    FfnSmem& sm = *reinterpret_cast<FfnSmem*>(smem_raw + (size_t)kStages * kStageBytes);
+    FfnSmem<NS>& sm = *reinterpret_cast<FfnSmem<NS>*>(smem_raw + (size_t)NS * kStageBytes);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < NS; ++i) {
             mbar_init(&sm.full[i], 1);
             mbar_init(&sm.empty[i], NCW);
         }
         mbar_init_fence();
     }
-    for (int i = tid; i < 2 * kSegMax * kMT; i += K::kNT) (&sm.gu[0][0])[i] = 0.0f;
+    for (int i = tid; i < 2 * kSegMax * kMT; i += kNT) (&sm.gu[0][0])[i] = 0.0f;
 
     // Everything below reads what the routing / dispatch kernel wrote.
     pdl_wait_primary();
 
-    // ---- unit tables: groups per unit, prefix-summed per class ----
-    int off = 0;
-    for (int c = 0; c < a.ncls; ++c) {
-        const UnitClass& uc = a.cls[c];
-        const int units = uc.kind == kUnitShared ? 1
-                          : uc.kind == kUnitDept ? a.ws.counts[1]
-                                                 : a.ws.counts[0];
-        for (int q = tid; q < units; q += K::kNT)
-            sm.gpre[off + q] = (unit_tokens(a, c, q) + kMT - 1) / kMT;
-        __syncthreads();
-        const int total = block_exclusive_scan<K::kNT>(sm.gpre + off, units, sm.warp_tmp);
-        // exclusive -> inclusive prefix
-        for (int q = tid; q < units; q += K::kNT)
-            sm.gpre[off + q] += (unit_tokens(a, c, q) + kMT - 1) / kMT;
-        if (tid == 0) {
-            sm.cls_units[c] = units;
-            sm.cls_groups[c] = total;
-            sm.cls_off[c] = off;
+    // ---- unit table: the dispatch's per-unit records (one coalesced load), or,
+    // when units with more than max_tokens tokens go to the tensor-core kernel,
+    // the records of the remaining units with their own group prefix ----
+    if (a.max_tokens >= a.T) {
+        int off = 0;
+        for (int c = 0; c < a.ncls; ++c) {
+            const UnitClass& uc = a.cls[c];
+            const int cap = class_capacity(uc, a.n, a.g);
+            if (uc.kind == kUnitShared) {
+                if (tid == 0) sm.units[off] = make_int4(0, 0, a.T, (a.T + kMT - 1) / kMT);
+            } else {
+                const int4* src = uc.kind == kUnitDept ? a.ws.dept_units : a.ws.exp_units;
+                for (int q = tid; q < cap; q += kNT) sm.units[off + q] = src[q];
+            }
+            if (tid == 0) {
+                sm.cls_units[c] = uc.kind == kUnitShared ? 1
+                                  : uc.kind == kUnitDept ? a.ws.counts[1] : a.ws.counts[0];
+                sm.cls_off[c] = off;
+            }
+            off += cap;
         }
-        off += units;
+        __syncthreads();
+        if (tid < a.ncls) {
+            const int nu = sm.cls_units[tid];
+            sm.cls_groups[tid] = nu > 0 ? sm.units[sm.cls_off[tid] + nu - 1].w : 0;
+        }
+        __syncthreads();
+    } else {
+        if (warp == 0) {
+            int off = 0;
+            for (int c = 0; c < a.ncls; ++c) {
+                const UnitClass& uc = a.cls[c];
+                int kept, groups;
+                if (uc.kind == kUnitShared) {
+                    const bool keep = a.T <= a.max_tokens;
+                    kept = keep ? 1 : 0;
+                    groups = keep ? (a.T + kMT - 1) / kMT : 0;
+                    if (lane == 0 && keep) sm.units[off] = make_int4(0, 0, a.T, groups);
+                } else {
+                    const int4* src = uc.kind == kUnitDept ? a.ws.dept_units : a.ws.exp_units;
+                    const int A = uc.kind == kUnitDept ? a.ws.counts[1] : a.ws.counts[0];
+                    kept = filter_units_warp(src, A, 1, a.max_tokens, kMT, sm.units + off, &groups);
+                }
+                if (lane == 0) {
+                    sm.cls_units[c] = kept;
+                    sm.cls_groups[c] = groups;
+                    sm.cls_off[c] = off;
+                }
+                off += class_capacity(uc, a.n, a.g);
+            }
+        }
         __syncthreads();
     }
     long long R = 0;
@@ -331,8 +328,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) ffn_stream_kernel(FfnArgs a
             Seg s;
             bool ok = true;
             auto issue = [&](const char* src, int nr) -> bool {
-                const int slot = it % kStages;
-                const uint32_t par = ((it / kStages) & 1u) ^ 1u;
+                const int slot = it % NS;
+                const uint32_t par = ((it / NS) & 1u) ^ 1u;
                 if (!mbar_wait_bounded(&sm.empty[slot], par)) return false;
                 const uint32_t bytes = (uint32_t)nr * row_bytes;
                 mbar_arrive_expect_tx(&sm.full[slot], bytes);
@@ -342,7 +339,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) ffn_stream_kernel(FfnArgs a
             };
             while (ok && next_seg(a, sm, r, r_end, s)) {
                 const UnitClass& uc = a.cls[s.cls];
-                const size_t ubase = ((size_t)unit_weight_index(a, s.cls, s.q) * uc.rows + s.row0) *
+                const size_t ubase = ((size_t)sm.units[sm.cls_off[s.cls] + s.q].x * uc.rows + s.row0) *
                                      (size_t)row_bytes;
                 const char* g = static_cast<const char*>(uc.w_gate) + ubase;
                 const char* u = static_cast<const char*>(uc.w_up) + ubase;
@@ -357,22 +354,29 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) ffn_stream_kernel(FfnArgs a
             }
             if (!ok) set_status(a.ws.status, kDevErrTimeout);
             // Drain: every issued copy must land before the CTA may exit.
-            const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0u;
+            const uint32_t first = it > (uint32_t)NS ? it - NS : 0u;
             for (uint32_t i = first; i < it; ++i)
-                mbar_wait_bounded(&sm.full[i % kStages], (i / kStages) & 1u);
+                mbar_wait_bounded(&sm.full[i % NS], (i / NS) & 1u);
         }
         return;
     }
 
     // ===================== consumers =====================
-    const int ctid = tid;  // 0 .. kNC-1
+    int coff[CH];
+    bool cval[CH];
+#pragma unroll
+    for (int j = 0; j < CH; ++j) {
+        const int c = tid + j * K::kNC;
+        cval[j] = c < nchunks;
+        coff[j] = c * 8 * K::kBw;
+    }
     uint32_t it = 0;
     long long r = r_begin;
     Seg s;
     bool ok = true;
     auto wait_full = [&](int slot, uint32_t i) -> bool {
         if (!ok) return false;
-        if (!mbar_wait_bounded(&sm.full[slot], (i / kStages) & 1u)) {
+        if (!mbar_wait_bounded(&sm.full[slot], (i / NS) & 1u)) {
             ok = false;
             set_status(a.ws.status, kDevErrTimeout);
         }
@@ -386,25 +390,27 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) ffn_stream_kernel(FfnArgs a
     while (next_seg(a, sm, r, r_end, s)) {
         int tok[kMT], orow[kMT];
         float wt[kMT];
-        const int mg = group_tokens(a, s, tok, wt, orow);
+        const int mg = group_tokens(a, sm.units[sm.cls_off[s.cls] + s.q], a.cls[s.cls].kind, s.grp,
+                                    tok, wt, orow);
 
         // ---- phase A: gate / up dot products ----
         {
-            float xr[CH][kMT][8];
+            float2 xr[CH][kMT][4];
 #pragma unroll
             for (int j = 0; j < CH; ++j) {
-                const int c = ctid + j * K::kNC;
 #pragma unroll
                 for (int m = 0; m < kMT; ++m) {
-                    if (c < nchunks && m < mg) {
-                        const float4* xp =
-                            reinterpret_cast<const float4*>(a.x + (size_t)tok[m] * a.d + c * 8);
+                    if (cval[j] && m < mg) {
+                        const float4* xp = reinterpret_cast<const float4*>(
+                            a.x + (size_t)tok[m] * a.d + (tid + j * K::kNC) * 8);
                         const float4 lo = __ldg(xp), hi = __ldg(xp + 1);
-                        xr[j][m][0] = lo.x; xr[j][m][1] = lo.y; xr[j][m][2] = lo.z; xr[j][m][3] = lo.w;
-                        xr[j][m][4] = hi.x; xr[j][m][5] = hi.y; xr[j][m][6] = hi.z; xr[j][m][7] = hi.w;
+                        xr[j][m][0] = make_float2(lo.x, lo.y);
+                        xr[j][m][1] = make_float2(lo.z, lo.w);
+                        xr[j][m][2] = make_float2(hi.x, hi.y);
+                        xr[j][m][3] = make_float2(hi.z, hi.w);
                     } else {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) xr[j][m][e] = 0.0f;
+                        for (int e = 0; e < 4; ++e) xr[j][m][e] = make_float2(0.0f, 0.0f);
                     }
                 }
             }
@@ -412,16 +418,16 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) ffn_stream_kernel(FfnArgs a
                 const int nr = min(rps, s.nrows - rb);
 #pragma unroll 1
                 for (int mat = 0; mat < 2; ++mat) {
-                    const int slot = it % kStages;
+                    const int slot = it % NS;
                     if (wait_full(slot, it)) {
                         const char* st = reinterpret_cast<const char*>(ring + (size_t)slot * kStageBytes);
                         float* gr = &sm.gu[mat][rb * kMT];
                         if (mg == 1)
-                            K::template gu_stage<1>(st, nr, row_bytes, ctid, nchunks, xr, gr, mg, lane);
+                            K::template gu_any<1>(st, nr, row_bytes, coff, cval, xr, gr, mg, lane);
                         else if (mg == 2)
-                            K::template gu_stage<2>(st, nr, row_bytes, ctid, nchunks, xr, gr, mg, lane);
+                            K::template gu_any<2>(st, nr, row_bytes, coff, cval, xr, gr, mg, lane);
                         else
-                            K::template gu_stage<4>(st, nr, row_bytes, ctid, nchunks, xr, gr, mg, lane);
+                            K::template gu_any<4>(st, nr, row_bytes, coff, cval, xr, gr, mg, lane);
                         release(slot);
                     }
                     ++it;
@@ -432,7 +438,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) ffn_stream_kernel(FfnArgs a
         if (named_bar_or(1, K::kNC, !ok)) break;
 
         // ---- SwiGLU: h = SiLU(g) * u (times the token's weight when accumulating) ----
-        for (int i = ctid; i < s.nrows * kMT; i += K::kNC) {
+        for (int i = tid; i < s.nrows * kMT; i += K::kNC) {
             const int m = i & (kMT - 1);
             float hv = 0.0f;
             if (m < mg) {
@@ -447,25 +453,25 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) ffn_stream_kernel(FfnArgs a
         named_bar_sync(1, K::kNC);
 
         // ---- phase B: down projection into per-thread column accumulators ----
-        float yacc[CH][kMT][8];
+        float2 yacc[CH][kMT][4];
 #pragma unroll
         for (int j = 0; j < CH; ++j)
 #pragma unroll
             for (int m = 0; m < kMT; ++m)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) yacc[j][m][e] = 0.0f;
+                for (int e = 0; e < 4; ++e) yacc[j][m][e] = make_float2(0.0f, 0.0f);
         for (int rb = 0; rb < s.nrows; rb += rps) {
             const int nr = min(rps, s.nrows - rb);
-            const int slot = it % kStages;
+            const int slot = it % NS;
             if (wait_full(slot, it)) {
                 const char* st = reinterpret_cast<const char*>(ring + (size_t)slot * kStageBytes);
                 const float* hr = &sm.h[rb * kMT];
                 if (mg == 1)
-                    K::template down_stage<1>(st, nr, row_bytes, ctid, nchunks, hr, yacc);
+                    K::template down_any<1>(st, nr, row_bytes, coff, cval, hr, yacc);
                 else if (mg == 2)
-                    K::template down_stage<2>(st, nr, row_bytes, ctid, nchunks, hr, yacc);
+                    K::template down_any<2>(st, nr, row_bytes, coff, cval, hr, yacc);
                 else
-                    K::template down_stage<4>(st, nr, row_bytes, ctid, nchunks, hr, yacc);
+                    K::template down_any<4>(st, nr, row_bytes, coff, cval, hr, yacc);
                 release(slot);
             }
             ++it;
@@ -474,14 +480,16 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) ffn_stream_kernel(FfnArgs a
         // ---- add this CTA's partial rows into the output ----
 #pragma unroll
         for (int j = 0; j < CH; ++j) {
-            const int c = ctid + j * K::kNC;
-            if (c < nchunks) {
+            if (cval[j]) {
+                const int col = (tid + j * K::kNC) * 8;
 #pragma unroll
                 for (int m = 0; m < kMT; ++m) {
                     if (m < mg) {
-                        float4* dst = reinterpret_cast<float4*>(a.out + (size_t)orow[m] * a.d + c * 8);
-                        atomicAdd(dst, make_float4(yacc[j][m][0], yacc[j][m][1], yacc[j][m][2], yacc[j][m][3]));
-                        atomicAdd(dst + 1, make_float4(yacc[j][m][4], yacc[j][m][5], yacc[j][m][6], yacc[j][m][7]));
+                        float4* dst = reinterpret_cast<float4*>(a.out + (size_t)orow[m] * a.d + col);
+                        atomicAdd(dst, make_float4(yacc[j][m][0].x, yacc[j][m][0].y,
+                                                   yacc[j][m][1].x, yacc[j][m][1].y));
+                        atomicAdd(dst + 1, make_float4(yacc[j][m][2].x, yacc[j][m][2].y,
+                                                       yacc[j][m][3].x, yacc[j][m][3].y));
                     }
                 }
             }
@@ -489,21 +497,18 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) ffn_stream_kernel(FfnArgs a
     }
 }
 
-template <typename WT, int NCW, int CH, int RMAX>
+template <typename WT, int NCW, int CH, int RMAX, int CPS>
 cudaError_t launch_ffn_t(const FfnArgs& a, cudaStream_t s) {
-    auto kern = ffn_stream_kernel<WT, NCW, CH, RMAX>;
-    const size_t smem = (size_t)kStages * kStageBytes + sizeof(FfnSmem);
-    static bool configured[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    auto kern = ffn_stream_kernel<WT, NCW, CH, RMAX, CPS>;
+    constexpr int NS = kRingBytesPerSM / kStageBytes / CPS;
+    // unit table: one record per possible unit of every class
+    int units = 0;
+    for (int c = 0; c < a.ncls; ++c) units += class_capacity(a.cls[c], a.n, a.g);
+    const size_t smem = (size_t)NS * kStageBytes + sizeof(FfnSmem<NS>) + (size_t)units * sizeof(int4);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) configured[dev] = true;
-    }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(device_sm_count(), 1, 1);
+    cfg.gridDim = dim3(device_sm_count() * CPS, 1, 1);
     cfg.blockDim = dim3((NCW + 1) * 32, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -553,16 +558,30 @@ __global__ void zero_kernel(uint4* p, size_t n16) {
 
 }  // namespace
 
+// Launch shape of the bf16 kernel for d <= 2048: consumer warps, 8-column
+// chunks per thread, rows per stage, CTAs per SM.
+#ifndef MOE_CC_NCW
+#define MOE_CC_NCW 8
+#endif
+#ifndef MOE_CC_CH
+#define MOE_CC_CH 1
+#endif
+#ifndef MOE_CC_RMAX
+#define MOE_CC_RMAX 4
+#endif
+#ifndef MOE_CC_CPS
+#define MOE_CC_CPS 2
+#endif
+
 cudaError_t launch_ffn(const FfnArgs& a, cudaStream_t s) {
-    // Consumer warps x chunks per thread must cover d/8 chunks; RMAX is the
-    // most rows one 16 KB stage holds at that width.
-    // (15 consumer warps + 1 producer = 512 threads keeps a 128-register cap.)
+    // Consumer warps x chunks per thread x 8 must cover d; RMAX is the most
+    // rows one 16 KB stage holds at that width.
     if (a.dtype == MOE_DTYPE_BF16) {
-        if (a.d <= 2048) return launch_ffn_t<__nv_bfloat16, 8, 1, 4>(a, s);
-        return launch_ffn_t<__nv_bfloat16, 15, 2, 1>(a, s);
+        if (a.d <= 2048) return launch_ffn_t<__nv_bfloat16, MOE_CC_NCW, MOE_CC_CH, MOE_CC_RMAX, MOE_CC_CPS>(a, s);
+        return launch_ffn_t<__nv_bfloat16, 15, 2, 1, 1>(a, s);
     }
-    if (a.d <= 1024) return launch_ffn_t<float, 4, 1, 8>(a, s);
-    return launch_ffn_t<float, 15, 2, 1>(a, s);
+    if (a.d <= 1024) return launch_ffn_t<float, 4, 1, 8, 1>(a, s);
+    return launch_ffn_t<float, 15, 2, 1, 1>(a, s);
 }
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {

@@ -1,6 +1,7 @@
 // Host-side launchers of the decode-layer kernels (internal to the library).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -58,7 +59,24 @@ struct FfnArgs {
     int rows_dept_base;   // ROWS mode: first department row
     int rows_shared_base; // ROWS mode: first shared-expert row
     int pdl;              // launch as a programmatic dependent
+    int max_tokens;       // CUDA-core kernel: units with more tokens are skipped
 };
+
+// Capacity of a class's unit table (records the dispatch may have written).
+__host__ __device__ __forceinline__ int class_capacity(const UnitClass& c, int n, int g) {
+    return c.kind == kUnitShared ? 1 : c.kind == kUnitDept ? n / g : n;
+}
+
+// Tensor-core FFN: the FFN arguments plus one TMA descriptor per class and
+// matrix (gate, up, down) over the [units * rows, d] bf16 weight tensor.
+struct TcArgs {
+    FfnArgs f;
+    CUtensorMap maps[3][3];
+    int min_tokens;       // units with at least this many tokens
+};
+
+// Units with at least this many tokens run on the tensor cores.
+constexpr int kTcMinTokens = 4;
 
 struct CombineArgs {
     const float* rows;
@@ -72,6 +90,8 @@ struct CombineArgs {
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s);
 cudaError_t launch_ffn(const FfnArgs& a, cudaStream_t s);
+cudaError_t launch_ffn_tc(const TcArgs& a, cudaStream_t s);
+size_t ffn_tc_smem_bytes(int units);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
 cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t s);
 

@@ -17,17 +17,18 @@ namespace moe {
 
 namespace {
 
-constexpr int kRouteWarps = 4;
-constexpr int kRouteThreads = kRouteWarps * 32;
-constexpr int kDispatchThreads = 256;
+constexpr int kRouteThreads = 512;
+constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kDispatchThreads = 512;
 constexpr int kMaskWords = (kMaxT + 31) / 32;
 
 struct DispatchSmem {
     uint32_t emask[kMaxN * kMaskWords];       // expert -> token bitmask
     uint32_t dmask[(kMaxN / 2) * kMaskWords]; // department -> token bitmask
-    int cnt[kMaxN + 1];
-    int act[kMaxN + 1];
-    int warp_tmp[32];
+    int cnt[kMaxN];                           // tokens per unit -> offsets
+    int act[kMaxN];                           // active flag -> active position
+    int grp[kMaxN];                           // register groups -> group prefix
+    int3 warp_tmp[32];
     int err;
 };
 
@@ -36,6 +37,38 @@ __device__ __forceinline__ int mask_rank(const uint32_t* row, int t) {
     int r = __popc(row[t >> 5] & ((1u << (t & 31)) - 1u));
     for (int w = 0; w < (t >> 5); ++w) r += __popc(row[w]);
     return r;
+}
+
+// Counts of `units` mask rows -> offsets, active lists and the FFN unit records.
+template <int NT>
+__device__ void unit_lists(const uint32_t* mask, int units, int W, int32_t* count_out,
+                           int32_t* off_out, int32_t* act_out, int4* rec_out, int32_t* n_active,
+                           DispatchSmem& sm) {
+    const int tid = threadIdx.x;
+    for (int u = tid; u < units; u += NT) {
+        int c = 0;
+        for (int w = 0; w < W; ++w) c += __popc(mask[u * W + w]);
+        sm.cnt[u] = c;
+        sm.act[u] = c > 0 ? 1 : 0;
+        sm.grp[u] = (c + kGroupTokens - 1) / kGroupTokens;
+        count_out[u] = c;
+    }
+    __syncthreads();
+    const int3 tot = block_exclusive_scan3<NT>(sm.cnt, sm.act, sm.grp, units, sm.warp_tmp);
+    for (int u = tid; u < units; u += NT) {
+        off_out[u] = sm.cnt[u];
+        const int next_act = u + 1 < units ? sm.act[u + 1] : tot.y;
+        if (next_act != sm.act[u]) {  // active
+            const int next_grp = u + 1 < units ? sm.grp[u + 1] : tot.z;
+            const int next_off = u + 1 < units ? sm.cnt[u + 1] : tot.x;
+            act_out[sm.act[u]] = u;
+            rec_out[sm.act[u]] = make_int4(u, sm.cnt[u], next_off - sm.cnt[u], next_grp);
+        }
+    }
+    if (tid == 0) {
+        off_out[units] = tot.x;
+        *n_active = tot.y;
+    }
 }
 
 // Builds every dispatch list in the workspace.  One block, NT threads.
@@ -70,25 +103,8 @@ __device__ void dispatch_block(const int32_t* idx, const float* wts, int T, int 
         return;
     }
     // ---- experts ----
-    for (int e = tid; e < n; e += NT) {
-        int c = 0;
-        for (int w = 0; w < W; ++w) c += __popc(sm.emask[e * W + w]);
-        sm.cnt[e] = c;
-        sm.act[e] = c > 0 ? 1 : 0;
-        ws.exp_count[e] = c;
-    }
-    __syncthreads();
-    const int total = block_exclusive_scan<NT>(sm.cnt, n, sm.warp_tmp);
-    const int A_e = block_exclusive_scan<NT>(sm.act, n, sm.warp_tmp);
-    for (int e = tid; e < n; e += NT) {
-        ws.exp_off[e] = sm.cnt[e];
-        const bool active = (e + 1 < n ? sm.act[e + 1] : A_e) != sm.act[e];
-        if (active) ws.act_exp[sm.act[e]] = e;
-    }
-    if (tid == 0) {
-        ws.exp_off[n] = total;
-        ws.counts[0] = A_e;
-    }
+    unit_lists<NT>(sm.emask, n, W, ws.exp_count, ws.exp_off, ws.act_exp, ws.exp_units,
+                   &ws.counts[0], sm);
     for (int a = tid; a < TK; a += NT) {
         const int t = a / k;
         const int e = idx[a];
@@ -112,25 +128,8 @@ __device__ void dispatch_block(const int32_t* idx, const float* wts, int T, int 
         sm.dmask[i] = v;
     }
     __syncthreads();
-    for (int j = tid; j < m; j += NT) {
-        int c = 0;
-        for (int w = 0; w < W; ++w) c += __popc(sm.dmask[j * W + w]);
-        sm.cnt[j] = c;
-        sm.act[j] = c > 0 ? 1 : 0;
-        ws.dept_count[j] = c;
-    }
-    __syncthreads();
-    const int dtotal = block_exclusive_scan<NT>(sm.cnt, m, sm.warp_tmp);
-    const int A_d = block_exclusive_scan<NT>(sm.act, m, sm.warp_tmp);
-    for (int j = tid; j < m; j += NT) {
-        ws.dept_off[j] = sm.cnt[j];
-        const bool active = (j + 1 < m ? sm.act[j + 1] : A_d) != sm.act[j];
-        if (active) ws.act_dept[sm.act[j]] = j;
-    }
-    if (tid == 0) {
-        ws.dept_off[m] = dtotal;
-        ws.counts[1] = A_d;
-    }
+    unit_lists<NT>(sm.dmask, m, W, ws.dept_count, ws.dept_off, ws.act_dept, ws.dept_units,
+                   &ws.counts[1], sm);
     for (int i = tid; i < m * T; i += NT) {
         const int j = i / T, t = i - (i / T) * T;
         const uint32_t* row = &sm.dmask[j * W];
@@ -224,12 +223,22 @@ __device__ void topk_warp(const float* logits_row, const float* bias, int n, int
     if (bad && lane == 0) set_status(status, kDevErrRouting);
 }
 
-// Router logits: warp w of block b computes expert b*4+w for every token.
-// The last block to finish picks the top-k of every token and, on the
-// whole-layer path, builds the dispatch lists.
 template <int J>
+__device__ __forceinline__ void topk_rows(const RouteArgs& a, int warp) {
+    for (int t = warp; t < a.T; t += kRouteWarps)
+        topk_warp<J>(a.ws.logits + (size_t)t * a.n, a.bias, a.n, a.k, a.scale,
+                     a.topk_idx + (size_t)t * a.k, a.topk_w + (size_t)t * a.k, a.ws.status);
+}
+
+// Router logits: block e computes expert e's logit for every token; each
+// thread holds RCH float4 chunks of the router row, all loaded up front so
+// the row arrives in one memory round trip.  The last block to finish picks
+// the top-k of every token (one warp per token) and, on the whole-layer path,
+// builds the dispatch lists.
+template <int RCH>
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
     __shared__ DispatchSmem sm;
+    __shared__ float red[kRouteWarps][8];
     __shared__ int s_last;
     // Let the FFN grid (launched as a programmatic dependent) start its prologue.
     pdl_allow_dependents();
@@ -243,44 +252,59 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
             y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 
-    const int e = blockIdx.x * kRouteWarps + warp;
-    if (e < a.n) {
-        const float4* wr = reinterpret_cast<const float4*>(a.w_router + (size_t)e * a.d);
-        const int d4 = a.d >> 2;
-        for (int t0 = 0; t0 < a.T; t0 += 8) {
-            float acc[8];
+    const int e = blockIdx.x;
+    const int d4 = a.d >> 2;
+    const float4* wr = reinterpret_cast<const float4*>(a.w_router + (size_t)e * a.d);
+    float4 w[RCH];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-            for (int c = lane; c < d4; c += 32) {
-                const float4 wv = __ldg(wr + c);
+    for (int i = 0; i < RCH; ++i) {
+        const int c = tid + i * kRouteThreads;
+        w[i] = c < d4 ? __ldg(wr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int t0 = 0; t0 < a.T; t0 += 8) {
+        float acc[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    if (t0 + i < a.T) {
-                        const float4 xv =
-                            __ldg(reinterpret_cast<const float4*>(a.x + (size_t)(t0 + i) * a.d) + c);
-                        acc[i] = fmaf(wv.x, xv.x, acc[i]);
-                        acc[i] = fmaf(wv.y, xv.y, acc[i]);
-                        acc[i] = fmaf(wv.z, xv.z, acc[i]);
-                        acc[i] = fmaf(wv.w, xv.w, acc[i]);
+        for (int q = 0; q < 8; ++q) {
+            acc[q] = 0.f;
+            if (t0 + q < a.T) {
+                const float4* xr = reinterpret_cast<const float4*>(a.x + (size_t)(t0 + q) * a.d);
+#pragma unroll
+                for (int i = 0; i < RCH; ++i) {
+                    const int c = tid + i * kRouteThreads;
+                    if (c < d4) {
+                        const float4 xv = __ldg(xr + c);
+                        acc[q] = fmaf(w[i].x, xv.x, acc[q]);
+                        acc[q] = fmaf(w[i].y, xv.y, acc[q]);
+                        acc[q] = fmaf(w[i].z, xv.z, acc[q]);
+                        acc[q] = fmaf(w[i].w, xv.w, acc[q]);
                     }
                 }
             }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float v = warp_sum(acc[i]);
-                if (lane == 0 && t0 + i < a.T) a.ws.logits[(size_t)(t0 + i) * a.n + e] = v;
-            }
         }
+        int vi;
+        const float v = warp_reduce_spread<8>(acc, lane, vi);
+        if ((lane & 3) == 0) red[warp][vi] = v;
+        __syncthreads();
+        if (tid < 8 && t0 + tid < a.T) {
+            float s = 0.f;
+#pragma unroll
+            for (int w_ = 0; w_ < kRouteWarps; ++w_) s += red[w_][tid];
+            a.ws.logits[(size_t)(t0 + tid) * a.n + e] = s;
+        }
+        __syncthreads();
     }
     __threadfence();
-    __syncthreads();
     if (tid == 0) s_last = atomicAdd(&a.ws.sync[0], 1u) == gridDim.x - 1;
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    for (int t = warp; t < a.T; t += kRouteWarps)
-        topk_warp<J>(a.ws.logits + (size_t)t * a.n, a.bias, a.n, a.k, a.scale,
-                     a.topk_idx + (size_t)t * a.k, a.topk_w + (size_t)t * a.k, a.ws.status);
+    const int J = (a.n + 31) / 32;
+    if (J <= 1) topk_rows<1>(a, warp);
+    else if (J <= 2) topk_rows<2>(a, warp);
+    else if (J <= 4) topk_rows<4>(a, warp);
+    else if (J <= 8) topk_rows<8>(a, warp);
+    else if (J <= 16) topk_rows<16>(a, warp);
+    else topk_rows<32>(a, warp);
     if (tid == 0) a.ws.sync[0] = 0u;  // ready for the next call
     if (a.fuse_dispatch) {
         __syncthreads();
@@ -296,14 +320,12 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
 }  // namespace
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
-    const int blocks = (a.n + kRouteWarps - 1) / kRouteWarps;
-    const int J = (a.n + 31) / 32;
-    if (J <= 1) route_kernel<1><<<blocks, kRouteThreads, 0, s>>>(a);
-    else if (J <= 2) route_kernel<2><<<blocks, kRouteThreads, 0, s>>>(a);
-    else if (J <= 4) route_kernel<4><<<blocks, kRouteThreads, 0, s>>>(a);
-    else if (J <= 8) route_kernel<8><<<blocks, kRouteThreads, 0, s>>>(a);
-    else if (J <= 16) route_kernel<16><<<blocks, kRouteThreads, 0, s>>>(a);
-    else route_kernel<32><<<blocks, kRouteThreads, 0, s>>>(a);
+    // float4 chunks of a router row per thread: ceil(d / 4 / threads)
+    const int rch = (a.d / 4 + kRouteThreads - 1) / kRouteThreads;
+    const int blocks = a.n;
+    if (rch <= 1) route_kernel<1><<<blocks, kRouteThreads, 0, s>>>(a);
+    else if (rch <= 2) route_kernel<2><<<blocks, kRouteThreads, 0, s>>>(a);
+    else route_kernel<4><<<blocks, kRouteThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 

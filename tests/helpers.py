@@ -79,6 +79,7 @@ def dispatch_lists(binding, ws, T, n, k, g):
         "tok_asg": arr("tok_asg", T * k, torch.int32).reshape(T, k),
     }
     out["active_experts"] = arr("act_exp", n, torch.int32)[: out["A_e"]]
+    out["exp_units"] = arr("exp_units", 4 * n, torch.int32).reshape(n, 4)[: out["A_e"]]
     if g > 1:
         m = n // g
         D = int(arr("dept_off", m + 1, torch.int32)[m])
@@ -90,7 +91,19 @@ def dispatch_lists(binding, ws, T, n, k, g):
             "tok_dpos": arr("tok_dpos", T * m, torch.int32).reshape(T, m),
         })
         out["active_depts"] = arr("act_dept", m, torch.int32)[: out["A_d"]]
+        out["dept_units"] = arr("dept_units", 4 * m, torch.int32).reshape(m, 4)[: out["A_d"]]
     return out
+
+
+def unit_records(active, off, count, group=4):
+    """Expected FFN work records: {unit, first entry, entries, inclusive
+    prefix of ceil(entries / group)} per active unit, ascending."""
+    rec, run = [], 0
+    for u in active:
+        c = int(count[u])
+        run += -(-c // group)
+        rec.append([int(u), int(off[u]), c, run])
+    return np.array(rec, np.int32).reshape(-1, 4)
 
 
 def assert_dispatch_equal(dev, ref, g, w_rtol=1e-7):
@@ -99,9 +112,16 @@ def assert_dispatch_equal(dev, ref, g, w_rtol=1e-7):
     for key in ("exp_count", "exp_off", "asg_tok", "asg_slot", "tok_asg", "active_experts"):
         np.testing.assert_array_equal(dev[key], ref[key], err_msg=key)
     np.testing.assert_allclose(dev["asg_w"], ref["asg_w"], rtol=w_rtol, err_msg="asg_w")
+    np.testing.assert_array_equal(
+        dev["exp_units"], unit_records(ref["active_experts"], ref["exp_off"], ref["exp_count"]),
+        err_msg="exp_units")
     if g > 1:
         for key in ("dept_count", "dept_off", "dept_tok", "tok_dpos", "active_depts"):
             np.testing.assert_array_equal(dev[key], ref[key], err_msg=key)
+        np.testing.assert_array_equal(
+            dev["dept_units"],
+            unit_records(ref["active_depts"], ref["dept_off"], ref["dept_count"]),
+            err_msg="dept_units")
         np.testing.assert_allclose(dev["dept_w"], ref["dept_w"], rtol=max(w_rtol, 1e-6),
                                    err_msg="dept_w")
 
