@@ -70,10 +70,10 @@ const char* moe_last_error(void);
  * Tensor-core threshold of the FFN steps: a unit (expert, department or
  * shared expert) whose gathered token count is at least min_tokens runs on the
  * tcgen05 kernel, the others on the CUDA-core weight stream.  0 restores the
- * library default (4); a value above every batch size keeps everything on the
- * CUDA cores.  Process-wide; returns the previous setting (0 = default), or
+ * library default (every unit on the CUDA cores); a value above every batch
+ * size does the same.  Process-wide; returns the previous setting (0 = default), or
  * MOE_ERR_INVALID_ARG for a negative value.  The tensor-core kernel applies to
- * bf16 weights with d % 128 == 0.
+ * bf16 weights with d % 128 == 0 and unit row counts that are multiples of 128.
  */
 int moe_set_tc_min_tokens(int min_tokens);
 
@@ -110,6 +110,8 @@ int moe_set_tc_min_tokens(int min_tokens);
  *                        ceil(assignments / 4)} -- the FFN's work table
  *   dept_units int32[m][4] the same per active department over X^j
  *   sync      uint32[4]  internal counters (kept at zero between calls)
+ *   xb        bf16[2][T][8192] activations split as x = hi + lo (scratch of the
+ *                        tensor-core FFN; rows packed at the call's d)
  * The department arrays are present only when experts_per_dept > 1.
  */
 typedef struct moe_ws_layout {
@@ -119,6 +121,7 @@ typedef struct moe_ws_layout {
     size_t dept_count, dept_off, dept_tok, dept_w, tok_dpos, act_dept;
     size_t exp_units, dept_units;
     size_t sync;
+    size_t xb;
 } moe_ws_layout;
 
 /* Required workspace bytes; 0 on invalid arguments.  T, n, k as for routing;

@@ -27,7 +27,7 @@ ERRORS = {-1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_WOR
 
 WS_FIELDS = ("total", "status", "counts", "logits", "exp_count", "exp_off", "asg_tok",
              "asg_slot", "asg_w", "tok_asg", "act_exp", "dept_count", "dept_off", "dept_tok",
-             "dept_w", "tok_dpos", "act_dept", "exp_units", "dept_units", "sync")
+             "dept_w", "tok_dpos", "act_dept", "exp_units", "dept_units", "sync", "xb")
 
 
 class WsLayout(C.Structure):

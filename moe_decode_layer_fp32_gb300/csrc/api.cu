@@ -66,6 +66,7 @@ bool layout_of(int T, int n, int k, int g, moe_ws_layout* L) {
     L->exp_units = take((size_t)n * 4 * sizeof(int32_t));
     L->dept_units = take((size_t)m * 4 * sizeof(int32_t));
     L->sync = take(4 * sizeof(uint32_t));
+    L->xb = take((size_t)2 * T * moe::kMaxXbHidden * 2);
     L->total = off;
     return true;
 }
@@ -92,6 +93,7 @@ moe::WsPtrs resolve(const void* ws, const moe_ws_layout& L) {
     p.exp_units = reinterpret_cast<int4*>(b + L.exp_units);
     p.dept_units = reinterpret_cast<int4*>(b + L.dept_units);
     p.sync = reinterpret_cast<uint32_t*>(b + L.sync);
+    p.xb = reinterpret_cast<__nv_bfloat16*>(b + L.xb);
     return p;
 }
 
@@ -172,15 +174,17 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// TMA descriptor of one [units * rows, d] bf16 weight tensor, 64 x 16 boxes, 128 B swizzle.
+// TMA descriptor of one [units * rows, d] bf16 weight tensor viewed as 3-D
+// {64 columns, rows, d / 64 column chunks}; boxes of 64 x kTcBoxRows x 2
+// (256 contiguous bytes of each row per op), 128 B swizzle.
 bool encode_weight_map(CUtensorMap* map, const void* base, int units, int rows, int d) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)units * rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
-    const cuuint32_t box[2] = {64, 16};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+    const cuuint64_t dims[3] = {64, (cuuint64_t)units * rows, (cuuint64_t)(d / 64)};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, 128};
+    const cuuint32_t box[3] = {64, (cuuint32_t)moe::kTcBoxRows, 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -190,10 +194,36 @@ int tc_min_tokens() {
     return v > 0 ? v : moe::kTcMinTokens;
 }
 
-// FFN step: the CUDA-core stream for units with few tokens and, when some unit
-// can reach the threshold, the tensor-core kernel for the others.
-int run_ffn(moe::FfnArgs& a, int T, int n, int k, int g, int has_shared, void* stream,
-            const char* who) {
+// Whether the tensor-core kernel takes part in this FFN step, and its TMA
+// descriptors: bf16 weights, d a multiple of 128, and a batch large enough for
+// some unit to reach the token threshold.
+bool prepare_tc(const moe::FfnArgs& a, int T, moe::TcArgs* t) {
+    const int mt = tc_min_tokens();
+    int units = 0;
+    for (int c = 0; c < a.ncls; ++c) units += moe::class_capacity(a.cls[c], a.n, a.g);
+    if (a.dtype != MOE_DTYPE_BF16 || a.d % moe::kTcHiddenQuantum != 0 || a.d > moe::kMaxXbHidden || T < mt ||
+        moe::ffn_tc_smem_bytes(units) > 227 * 1024)
+        return false;
+    for (int c = 0; c < a.ncls; ++c)
+        if (a.cls[c].rows % moe::kTcBoxRows != 0) return false;
+    t->f = a;
+    t->min_tokens = mt;
+    for (int c = 0; c < a.ncls; ++c) {
+        const moe::UnitClass& uc = a.cls[c];
+        const int nu = moe::class_capacity(uc, a.n, a.g);
+        if (!encode_weight_map(&t->maps[c][0], uc.w_gate, nu, uc.rows, a.d) ||
+            !encode_weight_map(&t->maps[c][1], uc.w_up, nu, uc.rows, a.d) ||
+            !encode_weight_map(&t->maps[c][2], uc.w_down, nu, uc.rows, a.d))
+            return false;
+    }
+    return true;
+}
+
+// FFN step: the CUDA-core stream for units with few tokens and, when `tc`, the
+// tensor-core kernel for the others.  x_split: ws.xb already holds the split
+// activations (the whole-layer path writes it in the routing kernel).
+int run_ffn(moe::FfnArgs& a, int T, int n, int k, int g, int has_shared, bool tc,
+            moe::TcArgs& t, bool x_split, void* stream, const char* who) {
     a.rows_dept_base = T * k;
     a.rows_shared_base = (int)rows_count(T, n, k, g, 0);
     cudaError_t e;
@@ -202,28 +232,15 @@ int run_ffn(moe::FfnArgs& a, int T, int n, int k, int g, int has_shared, void* s
         e = moe::launch_zero(a.out, bytes, as_stream(stream));
         if (e != cudaSuccess) return cuda_fail(e, who);
     }
-    const int mt = tc_min_tokens();
-    int units = 0;
-    for (int c = 0; c < a.ncls; ++c) units += moe::class_capacity(a.cls[c], a.n, a.g);
-    bool use_tc = a.dtype == MOE_DTYPE_BF16 && a.d % 128 == 0 && T >= mt &&
-                  moe::ffn_tc_smem_bytes(units) <= 227 * 1024;
-    moe::TcArgs t;
-    if (use_tc) {
-        t.f = a;
-        t.min_tokens = mt;
-        for (int c = 0; c < a.ncls && use_tc; ++c) {
-            const moe::UnitClass& uc = a.cls[c];
-            const int nu = moe::class_capacity(uc, a.n, a.g);
-            use_tc = encode_weight_map(&t.maps[c][0], uc.w_gate, nu, uc.rows, a.d) &&
-                     encode_weight_map(&t.maps[c][1], uc.w_up, nu, uc.rows, a.d) &&
-                     encode_weight_map(&t.maps[c][2], uc.w_down, nu, uc.rows, a.d);
-        }
+    if (tc && !x_split) {
+        e = moe::launch_split_x(a.x, (long long)T * a.d, a.ws.xb, as_stream(stream));
+        if (e != cudaSuccess) return cuda_fail(e, who);
     }
-    a.max_tokens = use_tc ? mt - 1 : INT_MAX;
+    a.max_tokens = tc ? t.min_tokens - 1 : INT_MAX;
     e = moe::launch_ffn(a, as_stream(stream));
     if (e != cudaSuccess) return cuda_fail(e, who);
-    if (use_tc) {
-        t.f.max_tokens = a.max_tokens;
+    if (tc) {
+        t.f = a;
         e = moe::launch_ffn_tc(t, as_stream(stream));
         if (e != cudaSuccess) return cuda_fail(e, who);
     }
@@ -376,7 +393,9 @@ int moe_ffn_vanilla(const float* x, int T, int d, int n, int k, int I, int dtype
     int rc = setup_vanilla(a, x, T, d, n, k, I, dtype, w_gate, w_up, w_down, I_s, s_gate, s_up,
                            s_down, ws, ws_bytes, out_mode, out, who);
     if (rc) return rc;
-    return run_ffn(a, T, n, k, 1, I_s > 0, stream, who);
+    moe::TcArgs t;
+    const bool tc = prepare_tc(a, T, &t);
+    return run_ffn(a, T, n, k, 1, I_s > 0, tc, t, false, stream, who);
 }
 
 static int setup_deamoe(moe::FfnArgs& a, const float* x, int T, int d, int n, int k, int g,
@@ -422,7 +441,9 @@ int deamoe_ffn(const float* x, int T, int d, int n, int k, int experts_per_dept,
                           dept_down, priv_gate, priv_up, priv_down, I_s, s_gate, s_up, s_down, ws,
                           ws_bytes, out_mode, out, who);
     if (rc) return rc;
-    return run_ffn(a, T, n, k, experts_per_dept, I_s > 0, stream, who);
+    moe::TcArgs t;
+    const bool tc = prepare_tc(a, T, &t);
+    return run_ffn(a, T, n, k, experts_per_dept, I_s > 0, tc, t, false, stream, who);
 }
 
 int moe_combine(const float* rows, int T, int d, int n, int k, int experts_per_dept,
@@ -450,7 +471,7 @@ int moe_combine(const float* rows, int T, int d, int n, int k, int experts_per_d
 
 static int layer_route(const float* x, int T, int d, int n, int k, float scale, const float* w_router,
                        const float* bias, int g, const moe_ws_layout& L, void* ws, int32_t* topk_idx,
-                       float* topk_w, float* y, void* stream, const char* who) {
+                       float* topk_w, float* y, bool split_x, void* stream, const char* who) {
     if (!w_router || !aligned16(w_router)) return fail(MOE_ERR_INVALID_ARG, "%s: w_router null or unaligned", who);
     if (!topk_idx || !topk_w) return fail(MOE_ERR_INVALID_ARG, "%s: routing outputs are null", who);
     moe::RouteArgs r = {};
@@ -466,6 +487,7 @@ static int layer_route(const float* x, int T, int d, int n, int k, float scale, 
     r.g = g;
     r.y_zero = y;
     r.y_elems = (long long)T * d;
+    r.split_x = split_x ? 1 : 0;
     cudaError_t e = moe::launch_route(r, as_stream(stream));
     if (e != cudaSuccess) return cuda_fail(e, who);
     return MOE_OK;
@@ -483,9 +505,12 @@ int moe_layer_forward(const float* x, int T, int d, int n, int k, float scale,
     if (rc) return rc;
     moe_ws_layout L;
     layout_of(T, n, k, 1, &L);
-    if ((rc = layer_route(x, T, d, n, k, scale, w_router, bias, 1, L, ws, topk_idx, topk_w, y, stream, who)))
+    moe::TcArgs t;
+    const bool tc = prepare_tc(a, T, &t);
+    if ((rc = layer_route(x, T, d, n, k, scale, w_router, bias, 1, L, ws, topk_idx, topk_w, y, tc,
+                          stream, who)))
         return rc;
-    return run_ffn(a, T, n, k, 1, I_s > 0, stream, who);
+    return run_ffn(a, T, n, k, 1, I_s > 0, tc, t, true, stream, who);
 }
 
 int deamoe_layer_forward(const float* x, int T, int d, int n, int k, float scale,
@@ -503,10 +528,12 @@ int deamoe_layer_forward(const float* x, int T, int d, int n, int k, float scale
     if (rc) return rc;
     moe_ws_layout L;
     layout_of(T, n, k, experts_per_dept, &L);
+    moe::TcArgs t;
+    const bool tc = prepare_tc(a, T, &t);
     if ((rc = layer_route(x, T, d, n, k, scale, w_router, bias, experts_per_dept, L, ws, topk_idx,
-                          topk_w, y, stream, who)))
+                          topk_w, y, tc, stream, who)))
         return rc;
-    return run_ffn(a, T, n, k, experts_per_dept, I_s > 0, stream, who);
+    return run_ffn(a, T, n, k, experts_per_dept, I_s > 0, tc, t, true, stream, who);
 }
 
 int64_t moe_unique_weight_bytes_vanilla(int d, int n, int I, int I_s, int dtype, int A_e) {

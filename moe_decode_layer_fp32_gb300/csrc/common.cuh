@@ -36,7 +36,41 @@ struct WsPtrs {
     int4* exp_units;    // per active expert: {expert, token offset, token count, group prefix}
     int4* dept_units;   // per active department: same
     uint32_t* sync;
+    __nv_bfloat16* xb;  // [2][T][d] activations as bf16 hi, lo (x = hi + lo)
 };
+
+// Widest hidden size the activation split buffer holds.
+constexpr int kMaxXbHidden = 8192;
+
+// x -> (hi, lo) bf16 with hi = bf16(x), lo = bf16(x - hi): 8 elements.
+__device__ __forceinline__ void split_bf16x8(const float4 a, const float4 b, uint4& hi, uint4& lo) {
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * i]), h1 = __float2bfloat16_rn(v[2 * i + 1]);
+        const __nv_bfloat16 l0 = __float2bfloat16_rn(v[2 * i] - __bfloat162float(h0));
+        const __nv_bfloat16 l1 = __float2bfloat16_rn(v[2 * i + 1] - __bfloat162float(h1));
+        h[i] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+        l[i] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// Grid-stride split of x[T*d] into ws.xb (hi rows, then lo rows).
+__device__ __forceinline__ void split_activations(const float* x, long long elems, __nv_bfloat16* xb,
+                                                  long long tid0, long long stride) {
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    uint4* hi = reinterpret_cast<uint4*>(xb);
+    uint4* lo = reinterpret_cast<uint4*>(xb + elems);
+    for (long long i = tid0; i < elems / 8; i += stride) {
+        uint4 h, l;
+        split_bf16x8(x4[2 * i], x4[2 * i + 1], h, l);
+        hi[i] = h;
+        lo[i] = l;
+    }
+}
 
 // Tokens per register group of the FFN kernels; a unit with M tokens is
 // processed as ceil(M / kGroupTokens) groups.
@@ -116,6 +150,17 @@ __device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint3
         " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst_smem)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
+}
+
+// ---- cp.async (16-byte global -> shared, L2 only) ---------------------------------
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // ---- named barrier among a subset of warps -----------------------------------

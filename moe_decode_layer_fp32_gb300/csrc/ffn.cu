@@ -550,6 +550,11 @@ __global__ void combine_kernel(CombineArgs a) {
     reinterpret_cast<float4*>(a.y)[(size_t)t * d4 + c4] = acc;
 }
 
+__global__ void split_x_kernel(const float* x, long long elems, __nv_bfloat16* xb) {
+    split_activations(x, elems, xb, blockIdx.x * (long long)blockDim.x + threadIdx.x,
+                      (long long)gridDim.x * blockDim.x);
+}
+
 __global__ void zero_kernel(uint4* p, size_t n16) {
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16;
          i += (size_t)gridDim.x * blockDim.x)
@@ -602,4 +607,14 @@ cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+}  // namespace moe
+
+namespace moe {
+cudaError_t launch_split_x(const float* x, long long elems, __nv_bfloat16* xb, cudaStream_t s) {
+    const long long n8 = elems / 8;
+    const int threads = 256;
+    const long long want = (n8 + threads - 1) / threads;
+    split_x_kernel<<<(int)(want < 1024 ? (want > 0 ? want : 1) : 1024), threads, 0, s>>>(x, elems, xb);
+    return cudaGetLastError();
+}
 }  // namespace moe

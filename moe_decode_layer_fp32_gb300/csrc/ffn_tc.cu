@@ -8,19 +8,25 @@
 // Decoding" §2.1 eq. (1); a department backbone runs once over its token set
 // X^j (two-stage routing, §3.2).
 //
-// Mapping onto the MMA (D[M x N] = A[M x K] * B[N x K]^T, fp32 accumulate):
-//  * gate/up: A = a tile of <= 64 weight rows (K-major, 128 B swizzle, loaded
-//    by TMA in 16-row boxes), B = the tokens' activations, N = tokens;
+// Mapping onto the MMA (D[M x N] = A[M x K] * B[N x K]^T, fp32 accumulate,
+// M = 128):
+//  * gate/up: A = a tile of 128 weight rows (K-major, 128 B swizzle), B = the
+//    tokens' activations, N = tokens;
 //  * down:    A = W_down rows of the same tile read as an MN-major operand
-//    (M = 128 hidden columns, K = the tile's rows), B = H = SiLU(g) * u.
+//    (M = 128 hidden columns, K = the tile's 128 rows), B = H = SiLU(g) * u.
+// An MMA costs the tensor pipe a fixed ~45 cycles whatever N <= 64 is, so
+// each one must carry a full 128-row (4 KB) slice of weights to outrun HBM.
+// Weight tiles arrive as 3-D TMA boxes of 128 rows x 128 columns (256
+// contiguous bytes per row; 32 KB), which stream at full HBM rate.
 // Activations and H are split into bf16 hi + lo parts (x = hi + lo up to
 // 2^-17 relative), so the products keep close to fp32 accuracy: each token
 // occupies two B rows and the epilogue adds the two result columns.
 //
-// Warp roles (one CTA per SM): warp 0 issues TMA loads of weight tiles into an
-// 8-stage ring; warp 1 issues the MMAs (one thread) and owns the TMEM
+// Warp roles (one CTA per SM): warp 0 issues TMA loads of weight boxes into a
+// 4-stage ring; warp 1 issues the MMAs (one thread) and owns the TMEM
 // allocation; warps 2-5 are the epilogue (TMEM -> registers, SwiGLU, H tile,
-// output atomics); warps 6-9 convert activations into swizzled bf16 B tiles.
+// output atomics); warps 6-9 gather the bf16 hi/lo activations (split once per
+// layer) into swizzled B tiles with cp.async.
 // Every wait is bounded; on a timeout the kernel records an error status,
 // drains its copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -34,37 +40,48 @@ namespace moe {
 
 namespace {
 
-constexpr int kTcStages = 8;
-constexpr int kTcRows = 64;                 // weight rows per tile
-constexpr int kTcTokens = 32;               // tokens per group (hi + lo rows: N <= 64)
+// Geometry.  A weight stage is one TMA box: kTcRows rows x 2 column chunks of
+// 64 (K-blocks for gate/up, 128 hidden columns for down), landing as
+// [chunk][row][128 B] with 128 B swizzle.  Gate/up run in K-pairs: the gate
+// stage, then the up stage, of the same two K-blocks.
+constexpr int kTcRows = kTcBoxRows;               // 128
+constexpr int kChunkBytes = kTcRows * 128;        // 16 KB: one 64-column chunk
+constexpr int kAStage = 2 * kChunkBytes;          // 32 KB
+constexpr int kTcStages = 4;                      // weight ring
+constexpr int kTcTokens = 32;                     // tokens per group (hi + lo rows: N <= 64)
 constexpr int kTcMaxN = 2 * kTcTokens;
-constexpr int kAStage = 16384;              // gate+up tiles, or one down tile (2 halves)
-constexpr int kBStage = kTcMaxN * 128;      // activation tile: N rows x 64 bf16
-constexpr int kHTile = kTcMaxN * 128;       // H tile: N rows x (K <= 64) bf16
-constexpr int kTmemCols = 256;
-constexpr uint32_t kColG = 0, kColU = 64, kColY0 = 128, kColY1 = 192;
+constexpr int kBBlock = kTcMaxN * 128;            // activations of one K-block: N rows x 128 B
+constexpr int kBPair = 2 * kBBlock;               // ... of one K-pair
+constexpr int kTcBPairs = 3;                      // activation ring (K-pairs)
+constexpr int kHChunk = kTcMaxN * 128;            // H: [K chunk][N rows][128 B]
+constexpr int kHTile = 2 * kHChunk;               // K = 128 tile rows
+constexpr int kTmemCols = 512;
+constexpr uint32_t kColG = 0, kColU = 64, kColY = 128;
+constexpr int kYBufs = 6;                         // down accumulators, 64 columns each
 constexpr int kTcWarps = 10;
 constexpr int kTcThreads = kTcWarps * 32;
 
 struct TcSmem {
     uint64_t full[kTcStages];     // producer TMA bytes landed (weight ring)
     uint64_t empty[kTcStages];    // MMAs reading the weight stage are done
-    uint64_t bx_full[kTcStages];  // converter wrote the activation tile (own ring)
-    uint64_t bx_empty[kTcStages]; // MMAs reading the activation tile are done
+    uint64_t bx_full[kTcBPairs];  // activation K-pair gathered
+    uint64_t bx_empty[kTcBPairs]; // MMAs reading the activation K-pair are done
     uint64_t acc_full, acc_empty, h_full, mma_done;
-    uint64_t y_full[2], y_empty[2];
+    uint64_t y_full[kYBufs], y_empty[kYBufs];
     uint32_t tmem_base;
     int cls_units[3];
     int cls_groups[3];
     int cls_off[3];
+    int ep_row[4][kTcTokens];     // epilogue warps: output row of each tile token
+    float ep_w[4][kTcTokens];     // ... and its routing weight
     int4 units[1];                // per class: {unit, first entry, tokens, group prefix}
 };
 
 struct TSeg {
-    int cls, q, grp, row0, nrows;
+    int cls, q, grp, row0;
 };
 
-// Next tile of the CTA's row range [r, r_end) (rows; tiles <= kTcRows).
+// Next tile (kTcRows rows) of the CTA's row range [r, r_end).
 __device__ __forceinline__ bool next_tile(const TcArgs& a, const TcSmem& sm, int& r, int r_end,
                                           TSeg& s) {
     if (r >= r_end) return false;
@@ -76,7 +93,6 @@ __device__ __forceinline__ bool next_tile(const TcArgs& a, const TcSmem& sm, int
     const int rows = a.f.cls[c].rows;
     const int rel = r - base;
     const int vg = rel / rows;
-    const int rin = rel - vg * rows;
     const int4* u = sm.units + sm.cls_off[c];
     int lo = 0, hi = sm.cls_units[c] - 1;
     while (lo < hi) {
@@ -86,9 +102,8 @@ __device__ __forceinline__ bool next_tile(const TcArgs& a, const TcSmem& sm, int
     s.cls = c;
     s.q = lo;
     s.grp = vg - (lo > 0 ? u[lo - 1].w : 0);
-    s.row0 = rin;
-    s.nrows = min(min(rows - rin, r_end - r), kTcRows);
-    r += s.nrows;
+    s.row0 = rel - vg * rows;
+    r += kTcRows;
     return true;
 }
 
@@ -111,12 +126,6 @@ __device__ __forceinline__ void tile_token(const TcArgs& a, int kind, int entry,
     if (a.f.out_mode == MOE_OUT_ACCUM) row = t;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-    const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-    return l | (h << 16);
-}
-
 __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_constant__ TcArgs a) {
     extern __shared__ unsigned char smem_dyn[];
     // 1024-byte aligned tile regions (128 B swizzle atoms)
@@ -124,17 +133,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
         (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
     unsigned char* aring = base;
     unsigned char* bring = aring + kTcStages * kAStage;
-    unsigned char* htile = bring + kTcStages * kBStage;
+    unsigned char* htile = bring + kTcBPairs * kBPair;
     TcSmem& sm = *reinterpret_cast<TcSmem*>(htile + kHTile);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d = a.f.d;
-    const int KB = d / 64, DT = d / 128;
+    const int KP = d / 128, DT = d / 128;          // K-pairs (gate/up), M-tiles (down)
 
     if (tid == 0) {
         for (int i = 0; i < kTcStages; ++i) {
             mbar_init(&sm.full[i], 1);
             mbar_init(&sm.empty[i], 1);
+        }
+        for (int i = 0; i < kTcBPairs; ++i) {
             mbar_init(&sm.bx_full[i], 4);
             mbar_init(&sm.bx_empty[i], 1);
         }
@@ -142,7 +153,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
         mbar_init(&sm.acc_empty, 4);
         mbar_init(&sm.h_full, 4);
         mbar_init(&sm.mma_done, 1);
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kYBufs; ++b) {
             mbar_init(&sm.y_full[b], 1);
             mbar_init(&sm.y_empty[b], 4);
         }
@@ -164,10 +175,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
     // Everything below reads what the routing / dispatch kernel wrote.
     pdl_wait_primary();
 
-    // ---- unit table: this kernel's units (>= min_tokens tokens), groups of kTcTokens ----
-    if (warp == 0) {
+    // ---- unit table: this kernel's units (>= min_tokens tokens), groups of kTcTokens;
+    // warp c filters class c ----
+    if (warp < a.f.ncls) {
         int off = 0;
-        for (int c = 0; c < a.f.ncls; ++c) {
+        for (int c = 0; c < warp; ++c) off += class_capacity(a.f.cls[c], a.f.n, a.f.g);
+        {
+            const int c = warp;
             const UnitClass& uc = a.f.cls[c];
             int kept, groups;
             if (uc.kind == kUnitShared) {
@@ -186,16 +200,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                 sm.cls_groups[c] = groups;
                 sm.cls_off[c] = off;
             }
-            off += class_capacity(uc, a.f.n, a.f.g);
         }
     }
     __syncthreads();
 
-    // CTA's share of the row space, in 16-row quanta
+    // CTA's share of the row space, in whole tiles
     int Q = 0;
-    for (int c = 0; c < a.f.ncls; ++c) Q += a.f.cls[c].rows / 16 * sm.cls_groups[c];
-    const int r_begin = (int)((long long)Q * blockIdx.x / gridDim.x) * 16;
-    const int r_end = (int)((long long)Q * (blockIdx.x + 1) / gridDim.x) * 16;
+    for (int c = 0; c < a.f.ncls; ++c) Q += a.f.cls[c].rows / kTcRows * sm.cls_groups[c];
+    const int r_begin = (int)((long long)Q * blockIdx.x / gridDim.x) * kTcRows;
+    const int r_end = (int)((long long)Q * (blockIdx.x + 1) / gridDim.x) * kTcRows;
 
     bool ok = true;
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -214,34 +227,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
             uint32_t it = 0;
             int r = r_begin;
             TSeg s;
+            auto load = [&](const CUtensorMap* m, int y, int z) -> bool {
+                const int slot = it % kTcStages;
+                if (!wait(&sm.empty[slot], ((it / kTcStages) & 1u) ^ 1u)) return false;
+                mbar_arrive_expect_tx(&sm.full[slot], kAStage);
+                tma_load_3d(aring + slot * kAStage, m, 0, y, z, &sm.full[slot], pol);
+                ++it;
+                return true;
+            };
             while (ok && next_tile(a, sm, r, r_end, s)) {
                 const int4 rec = sm.units[sm.cls_off[s.cls] + s.q];
-                const int ybase = rec.x * a.f.cls[s.cls].rows + s.row0;
-                const int nq = s.nrows / 16;
-                const uint32_t bytes = (uint32_t)s.nrows * 128u * 2u;
-                const CUtensorMap* mg = &a.maps[s.cls][0];
-                const CUtensorMap* mu = &a.maps[s.cls][1];
-                const CUtensorMap* md = &a.maps[s.cls][2];
-                for (int kb = 0; ok && kb < KB; ++kb, ++it) {
-                    const int slot = it % kTcStages;
-                    if (!wait(&sm.empty[slot], ((it / kTcStages) & 1u) ^ 1u)) break;
-                    mbar_arrive_expect_tx(&sm.full[slot], bytes);
-                    unsigned char* A = aring + slot * kAStage;
-                    for (int q = 0; q < nq; ++q) {
-                        tma_load_2d(A + q * 2048, mg, kb * 64, ybase + q * 16, &sm.full[slot], pol);
-                        tma_load_2d(A + 8192 + q * 2048, mu, kb * 64, ybase + q * 16, &sm.full[slot], pol);
-                    }
+                const int y = rec.x * a.f.cls[s.cls].rows + s.row0;
+                const CUtensorMap* maps = a.maps[s.cls];
+                for (int p = 0; ok && p < KP; ++p) {
+                    if (!load(&maps[0], y, 2 * p)) break;
+                    if (!load(&maps[1], y, 2 * p)) break;
                 }
-                for (int dt = 0; ok && dt < DT; ++dt, ++it) {
-                    const int slot = it % kTcStages;
-                    if (!wait(&sm.empty[slot], ((it / kTcStages) & 1u) ^ 1u)) break;
-                    mbar_arrive_expect_tx(&sm.full[slot], bytes);
-                    unsigned char* A = aring + slot * kAStage;
-                    for (int h = 0; h < 2; ++h)
-                        for (int q = 0; q < nq; ++q)
-                            tma_load_2d(A + h * s.nrows * 128 + q * 2048, md, dt * 128 + h * 64,
-                                        ybase + q * 16, &sm.full[slot], pol);
-                }
+                for (int mt = 0; ok && mt < DT; ++mt)
+                    if (!load(&maps[2], y, 2 * mt)) break;
             }
             // every issued copy must land before the CTA may exit
             const uint32_t first = it > (uint32_t)kTcStages ? it - kTcStages : 0u;
@@ -251,54 +254,65 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
     } else if (warp == 1) {
         // ===================== MMA issuer =====================
         if (lane == 0) {
-            uint32_t it = 0, bit = 0, ti = 0, dtc = 0;
+            uint32_t it = 0, bp = 0, ti = 0, dtc = 0;
             int r = r_begin;
             TSeg s;
-            const uint32_t a_base = smem_u32(aring), b_base = smem_u32(bring), h_base = smem_u32(htile);
+            // descriptors: address field += byte offset >> 4 (all of smem < 256 KB)
+            const uint64_t a_k = smem_desc_sw128(smem_u32(aring), 16, 1024);          // K-major
+            const uint64_t a_mn = smem_desc_sw128(smem_u32(aring), kChunkBytes, 1024); // MN-major
+            const uint64_t b_k = smem_desc_sw128(smem_u32(bring), 16, 1024);
+            const uint64_t h_k = smem_desc_sw128(smem_u32(htile), 16, 1024);
             while (ok && next_tile(a, sm, r, r_end, s)) {
                 const int4 rec = sm.units[sm.cls_off[s.cls] + s.q];
                 const int mg = min(kTcTokens, rec.z - s.grp * kTcTokens);
-                const int Mp = (mg + 7) & ~7;
-                const int N = 2 * Mp;
+                const int N = 2 * ((mg + 7) & ~7);
                 const uint32_t id_gu = idesc_bf16_f32(128, N, false, false);
                 const uint32_t id_dn = idesc_bf16_f32(128, N, true, false);
                 if (!wait(&sm.acc_empty, (ti & 1u) ^ 1u)) break;
                 tc_fence_after_sync();
-                for (int kb = 0; ok && kb < KB; ++kb, ++it, ++bit) {
-                    const int slot = it % kTcStages, bslot = bit % kTcStages;
-                    if (!wait(&sm.full[slot], (it / kTcStages) & 1u) ||
-                        !wait(&sm.bx_full[bslot], (bit / kTcStages) & 1u))
-                        break;
-                    tc_fence_after_sync();
-                    const uint32_t A = a_base + slot * kAStage, Bx = b_base + bslot * kBStage;
+                for (int p = 0; ok && p < KP; ++p, ++bp) {
+                    const uint32_t bslot = bp % kTcBPairs;
+                    if (!wait(&sm.bx_full[bslot], (bp / kTcBPairs) & 1u)) break;
+                    const uint64_t bd = b_k + ((bslot * kBPair) >> 4);
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        const uint64_t bd = smem_desc_sw128(Bx + ks * 32, 16, 1024);
-                        const uint32_t acc = (kb | ks) ? 1u : 0u;
-                        umma_bf16(tmem + kColG, smem_desc_sw128(A + ks * 32, 16, 1024), bd, id_gu, acc);
-                        umma_bf16(tmem + kColU, smem_desc_sw128(A + 8192 + ks * 32, 16, 1024), bd, id_gu, acc);
+                    for (int gu = 0; gu < 2; ++gu, ++it) {
+                        const uint32_t slot = it % kTcStages;
+                        if (!wait(&sm.full[slot], (it / kTcStages) & 1u)) break;
+                        tc_fence_after_sync();
+                        const uint64_t ad = a_k + ((slot * kAStage) >> 4);
+                        const uint32_t acc_col = tmem + (gu ? kColU : kColG);
+#pragma unroll
+                        for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+                            for (int ks = 0; ks < 4; ++ks)
+                                umma_bf16(acc_col, ad + ((kb * kChunkBytes + ks * 32) >> 4),
+                                          bd + ((kb * kBBlock + ks * 32) >> 4), id_gu,
+                                          (p | kb | ks) ? 1u : 0u);
+                        umma_commit(&sm.empty[slot]);
                     }
-                    umma_commit(&sm.empty[slot]);
                     umma_commit(&sm.bx_empty[bslot]);
                 }
                 if (!ok) break;
                 umma_commit(&sm.acc_full);
                 if (!wait(&sm.h_full, ti & 1u)) break;
                 tc_fence_after_sync();
-                const int ksteps = s.nrows / 16;
-                for (int dt = 0; ok && dt < DT; ++dt, ++it, ++dtc) {
-                    const uint32_t b = dtc & 1u, use = dtc >> 1;
-                    const int slot = it % kTcStages;
-                    if (!wait(&sm.y_empty[b], (use & 1u) ^ 1u)) break;
+                // down: M-tile mt = 128 hidden columns; A is W_down read MN-major
+                // (chunk slabs kChunkBytes apart), K = the tile's 128 rows
+                for (int mt = 0; ok && mt < DT; ++mt, ++it, ++dtc) {
+                    const uint32_t slot = it % kTcStages;
                     if (!wait(&sm.full[slot], (it / kTcStages) & 1u)) break;
+                    const uint32_t yb = dtc % kYBufs;
+                    if (!wait(&sm.y_empty[yb], ((dtc / kYBufs) & 1u) ^ 1u)) break;
                     tc_fence_after_sync();
-                    const uint32_t A = a_base + slot * kAStage;
-                    for (int ks = 0; ks < ksteps; ++ks)
-                        umma_bf16(tmem + (b ? kColY1 : kColY0),
-                                  smem_desc_sw128(A + ks * 2048, s.nrows * 128, 1024),
-                                  smem_desc_sw128(h_base + ks * 32, 16, 1024), id_dn, ks ? 1u : 0u);
+                    const uint64_t ad = a_mn + ((slot * kAStage) >> 4);
+                    const uint32_t ycol = tmem + kColY + yb * 64;
+#pragma unroll
+                    for (int ks = 0; ks < kTcRows / 16; ++ks)
+                        umma_bf16(ycol, ad + ((ks * 2048) >> 4),
+                                  h_k + (((ks >> 2) * kHChunk + (ks & 3) * 32) >> 4), id_dn,
+                                  ks ? 1u : 0u);
+                    umma_commit(&sm.y_full[yb]);
                     umma_commit(&sm.empty[slot]);
-                    umma_commit(&sm.y_full[b]);
                 }
                 ++ti;
             }
@@ -310,6 +324,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
         const int quarter = warp & 3;                   // TMEM lanes this warp may access
         const int m = quarter * 32 + lane;              // tile row (gate/up) / hidden column (down)
         const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
+        // H is K-major [K chunk][token row][128 B]: this thread's K index is m
+        unsigned char* hcol = htile + (m >> 6) * kHChunk + (m & 7) * 2;
+        const int hchunk = (m & 63) >> 3;
         uint32_t ti = 0, dtc = 0;
         int r = r_begin;
         TSeg s;
@@ -319,6 +336,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
             const int first = rec.y + s.grp * kTcTokens;
             const int mg = min(kTcTokens, rec.z - s.grp * kTcTokens);
             const int Mp = (mg + 7) & ~7;
+            if (lane < mg) {
+                int t, row;
+                float w;
+                tile_token(a, kind, first + lane, t, w, row);
+                sm.ep_row[quarter][lane] = row;
+                sm.ep_w[quarter][lane] = w;
+            }
+            __syncwarp();
             if (!wait(&sm.acc_full, ti & 1u)) break;
             tc_fence_after_sync();
             for (int c0 = 0; c0 < Mp; c0 += 16) {
@@ -327,26 +352,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                 tmem_ld16(tmem + lanes + kColG + Mp + c0, glo);
                 tmem_ld16(tmem + lanes + kColU + c0, uhi);
                 tmem_ld16(tmem + lanes + kColU + Mp + c0, ulo);
-                if (m < s.nrows) {
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int j = c0 + jj;
-                        if (j < mg) {
-                            int t, row;
-                            float w;
-                            tile_token(a, kind, first + j, t, w, row);
-                            float h = silu_f(ghi[jj] + glo[jj]) * (uhi[jj] + ulo[jj]);
-                            if (a.f.out_mode == MOE_OUT_ACCUM) h *= w;
-                            const __nv_bfloat16 hh = __float2bfloat16_rn(h);
-                            const __nv_bfloat16 hl = __float2bfloat16_rn(h - __bfloat162float(hh));
-                            // H is K-major: token row j (hi) / Mp + j (lo), K index m
-                            const int chunk = m >> 3, within = m & 7;
-                            *reinterpret_cast<__nv_bfloat16*>(
-                                htile + j * 128 + (((chunk ^ (j & 7)) << 4) + within * 2)) = hh;
-                            const int jl = Mp + j;
-                            *reinterpret_cast<__nv_bfloat16*>(
-                                htile + jl * 128 + (((chunk ^ (jl & 7)) << 4) + within * 2)) = hl;
-                        }
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int j = c0 + jj;
+                    if (j < mg) {
+                        float h = silu_f(ghi[jj] + glo[jj]) * (uhi[jj] + ulo[jj]);
+                        if (a.f.out_mode == MOE_OUT_ACCUM) h *= sm.ep_w[quarter][j];
+                        const __nv_bfloat16 hh = __float2bfloat16_rn(h);
+                        const __nv_bfloat16 hl = __float2bfloat16_rn(h - __bfloat162float(hh));
+                        const int jl = Mp + j;
+                        *reinterpret_cast<__nv_bfloat16*>(hcol + j * 128 + ((hchunk ^ (j & 7)) << 4)) = hh;
+                        *reinterpret_cast<__nv_bfloat16*>(hcol + jl * 128 + ((hchunk ^ (jl & 7)) << 4)) = hl;
                     }
                 }
             }
@@ -358,10 +374,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                 mbar_arrive(&sm.h_full);
             }
             for (int dt = 0; ok && dt < DT; ++dt, ++dtc) {
-                const uint32_t b = dtc & 1u, use = dtc >> 1;
-                if (!wait(&sm.y_full[b], use & 1u)) break;
+                const uint32_t yb = dtc % kYBufs;
+                if (!wait(&sm.y_full[yb], (dtc / kYBufs) & 1u)) break;
                 tc_fence_after_sync();
-                const uint32_t ycol = b ? kColY1 : kColY0;
+                const uint32_t ycol = kColY + yb * 64;
+                float* orow = a.f.out + dt * 128 + m;
                 for (int c0 = 0; c0 < Mp; c0 += 16) {
                     float yhi[16], ylo[16];
                     tmem_ld16(tmem + lanes + ycol + c0, yhi);
@@ -369,26 +386,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                     if (c0 + 16 >= Mp) {
                         tc_fence_before_sync();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&sm.y_empty[b]);
+                        if (lane == 0) mbar_arrive(&sm.y_empty[yb]);
                     }
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) {
                         const int j = c0 + jj;
-                        if (j < mg) {
-                            int t, row;
-                            float w;
-                            tile_token(a, kind, first + j, t, w, row);
-                            atomicAdd(a.f.out + (size_t)row * d + dt * 128 + m, yhi[jj] + ylo[jj]);
-                        }
+                        if (j < mg) atomicAdd(orow + (size_t)sm.ep_row[quarter][j] * d, yhi[jj] + ylo[jj]);
                     }
                 }
             }
+            __syncwarp();
             ++ti;
         }
     } else {
-        // ===================== activation converter =====================
+        // ===================== activation gather =====================
+        // B tiles (one K-pair per slot) are copied with cp.async from the bf16
+        // hi / lo activations (split once per layer), kPre pairs ahead of the MMA.
+        constexpr int kPre = kTcBPairs - 1;
         const int ct = tid - 6 * 32;                    // 0..127
-        uint32_t bit = 0;
+        const __nv_bfloat16* xh = a.f.ws.xb;
+        const __nv_bfloat16* xl = a.f.ws.xb + (size_t)a.f.T * d;
+        uint32_t bp = 0;
         int r = r_begin;
         TSeg s;
         while (ok && next_tile(a, sm, r, r_end, s)) {
@@ -397,56 +415,65 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
             const int first = rec.y + s.grp * kTcTokens;
             const int mg = min(kTcTokens, rec.z - s.grp * kTcTokens);
             const int Mp = (mg + 7) & ~7;
-            const int items = 2 * Mp * 8;               // (B row, 16-byte chunk) pairs
-            // this thread's items are fixed for the tile: resolve their token rows once
-            const float* src[4];
+            const int items = 2 * Mp * 8;               // (B row, 16-byte chunk) pairs per K-block
+            // this thread's items are fixed for the tile: resolve them once
+            const __nv_bfloat16* src[4];
+            int dst[4];
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
                 const int item = ct + k4 * 128;
-                const int n = item >> 3;
+                const int n = item >> 3, c = item & 7;
                 const int j = n < Mp ? n : n - Mp;
                 src[k4] = nullptr;
+                dst[k4] = item < items ? n * 128 + ((c ^ (n & 7)) << 4) : -1;
                 if (item < items && j < mg) {
                     int t, row;
                     float w;
                     tile_token(a, kind, first + j, t, w, row);
-                    src[k4] = a.f.x + (size_t)t * d + (item & 7) * 8;
+                    src[k4] = (n < Mp ? xh : xl) + (size_t)t * d + c * 8;
                 }
             }
-            for (int kb = 0; ok && kb < KB; ++kb, ++bit) {
-                const int slot = bit % kTcStages;
-                if (!wait(&sm.bx_empty[slot], ((bit / kTcStages) & 1u) ^ 1u)) break;
-                unsigned char* Bt = bring + slot * kBStage;
+            auto issue = [&](int p) -> bool {
+                const uint32_t b = bp + p;
+                const int slot = b % kTcBPairs;
+                if (!wait(&sm.bx_empty[slot], ((b / kTcBPairs) & 1u) ^ 1u)) return false;
+                unsigned char* Bt = bring + slot * kBPair;
 #pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4) {
-                    const int item = ct + k4 * 128;
-                    if (item < items) {
-                        const int n = item >> 3, c = item & 7;
-                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                        if (src[k4]) {
-                            const float4* p = reinterpret_cast<const float4*>(src[k4] + kb * 64);
-                            const float4 x0 = __ldg(p), x1 = __ldg(p + 1);
-                            const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-                            float o[8];
-                            if (n < Mp) {
+                for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
-                                for (int e = 0; e < 8; ++e) o[e] = xv[e];
-                            } else {
-#pragma unroll
-                                for (int e = 0; e < 8; ++e)
-                                    o[e] = xv[e] - __bfloat162float(__float2bfloat16_rn(xv[e]));
-                            }
-                            v = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
-                                           pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        if (dst[k4] >= 0) {
+                            unsigned char* dp = Bt + kb * kBBlock + dst[k4];
+                            if (src[k4]) cp_async16(dp, src[k4] + (2 * p + kb) * 64);
+                            else *reinterpret_cast<uint4*>(dp) = make_uint4(0u, 0u, 0u, 0u);
                         }
-                        *reinterpret_cast<uint4*>(Bt + n * 128 + ((c ^ (n & 7)) << 4)) = v;
                     }
+                cp_async_commit();
+                return true;
+            };
+            // exactly kPre groups in flight before the first wait (empty ones
+            // when the tile has fewer pairs), one more per pair after
+            for (int p = 0; ok && p < kPre; ++p) {
+                if (p < KP) {
+                    if (!issue(p)) break;
+                } else {
+                    cp_async_commit();
                 }
+            }
+            for (int p = 0; ok && p < KP; ++p) {
+                if (p + kPre < KP) {
+                    if (!issue(p + kPre)) break;
+                } else {
+                    cp_async_commit();                  // keep one group per pair
+                }
+                cp_async_wait<kPre>();                  // pair p has landed
                 fence_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.bx_full[slot]);
+                if (lane == 0) mbar_arrive(&sm.bx_full[(bp + p) % kTcBPairs]);
             }
+            bp += KP;
         }
+        cp_async_wait<0>();
     }
 
     tc_fence_before_sync();
@@ -460,7 +487,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
 }  // namespace
 
 size_t ffn_tc_smem_bytes(int units) {
-    return 1024 + (size_t)kTcStages * (kAStage + kBStage) + kHTile + sizeof(TcSmem) +
+    return 1024 + (size_t)kTcStages * kAStage + (size_t)kTcBPairs * kBPair + kHTile + sizeof(TcSmem) +
            (size_t)units * sizeof(int4);
 }
 

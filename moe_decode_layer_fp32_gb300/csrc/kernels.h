@@ -27,6 +27,7 @@ struct RouteArgs {
     int g;                   // experts per department
     float* y_zero;           // zeroed by the route grid when non-null
     long long y_elems;
+    int split_x;             // also write the bf16 hi/lo activations (ws.xb)
 };
 
 struct DispatchArgs {
@@ -75,8 +76,13 @@ struct TcArgs {
     int min_tokens;       // units with at least this many tokens
 };
 
-// Units with at least this many tokens run on the tensor cores.
-constexpr int kTcMinTokens = 4;
+// Units with at least this many tokens run on the tensor cores (library
+// default: none; the caller opts in with moe_set_tc_min_tokens).
+constexpr int kTcMinTokens = 1 << 30;
+// Rows of one tensor-core weight tile / TMA box (unit rows must be a multiple),
+// and the hidden-size granularity of its down-projection stages.
+constexpr int kTcBoxRows = 128;
+constexpr int kTcHiddenQuantum = 128;
 
 struct CombineArgs {
     const float* rows;
@@ -94,6 +100,7 @@ cudaError_t launch_ffn_tc(const TcArgs& a, cudaStream_t s);
 size_t ffn_tc_smem_bytes(int units);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
 cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t s);
+cudaError_t launch_split_x(const float* x, long long elems, __nv_bfloat16* xb, cudaStream_t s);
 
 int device_sm_count();
 

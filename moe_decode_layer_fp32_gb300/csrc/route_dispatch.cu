@@ -244,6 +244,9 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
     pdl_allow_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
+    if (a.split_x)
+        split_activations(a.x, (long long)a.T * a.d, a.ws.xb, blockIdx.x * (long long)kRouteThreads + tid,
+                          (long long)gridDim.x * kRouteThreads);
     if (a.y_zero) {
         float4* y4 = reinterpret_cast<float4*>(a.y_zero);
         const long long n4 = a.y_elems >> 2;

@@ -33,8 +33,8 @@ def threshold(B):
     B.moe_set_tc_min_tokens(prev)
 
 
-SMALL_TC = synth.LayerShape("tc-small", d=256, n=16, k=4, dtype="bf16", g=4, I_sh=64, I_pr=16,
-                            I_s=32, batches=(5,))
+SMALL_TC = synth.LayerShape("tc-small", d=256, n=16, k=4, dtype="bf16", g=4, I_sh=256, I_pr=128,
+                            I_s=128, batches=(5,))
 
 
 @pytest.mark.parametrize("mode", ["tc", "cc"])
@@ -42,7 +42,7 @@ def test_small_layer_each_path(B, threshold, mode):
     threshold(1 if mode == "tc" else 10 ** 6)
     for T in (1, 5, 33):
         check_layer(B, SMALL_TC, T, seed=3)
-        van = synth.LayerShape("tc-small-v", d=256, n=16, k=4, dtype="bf16", I=48, I_s=32)
+        van = synth.LayerShape("tc-small-v", d=384, n=16, k=4, dtype="bf16", I=128, I_s=128)
         check_layer(B, van, T, seed=4)
 
 
