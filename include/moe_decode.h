@@ -165,6 +165,37 @@ int moe_route_topk(const float* x, const float* w_router, const float* bias,
                    int32_t* topk_idx, float* topk_w,
                    void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * moe_route_topk without a workspace and without allocating.  The paper has no
+ * counterpart: this is a library convenience.
+ *
+ * It is for callers that can neither pass a workspace nor let the library
+ * allocate: an engine that carves up all device memory once at start-up, or
+ * a decode loop that must not stall the device (cudaFree synchronises) or
+ * fail for lack of memory mid-step.  The logits scratch and the last-block
+ * counter live in one fixed device array that the library reserves when it
+ * is loaded; the call makes no cudaMalloc/cudaFree and calls no allocating
+ * routine.
+ *   Same arguments and results as moe_route_topk, except:
+ *   status   int32[1] device memory or NULL: receives the call's device status
+ *            word (0, or MOE_ERR_DEVICE for a non-finite logit), stream-ordered
+ *            after the kernel.
+ * Limits: those of moe_route_topk, and T * n <= 65536 (the fixed scratch
+ * holds 65536 fp32 logits, 256 KB); larger steps return MOE_ERR_UNSUPPORTED
+ * and launch nothing.
+ * Set-up: the first call on each device looks up the scratch's device address
+ * (cudaGetSymbolAddress) and remembers it; make that first call before any
+ * stream capture.
+ * Each call clears the scratch's status word and counter (stream-ordered)
+ * before its kernel runs.  There is one scratch per device and process:
+ * calls that overlap on the device (other streams, other host threads) race
+ * on it and give wrong results, so issue them one after another.
+ */
+int moe_route_topk_noalloc(const float* x, const float* w_router, const float* bias,
+                           int T, int d, int n, int k, float scale,
+                           int32_t* topk_idx, float* topk_w,
+                           int32_t* status, void* stream);
+
 /* ------------------------------------------------------------------------- */
 /* Step 2: dispatch (two-level index lists, built on the device)             */
 /* ------------------------------------------------------------------------- */

@@ -53,6 +53,7 @@ _SIGS = {
     "moe_workspace_init": (_I, [_P, _SZ, _P]),
     "moe_read_status": (_I, [_P, _SZ, C.POINTER(C.c_int32), C.POINTER(C.c_int32), _P]),
     "moe_route_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _SZ, _P]),
+    "moe_route_topk_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
     "moe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _P, _SZ, _P]),
     "moe_rows_count": (_I64, [_I, _I, _I, _I, _I]),
     "moe_ffn_vanilla": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P,
@@ -167,6 +168,15 @@ def moe_route_topk(x, w_router, bias, k: int, scale: float, topk_idx, topk_w, ws
     _check("moe_route_topk", lib().moe_route_topk(
         _ptr(x), _ptr(w_router), _ptr(bias), T, d, n, k, scale, _ptr(topk_idx), _ptr(topk_w),
         _ptr(ws), ws.numel(), _stream()))
+
+
+def moe_route_topk_noalloc(x, w_router, bias, k: int, scale: float, topk_idx, topk_w, status=None):
+    """``status``: int32 CUDA tensor of one element, or None."""
+    T, d = x.shape
+    n = w_router.shape[0]
+    _check("moe_route_topk_noalloc", lib().moe_route_topk_noalloc(
+        _ptr(x), _ptr(w_router), _ptr(bias), T, d, n, k, scale, _ptr(topk_idx), _ptr(topk_w),
+        _ptr(status), _stream()))
 
 
 def moe_dispatch(topk_idx, topk_w, n: int, experts_per_dept: int, ws):

@@ -4,6 +4,7 @@
 #include <climits>
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 #include "../../include/moe_decode.h"
@@ -262,6 +263,44 @@ int device_sm_count() {
 }
 }  // namespace moe
 
+// ---- fixed router scratch for moe_route_topk_noalloc ----------------------
+// Some callers cannot hand the library a workspace or let it allocate one:
+// an engine whose device memory is carved up once at start-up, or a caller
+// that must not stall the device (cudaFree synchronises) or fail for lack of
+// memory in the middle of a decode step.  For them the router step can run on
+// this array, which the loader reserves with the module.  Its size bounds the
+// step to T * n <= kNoAllocMaxLogits.
+constexpr int kNoAllocMaxLogits = 64 * 1024;          // T * n router logits (256 KB)
+constexpr size_t kNoAllocHeader = 256;                // [0] status word, [128] block counter
+static __device__ __align__(256) unsigned char g_route_scratch[kNoAllocHeader +
+                                                               (size_t)kNoAllocMaxLogits * sizeof(float)];
+
+namespace {
+constexpr int kScratchDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kScratchDevices] = {};
+
+// This device's address of g_route_scratch, looked up on the first call made
+// on the device and remembered after that.
+int route_scratch(void** out, const char* who) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    if (dev < 0 || dev >= kScratchDevices)
+        return fail(MOE_ERR_UNSUPPORTED, "%s: device %d is beyond the %d the scratch table tracks", who,
+                    dev, kScratchDevices);
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_route_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, who);
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return MOE_OK;
+}
+}  // namespace
+
 extern "C" {
 
 int moe_version(void) { return 100; }
@@ -336,6 +375,51 @@ int moe_route_topk(const float* x, const float* w_router, const float* bias, int
     a.g = 1;
     cudaError_t e = moe::launch_route(a, as_stream(stream));
     if (e != cudaSuccess) return cuda_fail(e, who);
+    return MOE_OK;
+}
+
+int moe_route_topk_noalloc(const float* x, const float* w_router, const float* bias, int T, int d,
+                           int n, int k, float scale, int32_t* topk_idx, float* topk_w,
+                           int32_t* status, void* stream) {
+    const char* who = "moe_route_topk_noalloc";
+    if (T < 1 || T > moe::kMaxT || n < 1 || n > moe::kMaxN || k < 1 || k > n || k > moe::kMaxK)
+        return fail(MOE_ERR_INVALID_ARG, "%s: invalid sizes T=%d n=%d k=%d", who, T, n, k);
+    if ((long long)T * n > kNoAllocMaxLogits)
+        return fail(MOE_ERR_UNSUPPORTED,
+                    "%s: T*n = %lld router logits exceed the fixed scratch (%d); use moe_route_topk "
+                    "with a workspace", who, (long long)T * n, kNoAllocMaxLogits);
+    int rc = check_hidden(x, d, who);
+    if (rc) return rc;
+    if (d > kMaxRouterHidden)
+        return fail(MOE_ERR_UNSUPPORTED, "%s: d=%d exceeds the router kernel's %d", who, d, kMaxRouterHidden);
+    if (!w_router || !aligned16(w_router)) return fail(MOE_ERR_INVALID_ARG, "%s: w_router null or unaligned", who);
+    if (!topk_idx || !topk_w) return fail(MOE_ERR_INVALID_ARG, "%s: outputs are null", who);
+    void* scratch = nullptr;
+    if ((rc = route_scratch(&scratch, who))) return rc;
+    char* b = static_cast<char*>(scratch);
+    cudaStream_t s = as_stream(stream);
+    // the status word and the last-block counter start every call at zero
+    cudaError_t e = cudaMemsetAsync(b, 0, kNoAllocHeader, s);
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    moe::RouteArgs a = {};
+    a.x = x;
+    a.w_router = w_router;
+    a.bias = bias;
+    a.T = T; a.d = d; a.n = n; a.k = k;
+    a.scale = scale;
+    a.topk_idx = topk_idx;
+    a.topk_w = topk_w;
+    a.ws.status = reinterpret_cast<int32_t*>(b);
+    a.ws.sync = reinterpret_cast<uint32_t*>(b + 128);
+    a.ws.logits = reinterpret_cast<float*>(b + kNoAllocHeader);
+    a.fuse_dispatch = 0;
+    a.g = 1;
+    e = moe::launch_route(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    if (status) {
+        e = cudaMemcpyAsync(status, b, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, who);
+    }
     return MOE_OK;
 }
 
