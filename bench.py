@@ -204,6 +204,7 @@ class Workload:
         self.unique = {}
         self.ffn_bytes = {}
         self.counts = {}
+        self.choice = {}
 
     def shared(self, L):
         return None if L["sgate"] is None else (L["sgate"], L["sup"], L["sdown"])
@@ -255,6 +256,21 @@ class Workload:
             self.unique[key] = U
             self.ffn_bytes[key] = U - 4 * s.d * s.n
             self.counts[key] = (A_e, A_d)
+            lay = B.moe_workspace_layout(key[1], s.n, s.k, self.g)
+            self.choice[key] = int(ws[lay["sync"] + 4: lay["sync"] + 8].cpu().view(torch.int32)[0])
+
+    def tc_launched(self, key, thr: int) -> bool:
+        """Whether the layer pass launches the tensor-core FFN kernel: in
+        automatic mode exactly when the kernels recorded a choice; with a fixed
+        threshold when the weights qualify and T >= thr."""
+        s, T = self.shape, key[1]
+        rows = [r for r in (s.I, s.I_sh, s.I_pr, s.I_s) if r > 0]
+        ok = s.dtype == "bf16" and s.d % 128 == 0 and all(r % 128 == 0 for r in rows)
+        if not ok:
+            return False
+        if thr > 0:
+            return T >= thr
+        return self.choice[key] != 0
 
 
 def capture(fn):
@@ -332,8 +348,12 @@ def run_ours(args, rank, world, local):
             gs = capture(fn)
             time_graphs([gs], [0] * 3, world, device)
             stage_us[name] = round(time_graphs([gs], [0] * reps, world, device) / (reps * R) * 1e6, 2)
+        paths = sorted({("tensor-core" if W.choice[(r, T)] == 2 else
+                         "cuda-core" if W.choice[(r, T)] == 1 or not W.tc_launched((r, T), args.tc_min_tokens)
+                         else "split") for r in range(R)})
         per_batch[str(T)] = {"us_per_layer": round(us, 2), "unique_MB": round(U / 1e6, 2),
                              "GBps": round(U / us / 1e3, 1), "stage_us": stage_us,
+                             "ffn_path": "/".join(paths),
                              "active_experts": round(sum(W.counts[(r, T)][0] for r in range(R)) / R, 2)}
         if shape.I_sh > 0:
             per_batch[str(T)]["active_depts"] = round(sum(W.counts[(r, T)][1] for r in range(R)) / R, 2)
@@ -348,7 +368,9 @@ def run_ours(args, rank, world, local):
     ffn_bytes = reps_f * sum(W.ffn_bytes.values())
     peaks = load_peaks()
     achieved = ffn_bytes / t_ffn / 1e9
-    roofline = {"bound": "hbm", "kernel": "ffn_stream_kernel", "achieved": round(achieved, 1),
+    ffn_kernels = sorted({"ffn_tc_kernel" if W.choice[key] == 2 else "ffn_stream_kernel" for key in W.ws})
+    roofline = {"bound": "hbm", "kernel": "expert FFN step (" + ", ".join(ffn_kernels) + ")",
+                "achieved": round(achieved, 1),
                 "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "us_per_launch": round(t_ffn / ffn_launches * 1e6, 2),
@@ -407,7 +429,9 @@ def run_ours(args, rank, world, local):
         "per_batch": per_batch,
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": args.steps * len(batches) * 2,
+        # per layer pass: routing (+ fused dispatch), CUDA-core FFN, tensor-core FFN when launched
+        "gpu_launches": sum(2 + int(W.tc_launched((i % R, T), args.tc_min_tokens))
+                            for i in range(args.steps) for T in batches),
         "clocks": clock_info,
         "cpu_baseline": cpu,
     }

@@ -67,13 +67,19 @@ int moe_version(void);
 const char* moe_last_error(void);
 
 /*
- * Tensor-core threshold of the FFN steps: a unit (expert, department or
- * shared expert) whose gathered token count is at least min_tokens runs on the
- * tcgen05 kernel, the others on the CUDA-core weight stream.  0 restores the
- * library default (every unit on the CUDA cores); a value above every batch
- * size does the same.  Process-wide; returns the previous setting (0 = default), or
- * MOE_ERR_INVALID_ARG for a negative value.  The tensor-core kernel applies to
- * bf16 weights with d % 128 == 0 and unit row counts that are multiples of 128.
+ * Tensor-core threshold of the FFN steps.  0 (the library default) chooses per
+ * call, on the device, between the tcgen05 kernel and the CUDA-core weight
+ * stream from the dispatched token counts (whichever streams fewer weight rows
+ * on the busiest SM, CUDA-core rows weighted 4/3 when d > 4096).  For
+ * d <= 4096 the tensor-core kernel is launched for that choice only when
+ * T > 4 and some unit class expects more than 4 tokens per unit under uniform
+ * routing (always, with a shared expert).  min_tokens > 0 fixes the split instead: units (experts,
+ * departments, the shared expert) with at least min_tokens gathered tokens
+ * run on the tcgen05 kernel, the others on the CUDA cores; a value above every
+ * batch size keeps everything on the CUDA cores.  Process-wide; returns the
+ * previous setting, or MOE_ERR_INVALID_ARG for a negative value.  The
+ * tensor-core kernel applies to bf16 weights with d % 128 == 0 and unit row
+ * counts that are multiples of 128.
  */
 int moe_set_tc_min_tokens(int min_tokens);
 
@@ -90,7 +96,8 @@ int moe_set_tc_min_tokens(int min_tokens);
  * ascending token id.
  *
  *   status    int32[4]   [0] first device error code (0 = none)
- *   counts    int32[4]   [0] active experts A_e, [1] active departments A_d
+ *   counts    int32[4]   [0] active experts A_e, [1] active departments A_d,
+ *                        [2], [3] their totals of ceil(tokens / 32)
  *   logits    float[T*n] router logits (scratch of moe_route_topk)
  *   exp_count int32[n]   assignments per expert
  *   exp_off   int32[n+1] exclusive prefix sum of exp_count
@@ -109,7 +116,11 @@ int moe_set_tc_min_tokens(int min_tokens);
  *                        assignments, inclusive prefix over active experts of
  *                        ceil(assignments / 4)} -- the FFN's work table
  *   dept_units int32[m][4] the same per active department over X^j
- *   sync      uint32[4]  internal counters (kept at zero between calls)
+ *   sync      uint32[4]  [0] internal counter (kept at zero between calls);
+ *                        [1] FFN kernel choice of the last FFN step: 0 none
+ *                        made (fixed threshold, or the step is not eligible
+ *                        for the tensor-core kernel), 1 CUDA cores, 2 tensor
+ *                        cores
  *   xb        bf16[2][T][8192] activations split as x = hi + lo (scratch of the
  *                        tensor-core FFN; rows packed at the call's d)
  * The department arrays are present only when experts_per_dept > 1.

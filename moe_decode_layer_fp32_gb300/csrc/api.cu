@@ -190,16 +190,44 @@ bool encode_weight_map(CUtensorMap* map, const void* base, int units, int rows, 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int tc_min_tokens() {
-    const int v = g_tc_min_tokens.load();
-    return v > 0 ? v : moe::kTcMinTokens;
-}
+// 0 (default): automatic per-call choice on the device; > 0: fixed threshold.
+int tc_min_tokens() { return g_tc_min_tokens.load(); }
 
 // Whether the tensor-core kernel takes part in this FFN step, and its TMA
 // descriptors: bf16 weights, d a multiple of 128, and a batch large enough for
 // some unit to reach the token threshold.
+// Expected tokens per active unit of the busiest class under uniform routing:
+// T*k/n per expert, T*P(department chosen) per department, T for the shared
+// expert.  P(department of g experts chosen) = 1 - C(n-g, k) / C(n, k).
+double expected_unit_tokens(const moe::FfnArgs& a, int T) {
+    double best = 0.0;
+    for (int c = 0; c < a.ncls; ++c) {
+        const moe::UnitClass& uc = a.cls[c];
+        double e = T;
+        if (uc.kind == moe::kUnitExpert) {
+            e = (double)T * a.k / a.n;
+        } else if (uc.kind == moe::kUnitDept) {
+            double miss = 1.0;
+            for (int i = 0; i < a.k; ++i)
+                miss *= a.n - a.g - i > 0 ? (double)(a.n - a.g - i) / (a.n - i) : 0.0;
+            e = T * (1.0 - miss);
+        }
+        best = e > best ? e : best;
+    }
+    return best;
+}
+
 bool prepare_tc(const moe::FfnArgs& a, int T, moe::TcArgs* t) {
-    const int mt = tc_min_tokens();
+    const int thr = tc_min_tokens();
+    // Automatic mode launches the tensor-core kernel (which then decides on
+    // the device) for wide rows always, and otherwise only when some class
+    // expects more than kGroupTokens tokens per unit: below that the CUDA-core
+    // stream reads each weight once, which the tensor cores do not beat at
+    // d <= kTcWideHidden, and an idle launch costs a few µs.
+    if (thr == 0 && a.d <= moe::kTcWideHidden &&
+        (T <= moe::kGroupTokens || expected_unit_tokens(a, T) <= moe::kGroupTokens))
+        return false;
+    const int mt = thr > 0 ? thr : 1;
     int units = 0;
     for (int c = 0; c < a.ncls; ++c) units += moe::class_capacity(a.cls[c], a.n, a.g);
     if (a.dtype != MOE_DTYPE_BF16 || a.d % moe::kTcHiddenQuantum != 0 || a.d > moe::kMaxXbHidden || T < mt ||
@@ -208,7 +236,7 @@ bool prepare_tc(const moe::FfnArgs& a, int T, moe::TcArgs* t) {
     for (int c = 0; c < a.ncls; ++c)
         if (a.cls[c].rows % moe::kTcBoxRows != 0) return false;
     t->f = a;
-    t->min_tokens = mt;
+    t->min_tokens = thr > 0 ? thr : 1;
     for (int c = 0; c < a.ncls; ++c) {
         const moe::UnitClass& uc = a.cls[c];
         const int nu = moe::class_capacity(uc, a.n, a.g);
@@ -237,7 +265,9 @@ int run_ffn(moe::FfnArgs& a, int T, int n, int k, int g, int has_shared, bool tc
         e = moe::launch_split_x(a.x, (long long)T * a.d, a.ws.xb, as_stream(stream));
         if (e != cudaSuccess) return cuda_fail(e, who);
     }
-    a.max_tokens = tc ? t.min_tokens - 1 : INT_MAX;
+    a.auto_tc = tc && tc_min_tokens() == 0;
+    a.sms = moe::device_sm_count();
+    a.max_tokens = tc && !a.auto_tc ? t.min_tokens - 1 : INT_MAX;
     e = moe::launch_ffn(a, as_stream(stream));
     if (e != cudaSuccess) return cuda_fail(e, who);
     if (tc) {

@@ -312,6 +312,16 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
     }
     long long R = 0;
     for (int c = 0; c < a.ncls; ++c) R += (long long)a.cls[c].rows * sm.cls_groups[c];
+    if (a.auto_tc) {
+        // the tensor-core kernel takes the whole step when it is the faster one
+        __shared__ int s_tc;
+        if (tid == 0) s_tc = prefer_tc(a) ? 1 : 0;
+        __syncthreads();
+        if (s_tc) R = 0;
+        if (blockIdx.x == 0 && tid == 0) a.ws.sync[1] = 1u + (uint32_t)s_tc;
+    } else if (blockIdx.x == 0 && tid == 0) {
+        a.ws.sync[1] = 0u;
+    }
     const long long r_begin = R * blockIdx.x / gridDim.x;
     const long long r_end = R * (blockIdx.x + 1) / gridDim.x;
 

@@ -32,6 +32,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <climits>
+
 #include "../../include/moe_decode.h"
 #include "kernels.h"
 #include "tc_ptx.cuh"
@@ -48,7 +50,7 @@ constexpr int kTcRows = kTcBoxRows;               // 128
 constexpr int kChunkBytes = kTcRows * 128;        // 16 KB: one 64-column chunk
 constexpr int kAStage = 2 * kChunkBytes;          // 32 KB
 constexpr int kTcStages = 4;                      // weight ring
-constexpr int kTcTokens = 32;                     // tokens per group (hi + lo rows: N <= 64)
+constexpr int kTcTokens = kTcGroupTokens;         // tokens per group (hi + lo rows: N <= 64)
 constexpr int kTcMaxN = 2 * kTcTokens;
 constexpr int kBBlock = kTcMaxN * 128;            // activations of one K-block: N rows x 128 B
 constexpr int kBPair = 2 * kBBlock;               // ... of one K-pair
@@ -176,7 +178,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
     pdl_wait_primary();
 
     // ---- unit table: this kernel's units (>= min_tokens tokens), groups of kTcTokens;
-    // warp c filters class c ----
+    // warp c filters class c.  With auto_tc the kernel takes every unit when
+    // prefer_tc() holds and none otherwise (the CUDA-core kernel decides alike). ----
+    __shared__ int s_min_tok;
+    if (tid == 0) s_min_tok = a.f.auto_tc ? (prefer_tc(a.f) ? 1 : INT_MAX) : a.min_tokens;
+    __syncthreads();
+    const int min_tok = s_min_tok;
     if (warp < a.f.ncls) {
         int off = 0;
         for (int c = 0; c < warp; ++c) off += class_capacity(a.f.cls[c], a.f.n, a.f.g);
@@ -185,14 +192,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
             const UnitClass& uc = a.f.cls[c];
             int kept, groups;
             if (uc.kind == kUnitShared) {
-                const bool keep = a.f.T >= a.min_tokens;
+                const bool keep = a.f.T >= min_tok;
                 kept = keep ? 1 : 0;
                 groups = keep ? (a.f.T + kTcTokens - 1) / kTcTokens : 0;
                 if (lane == 0 && keep) sm.units[off] = make_int4(0, 0, a.f.T, groups);
             } else {
                 const int4* src = uc.kind == kUnitDept ? a.f.ws.dept_units : a.f.ws.exp_units;
                 const int A = uc.kind == kUnitDept ? a.f.ws.counts[1] : a.f.ws.counts[0];
-                kept = filter_units_warp(src, A, a.min_tokens, 1 << 30, kTcTokens, sm.units + off,
+                kept = filter_units_warp(src, A, min_tok, 1 << 30, kTcTokens, sm.units + off,
                                          &groups);
             }
             if (lane == 0) {

@@ -61,6 +61,8 @@ struct FfnArgs {
     int rows_shared_base; // ROWS mode: first shared-expert row
     int pdl;              // launch as a programmatic dependent
     int max_tokens;       // CUDA-core kernel: units with more tokens are skipped
+    int auto_tc;          // both kernels launched; they pick one by prefer_tc()
+    int sms;              // SMs of the device (grid of the tensor-core kernel)
 };
 
 // Capacity of a class's unit table (records the dispatch may have written).
@@ -76,13 +78,44 @@ struct TcArgs {
     int min_tokens;       // units with at least this many tokens
 };
 
-// Units with at least this many tokens run on the tensor cores (library
-// default: none; the caller opts in with moe_set_tc_min_tokens).
-constexpr int kTcMinTokens = 1 << 30;
 // Rows of one tensor-core weight tile / TMA box (unit rows must be a multiple),
-// and the hidden-size granularity of its down-projection stages.
+// the hidden-size granularity of its stages, and its tokens per group.
 constexpr int kTcBoxRows = 128;
 constexpr int kTcHiddenQuantum = 128;
+constexpr int kTcGroupTokens = 32;
+
+// Per-call choice between the two FFN kernels, made on the device from the
+// dispatch's unit records so that no host round trip is needed.  Both kernels
+// evaluate it on the same data and so agree.  Cost in weight rows streamed by
+// the busiest SM: the CUDA-core stream re-reads a unit's rows once per group
+// of kGroupTokens tokens and spreads rows evenly over the SMs; the tensor-core
+// kernel reads them once per kTcGroupTokens tokens but in whole 128-row tiles,
+// one SM per tile.  At d <= kTcWideHidden both stream at about the same rate
+// per SM, so the busiest SM's row count decides; on wider rows the CUDA-core
+// stream is measured about 4/3 slower per row and is weighted so.
+constexpr int kTcWideHidden = 4096;
+__device__ __forceinline__ bool prefer_tc(const FfnArgs& a) {
+    long long rows_cc = 0, tiles = 0;
+    for (int c = 0; c < a.ncls; ++c) {
+        const UnitClass& uc = a.cls[c];
+        int g_cc, g_tc;
+        if (uc.kind == kUnitShared) {
+            g_cc = (a.T + kGroupTokens - 1) / kGroupTokens;
+            g_tc = (a.T + kTcGroupTokens - 1) / kTcGroupTokens;
+        } else {
+            const bool dept = uc.kind == kUnitDept;
+            const int A = a.ws.counts[dept ? 1 : 0];
+            g_cc = A > 0 ? (dept ? a.ws.dept_units : a.ws.exp_units)[A - 1].w : 0;
+            g_tc = a.ws.counts[dept ? 3 : 2];
+        }
+        rows_cc += (long long)uc.rows * g_cc;
+        tiles += (long long)(uc.rows / kTcBoxRows) * g_tc;
+    }
+    const long long S = a.sms;
+    const long long tc_rows = (tiles + S - 1) / S * kTcBoxRows;
+    const long long cc_weight = a.d > kTcWideHidden ? 4 : 3;
+    return tiles > 0 && tc_rows * S * 3 < rows_cc * cc_weight;
+}
 
 struct CombineArgs {
     const float* rows;

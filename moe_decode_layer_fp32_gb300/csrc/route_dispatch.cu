@@ -30,6 +30,7 @@ struct DispatchSmem {
     int grp[kMaxN];                           // register groups -> group prefix
     int3 warp_tmp[32];
     int err;
+    int tc_groups;
 };
 
 // Rank of token t among the tokens set in a mask row (tokens ascending).
@@ -40,19 +41,26 @@ __device__ __forceinline__ int mask_rank(const uint32_t* row, int t) {
 }
 
 // Counts of `units` mask rows -> offsets, active lists and the FFN unit records.
+// Also writes the total of ceil(count / kTcGroupTokens) (tensor-core token groups).
 template <int NT>
 __device__ void unit_lists(const uint32_t* mask, int units, int W, int32_t* count_out,
                            int32_t* off_out, int32_t* act_out, int4* rec_out, int32_t* n_active,
-                           DispatchSmem& sm) {
+                           int32_t* tc_groups_out, DispatchSmem& sm) {
     const int tid = threadIdx.x;
+    if (tid == 0) sm.tc_groups = 0;
+    __syncthreads();
+    int tcg = 0;
     for (int u = tid; u < units; u += NT) {
         int c = 0;
         for (int w = 0; w < W; ++w) c += __popc(mask[u * W + w]);
         sm.cnt[u] = c;
         sm.act[u] = c > 0 ? 1 : 0;
         sm.grp[u] = (c + kGroupTokens - 1) / kGroupTokens;
+        tcg += (c + kTcGroupTokens - 1) / kTcGroupTokens;
         count_out[u] = c;
     }
+    tcg = warp_sum_int(tcg);
+    if ((tid & 31) == 0 && tcg) atomicAdd(&sm.tc_groups, tcg);
     __syncthreads();
     const int3 tot = block_exclusive_scan3<NT>(sm.cnt, sm.act, sm.grp, units, sm.warp_tmp);
     for (int u = tid; u < units; u += NT) {
@@ -68,6 +76,7 @@ __device__ void unit_lists(const uint32_t* mask, int units, int W, int32_t* coun
     if (tid == 0) {
         off_out[units] = tot.x;
         *n_active = tot.y;
+        *tc_groups_out = sm.tc_groups;
     }
 }
 
@@ -99,12 +108,14 @@ __device__ void dispatch_block(const int32_t* idx, const float* wts, int T, int 
             set_status(ws.status, kDevErrRouting);
             ws.counts[0] = 0;
             ws.counts[1] = 0;
+            ws.counts[2] = 0;
+            ws.counts[3] = 0;
         }
         return;
     }
     // ---- experts ----
     unit_lists<NT>(sm.emask, n, W, ws.exp_count, ws.exp_off, ws.act_exp, ws.exp_units,
-                   &ws.counts[0], sm);
+                   &ws.counts[0], &ws.counts[2], sm);
     for (int a = tid; a < TK; a += NT) {
         const int t = a / k;
         const int e = idx[a];
@@ -116,7 +127,10 @@ __device__ void dispatch_block(const int32_t* idx, const float* wts, int T, int 
     }
     __syncthreads();
     if (g <= 1) {
-        if (tid == 0) ws.counts[1] = 0;
+        if (tid == 0) {
+            ws.counts[1] = 0;
+            ws.counts[3] = 0;
+        }
         return;
     }
     // ---- departments: X^j = tokens that chose any expert of department j ----
@@ -129,7 +143,7 @@ __device__ void dispatch_block(const int32_t* idx, const float* wts, int T, int 
     }
     __syncthreads();
     unit_lists<NT>(sm.dmask, m, W, ws.dept_count, ws.dept_off, ws.act_dept, ws.dept_units,
-                   &ws.counts[1], sm);
+                   &ws.counts[1], &ws.counts[3], sm);
     for (int i = tid; i < m * T; i += NT) {
         const int j = i / T, t = i - (i / T) * T;
         const uint32_t* row = &sm.dmask[j * W];

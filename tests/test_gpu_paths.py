@@ -87,3 +87,67 @@ def test_dsv3_tc_sampled(B, threshold, T):
 def test_zipf_large_batch_tc(B, threshold, T):
     threshold(0)
     check_layer(B, synth.ZIPF_DEAMOE, T, seed=2, sample=list(range(0, T, 9)))
+
+
+def expected_auto_choice(shape, T, exp_count, dept_count, sms):
+    """Host restatement of the per-call kernel choice: 0 no choice (the step is
+    not eligible for the tensor-core kernel), 1 CUDA cores, 2 tensor cores."""
+    classes = []
+    if shape.I_sh > 0:
+        classes.append((shape.I_sh, dept_count))
+        if shape.I_pr > 0:
+            classes.append((shape.I_pr, exp_count))
+    else:
+        classes.append((shape.I, exp_count))
+    if shape.I_s > 0:
+        classes.append((shape.I_s, [T]))
+    if shape.dtype != "bf16" or shape.d % 128 or any(r % 128 for r, _ in classes):
+        return 0
+    wide = shape.d > 4096
+    if T <= 4 and not wide:
+        return 0
+    # launched only when some class expects more than 4 tokens per unit
+    expect = []
+    if shape.I_sh > 0:
+        miss = 1.0
+        for i in range(shape.k):
+            miss *= max(shape.n - shape.g - i, 0) / (shape.n - i)
+        expect.append(T * (1 - miss))
+    if shape.I_sh == 0 or shape.I_pr > 0:
+        expect.append(T * shape.k / shape.n)
+    if shape.I_s > 0:
+        expect.append(T)
+    if max(expect) <= 4 and not wide:
+        return 0
+    rows_cc = sum(r * sum(-(-int(c) // 4) for c in cnt) for r, cnt in classes)
+    tiles = sum(r // 128 * sum(-(-int(c) // 32) for c in cnt) for r, cnt in classes)
+    tc_rows = -(-tiles // sms) * 128
+    cc_weight = 4 if wide else 3
+    return 2 if tiles > 0 and tc_rows * sms * 3 < rows_cc * cc_weight else 1
+
+
+@pytest.mark.parametrize("shape,T", [(synth.VANILLA_128E, 16), (synth.VANILLA_128E, 4),
+                                     (synth.DEAMOE_7B, 16), (synth.DEAMOE_7B, 8),
+                                     (synth.DEAMOE_7B, 4), (synth.ZIPF_DEAMOE, 64),
+                                     (synth.DSV3_DEAMOE, 32), (synth.DSV3_VANILLA, 1)])
+def test_auto_choice_matches_cost_model(B, threshold, shape, T):
+    """Default mode: the FFN kernels pick one path per call on the device;
+    the choice they record equals the cost model evaluated on the host from
+    the same dispatch counts, and the output stays at parity (checked by
+    test_gpu_parity in the same mode)."""
+    threshold(0)
+    L = synth.make_layer(shape, 7, DEV)
+    x = synth.hidden(T, shape.d, 7, DEV)
+    ws, _, _, _ = H.run_layer_forward(B, shape, L, x)
+    torch.cuda.synchronize()
+    g = shape.g if shape.I_sh > 0 else 1
+    lists = H.dispatch_lists(B, ws, T, shape.n, shape.k, g)
+    lay = B.moe_workspace_layout(T, shape.n, shape.k, g)
+    got = int(ws.cpu()[lay["sync"] + 4: lay["sync"] + 8].view(torch.int32)[0])
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    want = expected_auto_choice(shape, T, lists["exp_count"], lists.get("dept_count", []), sms)
+    assert got == want
+    if (shape, T) == (synth.DEAMOE_7B, 16):
+        assert want == 2          # dense department backbones: tensor cores
+    if (shape, T) == (synth.VANILLA_128E, 16):
+        assert want == 0          # ~1 token per expert expected: tensor cores not launched
