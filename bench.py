@@ -375,7 +375,7 @@ def run_ours(args, rank, world, local):
                 "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "us_per_launch": round(t_ffn / ffn_launches * 1e6, 2),
                 "algorithmic_bytes_per_launch": int(sum(W.ffn_bytes.values()) / (R * len(batches))),
-                "traffic": None}
+                "traffic": load_traffic(args.workload) if not args.batches else None}
 
     # end to end through the C ABI with host buffers (copies inside the timed region)
     e2e = None
@@ -437,6 +437,22 @@ def run_ours(args, rank, world, local):
     }
     if rank == 0:
         print(json.dumps(out))
+
+
+def load_traffic(workload: str):
+    """DRAM bytes per FFN launch of this workload from the committed ncu
+    summaries (profiles/*.md: `traffic_bytes_per_launch[<workload>]: N`), or
+    None when no capture of the current kernels exists for it."""
+    import glob
+    import re
+    pat = re.compile(r"^traffic_bytes_per_launch\[" + re.escape(workload) + r"\]:\s*(\d+)\s*$")
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        with open(path) as f:
+            for line in f:
+                m = pat.match(line.strip())
+                if m:
+                    return int(m.group(1))
+    return None
 
 
 def load_peaks():
