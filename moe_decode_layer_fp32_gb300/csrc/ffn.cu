@@ -107,6 +107,70 @@ __device__ __forceinline__ bool next_seg(const FfnArgs& a, const FfnSmem<NS>& sm
     return true;
 }
 
+// Work-balanced split of the row space.  A row of a group of mg tokens costs
+// kRowCost + mg: the weight stream is the same for every row, but the
+// per-token dot products, reductions and accumulations grow with mg (a CTA
+// whose rows all carry 4 tokens was measured 1.5x slower than one whose rows
+// carry 1).  Within a class the units' costs follow from the dispatch records
+// alone: unit q (t tokens, G = ceil(t / kMT) groups) costs
+// rows * (kRowCost * G + t), and the records carry the exclusive token prefix
+// (.y) and the inclusive group prefix (.w).
+constexpr long long kRowCost = 5;
+
+__device__ __forceinline__ long long class_tokens(const int4* u, int nu) {
+    return nu > 0 ? (long long)u[nu - 1].y + u[nu - 1].z - u[0].y : 0;
+}
+
+template <int NS>
+__device__ __noinline__ long long split_total_cost(const FfnArgs& a, const FfnSmem<NS>& sm) {
+    long long tot = 0;
+    for (int c = 0; c < a.ncls; ++c) {
+        const int4* u = sm.units + sm.cls_off[c];
+        tot += (long long)a.cls[c].rows *
+               (kRowCost * sm.cls_groups[c] + class_tokens(u, sm.cls_units[c]));
+    }
+    return tot;
+}
+
+// Row-space position whose cost prefix is C (rounded down to a whole row).
+template <int NS>
+__device__ __noinline__ long long split_row_at(const FfnArgs& a, const FfnSmem<NS>& sm, long long C) {
+    long long row_base = 0;
+    for (int c = 0; c < a.ncls; ++c) {
+        const int rows = a.cls[c].rows;
+        const int nu = sm.cls_units[c];
+        const int4* u = sm.units + sm.cls_off[c];
+        const long long cc = (long long)rows * (kRowCost * sm.cls_groups[c] + class_tokens(u, nu));
+        if (C < cc || c == a.ncls - 1) {
+            if (nu == 0) return row_base;
+            if (C >= cc) return row_base + (long long)rows * sm.cls_groups[c];
+            auto pre = [&](int q) {  // cost of the units before q
+                const long long g = q > 0 ? u[q - 1].w : 0;
+                return (long long)rows * (kRowCost * g + (u[q].y - u[0].y));
+            };
+            int lo = 0, hi = nu - 1;    // last q with pre(q) <= C
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (pre(mid) <= C) lo = mid; else hi = mid - 1;
+            }
+            const int t = u[lo].z;
+            const int G = (t + kMT - 1) / kMT;
+            const long long Cq = C - pre(lo);
+            const long long full = (long long)rows * (kRowCost + kMT);
+            long long g = Cq / full;
+            if (g > G - 1) g = G - 1;
+            const int mg = min(kMT, t - (int)g * kMT);
+            long long i = (Cq - g * full) / (kRowCost + mg);
+            if (i > rows) i = rows;
+            const long long gpre = lo > 0 ? u[lo - 1].w : 0;
+            return row_base + (gpre + g) * rows + i;
+        }
+        C -= cc;
+        row_base += (long long)rows * sm.cls_groups[c];
+    }
+    return row_base;
+}
+
 // Tokens of a group: token id, weight and output row (ROWS or ACCUM mode).
 __device__ __forceinline__ int group_tokens(const FfnArgs& a, const int4 rec, int kind, int grp,
                                             int (&tok)[kMT], float (&wt)[kMT], int (&orow)[kMT]) {
@@ -322,8 +386,29 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
     } else if (blockIdx.x == 0 && tid == 0) {
         a.ws.sync[1] = 0u;
     }
-    const long long r_begin = R * blockIdx.x / gridDim.x;
-    const long long r_end = R * (blockIdx.x + 1) / gridDim.x;
+    // CTA's share: equal work (rows weighted by their tokens) when the unit
+    // table is the dispatch's own (token prefixes valid), equal rows otherwise
+    long long r_begin = R * blockIdx.x / gridDim.x;
+    long long r_end = R * (blockIdx.x + 1) / gridDim.x;
+    if (R > 0 && a.max_tokens >= a.T) {
+        // every group holding one token (e.g. T = 1) makes the cost uniform per row
+        long long groups = 0, tokens = 0;
+        for (int c = 0; c < a.ncls; ++c) {
+            groups += sm.cls_groups[c];
+            tokens += class_tokens(sm.units + sm.cls_off[c], sm.cls_units[c]);
+        }
+        if (tokens != groups) {
+            __shared__ long long s_split[2];
+            if (tid == 0 || tid == 32) {
+                const long long tot = split_total_cost(a, sm);
+                const unsigned b = blockIdx.x + (tid ? 1u : 0u);
+                s_split[tid ? 1 : 0] = b == gridDim.x ? R : split_row_at(a, sm, tot * b / gridDim.x);
+            }
+            __syncthreads();
+            r_begin = s_split[0];
+            r_end = s_split[1];
+        }
+    }
 
     const int row_bytes = a.d * K::kBw;
     const int rps = min(RMAX, kStageBytes / row_bytes);   // rows per stage
