@@ -21,6 +21,7 @@ constexpr int kRouteThreads = 512;
 constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kDispatchThreads = 512;
 constexpr int kMaskWords = (kMaxT + 31) / 32;
+constexpr int kStagedAssignments = 1024;   // T*k staged in shared memory for the fused dispatch
 
 struct DispatchSmem {
     uint32_t emask[kMaxN * kMaskWords];       // expert -> token bitmask
@@ -47,8 +48,6 @@ __device__ void unit_lists(const uint32_t* mask, int units, int W, int32_t* coun
                            int32_t* off_out, int32_t* act_out, int4* rec_out, int32_t* n_active,
                            int32_t* tc_groups_out, DispatchSmem& sm) {
     const int tid = threadIdx.x;
-    if (tid == 0) sm.tc_groups = 0;
-    __syncthreads();
     int tcg = 0;
     for (int u = tid; u < units; u += NT) {
         int c = 0;
@@ -60,7 +59,7 @@ __device__ void unit_lists(const uint32_t* mask, int units, int W, int32_t* coun
         count_out[u] = c;
     }
     tcg = warp_sum_int(tcg);
-    if ((tid & 31) == 0 && tcg) atomicAdd(&sm.tc_groups, tcg);
+    if ((tid & 31) == 0 && tcg) atomicAdd(&sm.tc_groups, tcg);   // zeroed by the caller
     __syncthreads();
     const int3 tot = block_exclusive_scan3<NT>(sm.cnt, sm.act, sm.grp, units, sm.warp_tmp);
     for (int u = tid; u < units; u += NT) {
@@ -89,7 +88,10 @@ __device__ void dispatch_block(const int32_t* idx, const float* wts, int T, int 
     const int W = (T + 31) >> 5;
     const int TK = T * k;
     for (int i = tid; i < n * W; i += NT) sm.emask[i] = 0u;
-    if (tid == 0) sm.err = 0;
+    if (tid == 0) {
+        sm.err = 0;
+        sm.tc_groups = 0;
+    }
     __syncthreads();
     for (int a = tid; a < TK; a += NT) {
         const int t = a / k;
@@ -135,6 +137,7 @@ __device__ void dispatch_block(const int32_t* idx, const float* wts, int T, int 
     }
     // ---- departments: X^j = tokens that chose any expert of department j ----
     const int m = n / g;
+    if (tid == 0) sm.tc_groups = 0;   // ordered before its use by the barrier below
     for (int i = tid; i < m * W; i += NT) {
         const int j = i / W, w = i - (i / W) * W;
         uint32_t v = 0u;
@@ -166,62 +169,69 @@ __device__ void dispatch_block(const int32_t* idx, const float* wts, int T, int 
 // Top-k of one token's keys (logit + bias) by one warp; lane holds experts
 // lane + 32*j.  Descending key, equal keys -> lower expert index first.  The
 // weights are scale * softmax over the selected unbiased logits.
+//
+// Keys are mapped to unsigned integers that order like the floats (-0 folded
+// into +0 so that it ties with +0, as a float comparison does).  Each round
+// takes the warp maximum of the lanes' best remaining keys and then the
+// smallest expert index holding it, both with single-instruction warp
+// reductions.  0 marks a taken (or absent) entry; NaN and -inf keys map below
+// every finite key, and picking one flags the routing as bad.
+__device__ __forceinline__ uint32_t ordered_key(float v) {
+    if (v == 0.0f) v = 0.0f;
+    const uint32_t b = __float_as_uint(v);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
 template <int J>
 __device__ void topk_warp(const float* logits_row, const float* bias, int n, int k, float scale,
-                          int32_t* idx_out, float* w_out, int32_t* status) {
+                          int32_t* idx_out, float* w_out, int32_t* status, int32_t* idx_sm,
+                          float* w_sm) {
     const int lane = threadIdx.x & 31;
-    float key[J], lg[J];
+    constexpr uint32_t kLowest = 0x007fffffu;   // ordered_key(-inf)
+    uint32_t key[J];
+    float lg[J];
 #pragma unroll
     for (int j = 0; j < J; ++j) {
         const int e = lane + 32 * j;
+        lg[j] = 0.0f;
+        key[j] = 0u;
         if (e < n) {
             const float l = __ldcg(logits_row + e);
+            const float kv = bias ? l + __ldg(bias + e) : l;
             lg[j] = l;
-            key[j] = bias ? l + __ldg(bias + e) : l;
-        } else {
-            lg[j] = 0.0f;
-            key[j] = -INFINITY;
+            // finite keys rank above kLowest; -inf and NaN take kLowest (still
+            // selectable, after every finite key, lowest index first)
+            key[j] = (kv == kv && kv != -INFINITY) ? ordered_key(kv) : kLowest;
         }
     }
-    uint32_t taken = 0u;
     int my_idx = 0;
     float my_lg = 0.0f;
     bool bad = false;
     for (int r = 0; r < k; ++r) {
-        float bk = -INFINITY;
-        int bi = INT_MAX;
+        uint32_t bk = 0u;
+        int bj = 0;
 #pragma unroll
-        for (int j = 0; j < J; ++j) {
-            const int e = lane + 32 * j;
-            if (e < n && !((taken >> j) & 1u)) {
-                if (key[j] > bk || (key[j] == bk && e < bi)) {
-                    bk = key[j];
-                    bi = e;
-                }
+        for (int j = 0; j < J; ++j)
+            if (key[j] > bk) {
+                bk = key[j];
+                bj = j;
             }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ok > bk || (ok == bk && oi < bi)) {
-                bk = ok;
-                bi = oi;
-            }
-        }
-        if (bi == INT_MAX) {  // only non-finite keys left
-            bad = true;
-            bi = 0;
-        }
-        const int owner = bi & 31, jb = bi >> 5;
+        const uint32_t top = __reduce_max_sync(0xffffffffu, bk);
+        const uint32_t cand = (bk == top && top != 0u) ? (uint32_t)(lane + 32 * bj) : 0xffffffffu;
+        const uint32_t bi = __reduce_min_sync(0xffffffffu, cand);
+        if (top <= kLowest) bad = true;   // a non-finite key (or none) was selected
+        const int e = bi == 0xffffffffu ? 0 : (int)bi;
+        const int owner = e & 31, jb = e >> 5;
         float v = 0.0f;
 #pragma unroll
         for (int j = 0; j < J; ++j)
-            if (j == jb) v = lg[j];
-        if (lane == owner) taken |= 1u << jb;
+            if (j == jb) {
+                v = lg[j];
+                if (lane == owner) key[j] = 0u;
+            }
         v = __shfl_sync(0xffffffffu, v, owner);
         if (lane == r) {
-            my_idx = bi;
+            my_idx = e;
             my_lg = v;
         }
     }
@@ -231,17 +241,23 @@ __device__ void topk_warp(const float* logits_row, const float* bias, int n, int
     const float ex = lane < k ? expf(my_lg - mx) : 0.0f;
     const float s = warp_sum(ex);
     if (lane < k) {
+        const float wv = scale * (ex / s);
         idx_out[lane] = my_idx;
-        w_out[lane] = scale * (ex / s);
+        w_out[lane] = wv;
+        if (idx_sm) {
+            idx_sm[lane] = my_idx;
+            w_sm[lane] = wv;
+        }
     }
     if (bad && lane == 0) set_status(status, kDevErrRouting);
 }
 
 template <int J>
-__device__ __forceinline__ void topk_rows(const RouteArgs& a, int warp) {
+__device__ __forceinline__ void topk_rows(const RouteArgs& a, int warp, int32_t* idx_sm, float* w_sm) {
     for (int t = warp; t < a.T; t += kRouteWarps)
         topk_warp<J>(a.ws.logits + (size_t)t * a.n, a.bias, a.n, a.k, a.scale,
-                     a.topk_idx + (size_t)t * a.k, a.topk_w + (size_t)t * a.k, a.ws.status);
+                     a.topk_idx + (size_t)t * a.k, a.topk_w + (size_t)t * a.k, a.ws.status,
+                     idx_sm ? idx_sm + t * a.k : nullptr, idx_sm ? w_sm + t * a.k : nullptr);
 }
 
 // Router logits: block e computes expert e's logit for every token; each
@@ -252,6 +268,8 @@ __device__ __forceinline__ void topk_rows(const RouteArgs& a, int warp) {
 template <int RCH>
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
     __shared__ DispatchSmem sm;
+    __shared__ int32_t s_idx[kStagedAssignments];   // top-k results for the fused dispatch
+    __shared__ float s_w[kStagedAssignments];
     __shared__ float red[kRouteWarps][8];
     __shared__ int s_last;
     // Let the FFN grid (launched as a programmatic dependent) start its prologue.
@@ -310,22 +328,28 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
         }
         __syncthreads();
     }
-    __threadfence();
-    if (tid == 0) s_last = atomicAdd(&a.ws.sync[0], 1u) == gridDim.x - 1;
+    // Count this block in.  The counter add is a GPU-scope release/acquire:
+    // it publishes the block's logits (ordered before it by the CTA barrier
+    // above) and lets the last block to arrive see every block's logits
+    // (ordered for its other threads by the barrier below).
+    if (tid == 0) s_last = atomic_add_acq_rel_gpu(&a.ws.sync[0], 1u) == gridDim.x - 1;
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
     const int J = (a.n + 31) / 32;
-    if (J <= 1) topk_rows<1>(a, warp);
-    else if (J <= 2) topk_rows<2>(a, warp);
-    else if (J <= 4) topk_rows<4>(a, warp);
-    else if (J <= 8) topk_rows<8>(a, warp);
-    else if (J <= 16) topk_rows<16>(a, warp);
-    else topk_rows<32>(a, warp);
+    // the fused dispatch reads the top-k results from shared memory when they fit
+    const bool staged = a.fuse_dispatch && a.T * a.k <= kStagedAssignments;
+    int32_t* idx_sm = staged ? s_idx : nullptr;
+    if (J <= 1) topk_rows<1>(a, warp, idx_sm, s_w);
+    else if (J <= 2) topk_rows<2>(a, warp, idx_sm, s_w);
+    else if (J <= 4) topk_rows<4>(a, warp, idx_sm, s_w);
+    else if (J <= 8) topk_rows<8>(a, warp, idx_sm, s_w);
+    else if (J <= 16) topk_rows<16>(a, warp, idx_sm, s_w);
+    else topk_rows<32>(a, warp, idx_sm, s_w);
     if (tid == 0) a.ws.sync[0] = 0u;  // ready for the next call
     if (a.fuse_dispatch) {
         __syncthreads();
-        dispatch_block<kRouteThreads>(a.topk_idx, a.topk_w, a.T, a.n, a.k, a.g, a.ws, sm);
+        dispatch_block<kRouteThreads>(staged ? s_idx : a.topk_idx, staged ? s_w : a.topk_w, a.T, a.n,
+                                      a.k, a.g, a.ws, sm);
     }
 }
 
