@@ -287,7 +287,11 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
             y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 
-    const int e = blockIdx.x;
+    // block = (expert e, block of 8 tokens); blocks of one expert are adjacent
+    // so that its router row is read from HBM once and then from L2
+    const int tblocks = (a.T + 7) >> 3;
+    const int e = blockIdx.x / tblocks;
+    const int tb = blockIdx.x - e * tblocks;
     const int d4 = a.d >> 2;
     const float4* wr = reinterpret_cast<const float4*>(a.w_router + (size_t)e * a.d);
     float4 w[RCH];
@@ -296,7 +300,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
         const int c = tid + i * kRouteThreads;
         w[i] = c < d4 ? __ldg(wr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    for (int t0 = 0; t0 < a.T; t0 += 8) {
+    {
+        const int t0 = tb * 8;
         float acc[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -363,7 +368,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
     // float4 chunks of a router row per thread: ceil(d / 4 / threads)
     const int rch = (a.d / 4 + kRouteThreads - 1) / kRouteThreads;
-    const int blocks = a.n;
+    const int blocks = a.n * ((a.T + 7) / 8);
     if (rch <= 1) route_kernel<1><<<blocks, kRouteThreads, 0, s>>>(a);
     else if (rch <= 2) route_kernel<2><<<blocks, kRouteThreads, 0, s>>>(a);
     else route_kernel<4><<<blocks, kRouteThreads, 0, s>>>(a);
