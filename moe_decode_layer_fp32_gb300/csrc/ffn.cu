@@ -86,9 +86,9 @@ __device__ __forceinline__ bool next_seg(const FfnArgs& a, const FfnSmem<NS>& sm
         ++c;
     }
     const int rows = a.cls[c].rows;
-    const long long rel = r - base;
-    const int vg = (int)(rel / rows);
-    const int rin = (int)(rel - (long long)vg * rows);
+    const int rel = (int)(r - base);       // row spaces stay far below 2^31
+    const int vg = rel / rows;
+    const int rin = rel - vg * rows;
     const int4* u = sm.units + sm.cls_off[c];
     int lo = 0, hi = sm.cls_units[c] - 1;  // first q whose group prefix exceeds vg
     while (lo < hi) {
@@ -115,14 +115,14 @@ __device__ __forceinline__ bool next_seg(const FfnArgs& a, const FfnSmem<NS>& sm
 // alone: unit q (t tokens, G = ceil(t / kMT) groups) costs
 // rows * (kRowCost * G + t), and the records carry the exclusive token prefix
 // (.y) and the inclusive group prefix (.w).
-constexpr long long kRowCost = 5;
+constexpr int kRowCost = 5;
 
-__device__ __forceinline__ long long class_tokens(const int4* u, int nu) {
-    return nu > 0 ? (long long)u[nu - 1].y + u[nu - 1].z - u[0].y : 0;
+__device__ __forceinline__ int class_tokens(const int4* u, int nu) {
+    return nu > 0 ? u[nu - 1].y + u[nu - 1].z - u[0].y : 0;
 }
 
 template <int NS>
-__device__ __noinline__ long long split_total_cost(const FfnArgs& a, const FfnSmem<NS>& sm) {
+__device__ __forceinline__ long long split_total_cost(const FfnArgs& a, const FfnSmem<NS>& sm) {
     long long tot = 0;
     for (int c = 0; c < a.ncls; ++c) {
         const int4* u = sm.units + sm.cls_off[c];
@@ -133,20 +133,21 @@ __device__ __noinline__ long long split_total_cost(const FfnArgs& a, const FfnSm
 }
 
 // Row-space position whose cost prefix is C (rounded down to a whole row).
+// 32-bit arithmetic throughout (the caller keeps the total cost below 2^31).
 template <int NS>
-__device__ __noinline__ long long split_row_at(const FfnArgs& a, const FfnSmem<NS>& sm, long long C) {
-    long long row_base = 0;
+__device__ __forceinline__ int split_row_at(const FfnArgs& a, const FfnSmem<NS>& sm, int C) {
+    int row_base = 0;
     for (int c = 0; c < a.ncls; ++c) {
         const int rows = a.cls[c].rows;
         const int nu = sm.cls_units[c];
         const int4* u = sm.units + sm.cls_off[c];
-        const long long cc = (long long)rows * (kRowCost * sm.cls_groups[c] + class_tokens(u, nu));
+        const int cc = rows * (kRowCost * sm.cls_groups[c] + class_tokens(u, nu));
         if (C < cc || c == a.ncls - 1) {
             if (nu == 0) return row_base;
-            if (C >= cc) return row_base + (long long)rows * sm.cls_groups[c];
+            if (C >= cc) return row_base + rows * sm.cls_groups[c];
             auto pre = [&](int q) {  // cost of the units before q
-                const long long g = q > 0 ? u[q - 1].w : 0;
-                return (long long)rows * (kRowCost * g + (u[q].y - u[0].y));
+                const int g = q > 0 ? u[q - 1].w : 0;
+                return rows * (kRowCost * g + (u[q].y - u[0].y));
             };
             int lo = 0, hi = nu - 1;    // last q with pre(q) <= C
             while (lo < hi) {
@@ -155,18 +156,16 @@ __device__ __noinline__ long long split_row_at(const FfnArgs& a, const FfnSmem<N
             }
             const int t = u[lo].z;
             const int G = (t + kMT - 1) / kMT;
-            const long long Cq = C - pre(lo);
-            const long long full = (long long)rows * (kRowCost + kMT);
-            long long g = Cq / full;
-            if (g > G - 1) g = G - 1;
-            const int mg = min(kMT, t - (int)g * kMT);
-            long long i = (Cq - g * full) / (kRowCost + mg);
-            if (i > rows) i = rows;
-            const long long gpre = lo > 0 ? u[lo - 1].w : 0;
+            const int Cq = C - pre(lo);
+            const int full = rows * (kRowCost + kMT);
+            const int g = min(Cq / full, G - 1);
+            const int mg = min(kMT, t - g * kMT);
+            const int i = min((Cq - g * full) / (kRowCost + mg), rows);
+            const int gpre = lo > 0 ? u[lo - 1].w : 0;
             return row_base + (gpre + g) * rows + i;
         }
         C -= cc;
-        row_base += (long long)rows * sm.cls_groups[c];
+        row_base += rows * sm.cls_groups[c];
     }
     return row_base;
 }
@@ -388,8 +387,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
     }
     // CTA's share: equal work (rows weighted by their tokens) when the unit
     // table is the dispatch's own (token prefixes valid), equal rows otherwise
-    long long r_begin = R * blockIdx.x / gridDim.x;
-    long long r_end = R * (blockIdx.x + 1) / gridDim.x;
+    long long r_begin = grid_share(R, blockIdx.x, gridDim.x, a.grid_magic);
+    long long r_end = grid_share(R, blockIdx.x + 1, gridDim.x, a.grid_magic);
     if (R > 0 && a.max_tokens >= a.T) {
         // every group holding one token (e.g. T = 1) makes the cost uniform per row
         long long groups = 0, tokens = 0;
@@ -399,14 +398,18 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
         }
         if (tokens != groups) {
             __shared__ long long s_split[2];
-            if (tid == 0 || tid == 32) {
-                const long long tot = split_total_cost(a, sm);
-                const unsigned b = blockIdx.x + (tid ? 1u : 0u);
-                s_split[tid ? 1 : 0] = b == gridDim.x ? R : split_row_at(a, sm, tot * b / gridDim.x);
+            const long long tot = split_total_cost(a, sm);
+            if (tot < (1ll << 31)) {
+                if (tid == 0 || tid == 32) {
+                    const unsigned b = blockIdx.x + (tid ? 1u : 0u);
+                    s_split[tid ? 1 : 0] =
+                        b == gridDim.x ? R
+                                       : split_row_at(a, sm, (int)grid_share(tot, b, gridDim.x, a.grid_magic));
+                }
+                __syncthreads();
+                r_begin = s_split[0];
+                r_end = s_split[1];
             }
-            __syncthreads();
-            r_begin = s_split[0];
-            r_end = s_split[1];
         }
     }
 
@@ -602,8 +605,11 @@ cudaError_t launch_ffn_t(const FfnArgs& a, cudaStream_t s) {
     const size_t smem = (size_t)NS * kStageBytes + sizeof(FfnSmem<NS>) + (size_t)units * sizeof(int4);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)(device_sm_count() * CPS);
+    FfnArgs args = a;
+    args.grid_magic = grid_magic_of(grid);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(device_sm_count() * CPS, 1, 1);
+    cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3((NCW + 1) * 32, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -612,7 +618,7 @@ cudaError_t launch_ffn_t(const FfnArgs& a, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = a.pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    return cudaLaunchKernelEx(&cfg, kern, args);
 }
 
 // ---- combine: y[t] = sum of the token's rows with their weights, fixed order ----

@@ -214,8 +214,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
     // CTA's share of the row space, in whole tiles
     int Q = 0;
     for (int c = 0; c < a.f.ncls; ++c) Q += a.f.cls[c].rows / kTcRows * sm.cls_groups[c];
-    const int r_begin = (int)((long long)Q * blockIdx.x / gridDim.x) * kTcRows;
-    const int r_end = (int)((long long)Q * (blockIdx.x + 1) / gridDim.x) * kTcRows;
+    const int r_begin = (int)grid_share(Q, blockIdx.x, gridDim.x, a.f.grid_magic) * kTcRows;
+    const int r_end = (int)grid_share(Q, blockIdx.x + 1, gridDim.x, a.f.grid_magic) * kTcRows;
 
     bool ok = true;
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -505,8 +505,11 @@ cudaError_t launch_ffn_tc(const TcArgs& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(ffn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)device_sm_count();
+    TcArgs args = a;
+    args.f.grid_magic = grid_magic_of(grid);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(device_sm_count(), 1, 1);
+    cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(kTcThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -515,7 +518,7 @@ cudaError_t launch_ffn_tc(const TcArgs& a, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, ffn_tc_kernel, a);
+    return cudaLaunchKernelEx(&cfg, ffn_tc_kernel, args);
 }
 
 }  // namespace moe

@@ -63,7 +63,23 @@ struct FfnArgs {
     int max_tokens;       // CUDA-core kernel: units with more tokens are skipped
     int auto_tc;          // both kernels launched; they pick one by prefer_tc()
     int sms;              // SMs of the device (grid of the tensor-core kernel)
+    unsigned long long grid_magic;   // set by the launcher: ceil(2^64 / grid)
 };
+
+// ceil(2^64 / g) for g >= 2 (2^64 / g when g divides it); grid_share() divides
+// by g with it.
+inline unsigned long long grid_magic_of(unsigned g) {
+    return g <= 1 ? 0ull : ~0ull / g + 1ull;
+}
+// floor(x * b / g) for x * b < 2^40 and g = gridDim.x, without a 64-bit
+// division (a long software routine on the GPU).  Exact: the product with
+// the rounded-up reciprocal errs by less than x * b / 2^64, below the 1/g
+// gap between a non-integer quotient and the next integer.
+__device__ __forceinline__ long long grid_share(long long x, unsigned b, unsigned g,
+                                                unsigned long long magic) {
+    if (g <= 1) return b ? x : 0;
+    return (long long)__umul64hi((unsigned long long)x * b, magic);
+}
 
 // Capacity of a class's unit table (records the dispatch may have written).
 __host__ __device__ __forceinline__ int class_capacity(const UnitClass& c, int n, int g) {
@@ -112,7 +128,7 @@ __device__ __forceinline__ bool prefer_tc(const FfnArgs& a) {
         tiles += (long long)(uc.rows / kTcBoxRows) * g_tc;
     }
     const long long S = a.sms;
-    const long long tc_rows = (tiles + S - 1) / S * kTcBoxRows;
+    const long long tc_rows = (long long)((unsigned)(tiles + S - 1) / (unsigned)S) * kTcBoxRows;
     const long long cc_weight = a.d > kTcWideHidden ? 4 : 3;
     return tiles > 0 && tc_rows * S * 3 < rows_cc * cc_weight;
 }
