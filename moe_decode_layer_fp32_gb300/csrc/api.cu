@@ -583,9 +583,14 @@ int moe_combine(const float* rows, int T, int d, int n, int k, int experts_per_d
     return MOE_OK;
 }
 
+// Routing step of the whole-layer path.  With `local` the routing kernel
+// writes the logits only and the CUDA-core FFN kernel (a.local_route) takes
+// the top-k and builds the dispatch in every CTA; otherwise the routing
+// kernel's last block does both for the FFN kernels to read.
 static int layer_route(const float* x, int T, int d, int n, int k, float scale, const float* w_router,
                        const float* bias, int g, const moe_ws_layout& L, void* ws, int32_t* topk_idx,
-                       float* topk_w, float* y, bool split_x, void* stream, const char* who) {
+                       float* topk_w, float* y, bool split_x, bool local, moe::FfnArgs& a,
+                       void* stream, const char* who) {
     if (!w_router || !aligned16(w_router)) return fail(MOE_ERR_INVALID_ARG, "%s: w_router null or unaligned", who);
     if (!topk_idx || !topk_w) return fail(MOE_ERR_INVALID_ARG, "%s: routing outputs are null", who);
     moe::RouteArgs r = {};
@@ -597,11 +602,19 @@ static int layer_route(const float* x, int T, int d, int n, int k, float scale, 
     r.topk_idx = topk_idx;
     r.topk_w = topk_w;
     r.ws = resolve(ws, L);
-    r.fuse_dispatch = 1;
     r.g = g;
     r.y_zero = y;
     r.y_elems = (long long)T * d;
     r.split_x = split_x ? 1 : 0;
+    r.fuse_dispatch = local ? 0 : 1;
+    r.logits_only = local ? 1 : 0;
+    if (local) {
+        a.local_route = 1;
+        a.bias = bias;
+        a.scale = scale;
+        a.topk_idx = topk_idx;
+        a.topk_w = topk_w;
+    }
     cudaError_t e = moe::launch_route(r, as_stream(stream));
     if (e != cudaSuccess) return cuda_fail(e, who);
     return MOE_OK;
@@ -621,8 +634,9 @@ int moe_layer_forward(const float* x, int T, int d, int n, int k, float scale,
     layout_of(T, n, k, 1, &L);
     moe::TcArgs t;
     const bool tc = prepare_tc(a, T, &t);
+    const bool local = !tc && moe::ffn_local_route_fits(a);
     if ((rc = layer_route(x, T, d, n, k, scale, w_router, bias, 1, L, ws, topk_idx, topk_w, y, tc,
-                          stream, who)))
+                          local, a, stream, who)))
         return rc;
     return run_ffn(a, T, n, k, 1, I_s > 0, tc, t, true, stream, who);
 }
@@ -644,8 +658,9 @@ int deamoe_layer_forward(const float* x, int T, int d, int n, int k, float scale
     layout_of(T, n, k, experts_per_dept, &L);
     moe::TcArgs t;
     const bool tc = prepare_tc(a, T, &t);
+    const bool local = !tc && moe::ffn_local_route_fits(a);
     if ((rc = layer_route(x, T, d, n, k, scale, w_router, bias, experts_per_dept, L, ws, topk_idx,
-                          topk_w, y, tc, stream, who)))
+                          topk_w, y, tc, local, a, stream, who)))
         return rc;
     return run_ffn(a, T, n, k, experts_per_dept, I_s > 0, tc, t, true, stream, who);
 }

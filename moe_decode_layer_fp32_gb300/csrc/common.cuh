@@ -236,6 +236,91 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// ---- routing: top-k of one token by one warp --------------------------------
+// Router of "DeaMoE: Efficient MoE Structure for Fast Small-Batch Decoding"
+// §2.1 eqs. (2)-(3): the k largest keys (logit + selection bias of "DeepSeekMoE
+// Guide", routing-bias formulation), descending, equal keys -> lower expert
+// index first; weights = scale * softmax over the selected unbiased logits.
+//
+// Keys are mapped to unsigned integers that order like the floats (-0 folded
+// into +0 so that it ties with +0, as a float comparison does).  Each round
+// takes the warp maximum of the lanes' best remaining keys and then the
+// smallest expert index holding it, both with single-instruction warp
+// reductions.  0 marks a taken (or absent) entry; NaN and -inf keys map below
+// every finite key, and picking one flags the routing as bad.
+__device__ __forceinline__ uint32_t ordered_key(float v) {
+    if (v == 0.0f) v = 0.0f;
+    const uint32_t b = __float_as_uint(v);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// Lane holds experts lane + 32*j of logits_row[0..n) (J*32 >= n, k <= n).
+// On return lane r < k holds the r-th selected expert and its weight; the
+// result (same on every lane) says whether a non-finite key was selected.
+template <int J>
+__device__ __forceinline__ bool topk_select_warp(const float* logits_row, const float* bias, int n,
+                                                 int k, float scale, int& out_idx, float& out_w) {
+    const int lane = threadIdx.x & 31;
+    constexpr uint32_t kLowest = 0x007fffffu;   // ordered_key(-inf)
+    uint32_t key[J];
+    float lg[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const int e = lane + 32 * j;
+        lg[j] = 0.0f;
+        key[j] = 0u;
+        if (e < n) {
+            const float l = __ldcg(logits_row + e);
+            const float kv = bias ? l + __ldg(bias + e) : l;
+            lg[j] = l;
+            // finite keys rank above kLowest; -inf and NaN take kLowest (still
+            // selectable, after every finite key, lowest index first)
+            key[j] = (kv == kv && kv != -INFINITY) ? ordered_key(kv) : kLowest;
+        }
+    }
+    int my_idx = 0;
+    float my_lg = 0.0f;
+    bool bad = false;
+    for (int r = 0; r < k; ++r) {
+        uint32_t bk = 0u;
+        int bj = 0;
+#pragma unroll
+        for (int j = 0; j < J; ++j)
+            if (key[j] > bk) {
+                bk = key[j];
+                bj = j;
+            }
+        const uint32_t top = __reduce_max_sync(0xffffffffu, bk);
+        const uint32_t cand = (bk == top && top != 0u) ? (uint32_t)(lane + 32 * bj) : 0xffffffffu;
+        const uint32_t bi = __reduce_min_sync(0xffffffffu, cand);
+        if (top <= kLowest) bad = true;   // a non-finite key (or none) was selected
+        const int e = bi == 0xffffffffu ? 0 : (int)bi;
+        const int owner = e & 31, jb = e >> 5;
+        float v = 0.0f;
+#pragma unroll
+        for (int j = 0; j < J; ++j)
+            if (j == jb) {
+                v = lg[j];
+                if (lane == owner) key[j] = 0u;
+            }
+        v = __shfl_sync(0xffffffffu, v, owner);
+        if (lane == r) {
+            my_idx = e;
+            my_lg = v;
+        }
+    }
+    float mx = lane < k ? my_lg : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float ex = lane < k ? expf(my_lg - mx) : 0.0f;
+    float s = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    out_idx = my_idx;
+    out_w = lane < k ? scale * (ex / s) : 0.0f;
+    return bad;
+}
+
 // Exclusive prefix sum of data[0..len) in place; returns the total.  All NT
 // threads of the block must call it.
 template <int NT>

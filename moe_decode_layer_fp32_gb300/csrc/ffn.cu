@@ -29,7 +29,7 @@ namespace moe {
 namespace {
 
 constexpr int kStageBytes = 16384;   // one ring slot
-constexpr int kRingBytesPerSM = 12 * kStageBytes;  // weights in flight per SM
+constexpr int kRingBytesPerSM = 10 * kStageBytes;  // weights in flight per SM
 constexpr int kMT = kGroupTokens;    // tokens per group (register tile)
 constexpr int kSegMax = 256;         // rows per segment (gate/up/h buffers)
 
@@ -65,6 +65,7 @@ struct FfnSmem {
     int cls_units[3];
     int cls_groups[3];
     int cls_off[3];                   // offset of the class's records in `units`
+    int cls_cost[3];                  // cost units of the class (see cost_units)
     // per unit: {weight index, first token entry, tokens, inclusive group prefix}
     int4 units[1];
 };
@@ -107,60 +108,81 @@ __device__ __forceinline__ bool next_seg(const FfnArgs& a, const FfnSmem<NS>& sm
     return true;
 }
 
-// Work-balanced split of the row space.  A row of a group of mg tokens costs
-// kRowCost + mg: the weight stream is the same for every row, but the
-// per-token dot products, reductions and accumulations grow with mg (a CTA
-// whose rows all carry 4 tokens was measured 1.5x slower than one whose rows
-// carry 1).  Within a class the units' costs follow from the dispatch records
-// alone: unit q (t tokens, G = ceil(t / kMT) groups) costs
-// rows * (kRowCost * G + t), and the records carry the exclusive token prefix
-// (.y) and the inclusive group prefix (.w).
-constexpr int kRowCost = 5;
+// Work-balanced split of the row space.  A row costs what its token group's
+// code path costs: groups of one or two tokens run the narrow register tiles,
+// groups of three or four the wide one, which was measured about 1.5x slower
+// per row (the weight stream is the same; the per-token dot products,
+// reductions and accumulations are not).  A unit of t tokens costs
+// rows * cost_units(t); every class keeps the exclusive prefix of its units'
+// cost units (cpre) next to the unit records.
+#ifndef MOE_COST_NARROW
+#define MOE_COST_NARROW 2
+#endif
+#ifndef MOE_COST_WIDE
+#define MOE_COST_WIDE 3
+#endif
+constexpr int kCostNarrow = MOE_COST_NARROW;
+constexpr int kCostWide = MOE_COST_WIDE;
 
-__device__ __forceinline__ int class_tokens(const int4* u, int nu) {
-    return nu > 0 ? u[nu - 1].y + u[nu - 1].z - u[0].y : 0;
+__device__ __forceinline__ int group_cost(int mg) { return mg > 2 ? kCostWide : kCostNarrow; }
+__device__ __forceinline__ int cost_units(int t) {
+    return (t / kMT) * group_cost(kMT) + (t % kMT ? group_cost(t % kMT) : 0);
+}
+
+// One warp: exclusive prefix of the records' cost units into cpre; returns
+// the class total (on every lane).
+__device__ __forceinline__ int class_cost_prefix_warp(const int4* u, int nu, int* cpre) {
+    const int lane = threadIdx.x & 31;
+    int carry = 0;
+    for (int b = 0; b < nu; b += 32) {
+        const int q = b + lane;
+        const int c = q < nu ? cost_units(u[q].z) : 0;
+        int inc = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += t;
+        }
+        if (q < nu) cpre[q] = carry + inc - c;
+        carry += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    return carry;
 }
 
 template <int NS>
 __device__ __forceinline__ long long split_total_cost(const FfnArgs& a, const FfnSmem<NS>& sm) {
     long long tot = 0;
-    for (int c = 0; c < a.ncls; ++c) {
-        const int4* u = sm.units + sm.cls_off[c];
-        tot += (long long)a.cls[c].rows *
-               (kRowCost * sm.cls_groups[c] + class_tokens(u, sm.cls_units[c]));
-    }
+    for (int c = 0; c < a.ncls; ++c) tot += (long long)a.cls[c].rows * sm.cls_cost[c];
     return tot;
 }
 
 // Row-space position whose cost prefix is C (rounded down to a whole row).
 // 32-bit arithmetic throughout (the caller keeps the total cost below 2^31).
 template <int NS>
-__device__ __forceinline__ int split_row_at(const FfnArgs& a, const FfnSmem<NS>& sm, int C) {
+__device__ __forceinline__ int split_row_at(const FfnArgs& a, const FfnSmem<NS>& sm, const int* cpre_all,
+                                            int C) {
     int row_base = 0;
     for (int c = 0; c < a.ncls; ++c) {
         const int rows = a.cls[c].rows;
         const int nu = sm.cls_units[c];
         const int4* u = sm.units + sm.cls_off[c];
-        const int cc = rows * (kRowCost * sm.cls_groups[c] + class_tokens(u, nu));
+        const int* cpre = cpre_all + sm.cls_off[c];
+        const int cc = rows * sm.cls_cost[c];
         if (C < cc || c == a.ncls - 1) {
             if (nu == 0) return row_base;
             if (C >= cc) return row_base + rows * sm.cls_groups[c];
-            auto pre = [&](int q) {  // cost of the units before q
-                const int g = q > 0 ? u[q - 1].w : 0;
-                return rows * (kRowCost * g + (u[q].y - u[0].y));
-            };
-            int lo = 0, hi = nu - 1;    // last q with pre(q) <= C
+            int lo = 0, hi = nu - 1;    // last q with rows * cpre[q] <= C
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
-                if (pre(mid) <= C) lo = mid; else hi = mid - 1;
+                if (rows * cpre[mid] <= C) lo = mid; else hi = mid - 1;
             }
             const int t = u[lo].z;
             const int G = (t + kMT - 1) / kMT;
-            const int Cq = C - pre(lo);
-            const int full = rows * (kRowCost + kMT);
+            const int Cq = C - rows * cpre[lo];
+            const int full = rows * group_cost(kMT);   // every group but the last is full
             const int g = min(Cq / full, G - 1);
             const int mg = min(kMT, t - g * kMT);
-            const int i = min((Cq - g * full) / (kRowCost + mg), rows);
+            const int i = min((Cq - g * full) / group_cost(mg), rows);
             const int gpre = lo > 0 ? u[lo - 1].w : 0;
             return row_base + (gpre + g) * rows + i;
         }
@@ -202,6 +224,306 @@ __device__ __forceinline__ int group_tokens(const FfnArgs& a, const int4 rec, in
             wt[i] = w;
             orow[i] = a.out_mode == MOE_OUT_ACCUM ? t : row;
         }
+    }
+    return mg;
+}
+
+// ---- routing inside the CTA (whole-layer path) ------------------------------
+// Every CTA takes the top-k of every token from the router logits and builds
+// its own unit records and per-unit token lists in shared memory, so that no
+// single block serialises the dispatch and nothing is read back from global
+// memory.  Order and content match the dispatch kernel's: ascending unit id,
+// then ascending token id; a department's token set X^j is the union of its
+// experts' sets, with weight omega = sum of the token's routing weights on
+// that department's experts, in slot order.  Units sit one per thread (the
+// experts, then the departments from the next warp boundary on), so the host
+// takes this path only when roundup32(n) + m fits the block.
+struct LocalRoute {
+    uint32_t* emask;   // [n][W]: bit t of row e = token t chose expert e
+    uint32_t* dmask;   // [m][W]: union over the department's experts
+    int16_t* idx;      // [T*k] selected experts
+    int16_t* didx;     // [T*k] their departments
+    float* w;          // [T*k] routing weights
+    int* off;          // [n + m] first list entry of each expert, then each department
+    int16_t* etok;     // [T*k] expert lists (ascending expert, then token): token
+    float* ew;         //       and routing weight
+    int16_t* dtok;     // [T*min(k, m)] department lists: token
+    float* dw;         //       and department weight omega
+    int4* wtot;        // per warp: totals of the unit scan
+    int* tcg;          // [2] tensor-core group totals (experts, departments)
+    int W, m;
+};
+
+__host__ __device__ __forceinline__ size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
+
+// Bytes of the local routing state for a block of nwarps warps.
+__host__ __device__ __forceinline__ size_t local_route_bytes(int T, int n, int k, int g, int nwarps) {
+    const size_t W = (size_t)(T + 31) / 32;
+    const size_t m = g > 1 ? (size_t)(n / g) : 0;
+    const size_t TK = (size_t)T * k;
+    const size_t DK = m ? (size_t)T * ((size_t)k < m ? (size_t)k : m) : 0;
+    return align16(4 * n * W) + align16(4 * m * W) + align16(2 * TK) * 2 + align16(4 * TK) +
+           align16(4 * (n + m)) + align16(2 * TK) + align16(4 * TK) + align16(2 * DK) + align16(4 * DK) +
+           align16(16 * (size_t)nwarps) + 16;
+}
+
+__device__ __forceinline__ LocalRoute local_route_at(unsigned char* p, int T, int n, int k, int g,
+                                                     int nwarps) {
+    LocalRoute lr;
+    lr.W = (T + 31) >> 5;
+    lr.m = g > 1 ? n / g : 0;
+    const size_t TK = (size_t)T * k;
+    const size_t DK = lr.m ? (size_t)T * (k < lr.m ? k : lr.m) : 0;
+    auto take = [&](size_t bytes) {
+        unsigned char* q = p;
+        p += align16(bytes);
+        return q;
+    };
+    lr.emask = reinterpret_cast<uint32_t*>(take(4 * (size_t)n * lr.W));
+    lr.dmask = reinterpret_cast<uint32_t*>(take(4 * (size_t)lr.m * lr.W));
+    lr.idx = reinterpret_cast<int16_t*>(take(2 * TK));
+    lr.didx = reinterpret_cast<int16_t*>(take(2 * TK));
+    lr.w = reinterpret_cast<float*>(take(4 * TK));
+    lr.off = reinterpret_cast<int*>(take(4 * (size_t)(n + lr.m)));
+    lr.etok = reinterpret_cast<int16_t*>(take(2 * TK));
+    lr.ew = reinterpret_cast<float*>(take(4 * TK));
+    lr.dtok = reinterpret_cast<int16_t*>(take(2 * DK));
+    lr.dw = reinterpret_cast<float*>(take(4 * DK));
+    lr.wtot = reinterpret_cast<int4*>(take(16 * (size_t)nwarps));
+    lr.tcg = reinterpret_cast<int*>(take(16));
+    return lr;
+}
+
+// Rank of token t among the tokens of a mask row (ascending).
+__device__ __forceinline__ int row_rank(const uint32_t* row, int t) {
+    int r = __popc(row[t >> 5] & ((1u << (t & 31)) - 1u));
+    for (int w = 0; w < (t >> 5); ++w) r += __popc(row[w]);
+    return r;
+}
+
+// Top-k of every token, one warp per token: selections into shared memory,
+// the expert bitmasks (zeroed by the caller) and department ids; CTA 0 also
+// stores them as the routing outputs.  Ends with a barrier.
+template <int J, int NT>
+__device__ void local_topk_rows(const FfnArgs& a, const LocalRoute& lr, bool writer) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int t = warp; t < a.T; t += NT / 32) {
+        int e;
+        float w;
+        const bool bad =
+            topk_select_warp<J>(a.ws.logits + (size_t)t * a.n, a.bias, a.n, a.k, a.scale, e, w);
+        if (lane < a.k) {
+            lr.idx[t * a.k + lane] = (int16_t)e;
+            lr.didx[t * a.k + lane] = (int16_t)(a.g > 1 ? e / a.g : e);
+            lr.w[t * a.k + lane] = w;
+            atomicOr(&lr.emask[e * lr.W + (t >> 5)], 1u << (t & 31));
+            if (writer) {
+                a.topk_idx[(size_t)t * a.k + lane] = e;
+                a.topk_w[(size_t)t * a.k + lane] = w;
+            }
+        }
+        if (bad && writer && lane == 0) set_status(a.ws.status, kDevErrRouting);
+    }
+    __syncthreads();
+}
+
+template <int NT>
+__device__ __forceinline__ void local_topk(const FfnArgs& a, const LocalRoute& lr, bool writer) {
+    const int J = (a.n + 31) / 32;
+    if (J <= 1) local_topk_rows<1, NT>(a, lr, writer);
+    else if (J <= 2) local_topk_rows<2, NT>(a, lr, writer);
+    else if (J <= 4) local_topk_rows<4, NT>(a, lr, writer);
+    else local_topk_rows<8, NT>(a, lr, writer);
+}
+
+// Inclusive warp scan of four counters.
+__device__ __forceinline__ int4 warp_inclusive_scan4(int4 v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int tx = __shfl_up_sync(0xffffffffu, v.x, o);
+        const int ty = __shfl_up_sync(0xffffffffu, v.y, o);
+        const int tz = __shfl_up_sync(0xffffffffu, v.z, o);
+        const int tw = __shfl_up_sync(0xffffffffu, v.w, o);
+        if (lane >= o) {
+            v.x += tx;
+            v.y += ty;
+            v.z += tz;
+            v.w += tw;
+        }
+    }
+    return v;
+}
+
+// After the top-k (every thread of the CTA; ends with a barrier): unit
+// counts, records and cost prefixes of every class, then the per-unit token
+// lists.  Expert u sits on thread u, department j on thread roundup32(n) + j,
+// so each kind's prefix sums are warp scans plus the totals of its earlier
+// warps.  CTA 0 (`writer`) also stores the dispatch in the workspace in the
+// layout moe_dispatch writes.
+template <int NS, int NT>
+__device__ void local_tables(const FfnArgs& a, FfnSmem<NS>& sm, int* cpre, const LocalRoute& lr,
+                             bool writer) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n = a.n, m = lr.m, W = lr.W;
+    const int n_pad = (n + 31) & ~31;
+    const bool isx = tid < n;
+    const bool isd = m > 0 && tid >= n_pad && tid < n_pad + m;
+    const int u = isx ? tid : tid - n_pad;
+    int cnt = 0;
+    if (isx) {
+        for (int w = 0; w < W; ++w) cnt += __popc(lr.emask[u * W + w]);
+    } else if (isd) {
+        for (int w = 0; w < W; ++w) {
+            uint32_t v = 0u;
+            for (int e = u * a.g; e < (u + 1) * a.g; ++e) v |= lr.emask[e * W + w];
+            lr.dmask[u * W + w] = v;
+            cnt += __popc(v);
+        }
+    }
+    // tokens, active units, groups, cost units
+    const int4 mine = make_int4(cnt, cnt > 0 ? 1 : 0, (cnt + kMT - 1) / kMT, cost_units(cnt));
+    const int4 inc = warp_inclusive_scan4(mine);
+    if (lane == 31) lr.wtot[warp] = inc;
+    if (tid < 2) lr.tcg[tid] = 0;
+    __syncthreads();
+    int4 pre = make_int4(inc.x - mine.x, inc.y - mine.y, inc.z - mine.z, inc.w - mine.w);
+    for (int w2 = isd ? n_pad / 32 : 0; w2 < warp; ++w2) {
+        const int4 t = lr.wtot[w2];
+        pre.x += t.x;
+        pre.y += t.y;
+        pre.z += t.z;
+        pre.w += t.w;
+    }
+    if (isx || isd) {
+        lr.off[isx ? u : n + u] = pre.x;
+        if (cnt > 0) {
+            const int4 r = make_int4(u, pre.x, cnt, pre.z + mine.z);
+            for (int c = 0; c < a.ncls; ++c) {
+                const int kind = a.cls[c].kind;
+                if ((isx && kind == kUnitExpert) || (isd && kind == kUnitDept)) {
+                    sm.units[sm.cls_off[c] + pre.y] = r;
+                    cpre[sm.cls_off[c] + pre.y] = pre.w;
+                }
+            }
+            if (writer) {
+                (isd ? a.ws.act_dept : a.ws.act_exp)[pre.y] = u;
+                (isd ? a.ws.dept_units : a.ws.exp_units)[pre.y] = r;
+                atomicAdd(&lr.tcg[isd ? 1 : 0], (cnt + kTcGroupTokens - 1) / kTcGroupTokens);
+            }
+        }
+        if (writer) {
+            (isd ? a.ws.dept_count : a.ws.exp_count)[u] = cnt;
+            (isd ? a.ws.dept_off : a.ws.exp_off)[u] = pre.x;
+        }
+        // the last unit of each kind holds the kind's totals
+        if (u == (isd ? m : n) - 1) {
+            const int4 tot = make_int4(pre.x + mine.x, pre.y + mine.y, pre.z + mine.z, pre.w + mine.w);
+            for (int c = 0; c < a.ncls; ++c) {
+                const int kind = a.cls[c].kind;
+                if ((isx && kind == kUnitExpert) || (isd && kind == kUnitDept)) {
+                    sm.cls_units[c] = tot.y;
+                    sm.cls_groups[c] = tot.z;
+                    sm.cls_cost[c] = tot.w;
+                }
+            }
+            if (writer) {
+                (isd ? a.ws.dept_off : a.ws.exp_off)[isd ? m : n] = tot.x;
+                a.ws.counts[isd ? 1 : 0] = tot.y;
+            }
+        }
+    }
+    if (tid == 0) {
+        for (int c = 0; c < a.ncls; ++c)
+            if (a.cls[c].kind == kUnitShared) {
+                const int G = (a.T + kMT - 1) / kMT;
+                sm.units[sm.cls_off[c]] = make_int4(0, 0, a.T, G);
+                cpre[sm.cls_off[c]] = 0;
+                sm.cls_units[c] = 1;
+                sm.cls_groups[c] = G;
+                sm.cls_cost[c] = cost_units(a.T);
+            }
+        if (writer && m == 0) {
+            a.ws.counts[1] = 0;
+            a.ws.counts[3] = 0;
+        }
+    }
+    __syncthreads();
+    if (writer && tid == 0) {
+        a.ws.counts[2] = lr.tcg[0];
+        if (m > 0) a.ws.counts[3] = lr.tcg[1];
+    }
+    // token lists: expert lists from every assignment, department lists from
+    // the first slot of each token on each department
+    const int TK = a.T * a.k;
+    for (int i = tid; i < TK; i += NT) {
+        const int t = i / a.k, sl = i - t * a.k;
+        const int e = lr.idx[i];
+        const float wv = lr.w[i];
+        const int pos = lr.off[e] + row_rank(lr.emask + e * W, t);
+        lr.etok[pos] = (int16_t)t;
+        lr.ew[pos] = wv;
+        if (writer) {
+            a.ws.asg_tok[pos] = t;
+            a.ws.asg_slot[pos] = sl;
+            a.ws.asg_w[pos] = wv;
+            a.ws.tok_asg[i] = pos;
+        }
+        if (m > 0) {
+            const int j = lr.didx[i];
+            bool first = true;
+            float om = 0.0f;   // omega: the token's weights on department j, slot order
+            for (int q = 0; q < a.k; ++q)
+                if (lr.didx[t * a.k + q] == j) {
+                    if (q < sl) first = false;
+                    om += lr.w[t * a.k + q];
+                }
+            if (first) {
+                const int pd = lr.off[n + j] + row_rank(lr.dmask + j * W, t);
+                lr.dtok[pd] = (int16_t)t;
+                lr.dw[pd] = om;
+                if (writer) {
+                    a.ws.dept_tok[pd] = t;
+                    a.ws.dept_w[pd] = om;
+                    a.ws.tok_dpos[t * m + j] = pd;
+                }
+            }
+        }
+    }
+    if (writer && m > 0)
+        for (int i = tid; i < a.T * m; i += NT) {
+            const int t = i / m, j = i - t * m;
+            if (!((lr.dmask[j * W + (t >> 5)] >> (t & 31)) & 1u)) a.ws.tok_dpos[i] = -1;
+        }
+    __syncthreads();
+}
+
+// Tokens of group `grp` of a unit from the shared-memory lists, with their
+// weights (ACCUM mode: the output row is the token).
+__device__ __forceinline__ int group_tokens_local(const LocalRoute& lr, const int4 rec, int kind, int grp,
+                                                  int (&tok)[kMT], float (&wt)[kMT], int (&orow)[kMT]) {
+    const int first = grp * kMT;
+    const int mg = min(kMT, rec.z - first);
+    const int p0 = rec.y + first;
+#pragma unroll
+    for (int i = 0; i < kMT; ++i) {
+        int t = 0;
+        float w = 0.0f;
+        if (i < mg) {
+            if (kind == kUnitShared) {
+                t = first + i;
+                w = 1.0f;
+            } else if (kind == kUnitDept) {
+                t = lr.dtok[p0 + i];
+                w = lr.dw[p0 + i];
+            } else {
+                t = lr.etok[p0 + i];
+                w = lr.ew[p0 + i];
+            }
+        }
+        tok[i] = t;
+        wt[i] = w;
+        orow[i] = t;
     }
     return mg;
 }
@@ -316,14 +638,37 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
         mbar_init_fence();
     }
     for (int i = tid; i < 2 * kSegMax * kMT; i += kNT) (&sm.gu[0][0])[i] = 0.0f;
+    // after the unit records: their cost prefixes, then the local routing state
+    int cap = 0;
+    for (int c = 0; c < a.ncls; ++c) cap += class_capacity(a.cls[c], a.n, a.g);
+    int* cpre = reinterpret_cast<int*>(sm.units + cap);
+    LocalRoute lr = {};
+    if (a.local_route) {
+        lr = local_route_at(reinterpret_cast<unsigned char*>(sm.units + cap) + align16(4 * (size_t)cap), a.T,
+                            a.n, a.k, a.g, NCW + 1);
+        for (int i = tid; i < a.n * lr.W; i += kNT) lr.emask[i] = 0u;
+        if (tid == 0) {
+            int off = 0;
+            for (int c = 0; c < a.ncls; ++c) {
+                sm.cls_off[c] = off;
+                off += class_capacity(a.cls[c], a.n, a.g);
+            }
+        }
+        __syncthreads();
+    }
 
     // Everything below reads what the routing / dispatch kernel wrote.
     pdl_wait_primary();
 
-    // ---- unit table: the dispatch's per-unit records (one coalesced load), or,
-    // when units with more than max_tokens tokens go to the tensor-core kernel,
-    // the records of the remaining units with their own group prefix ----
-    if (a.max_tokens >= a.T) {
+    // ---- unit table: built here from the router logits (whole-layer path),
+    // the dispatch's per-unit records (one coalesced load), or, when units
+    // with more than max_tokens tokens go to the tensor-core kernel, the
+    // records of the remaining units with their own group prefix ----
+    if (a.local_route) {
+        const bool writer = blockIdx.x == 0;
+        local_topk<kNT>(a, lr, writer);
+        local_tables<NS, kNT>(a, sm, cpre, lr, writer);
+    } else if (a.max_tokens >= a.T) {
         int off = 0;
         for (int c = 0; c < a.ncls; ++c) {
             const UnitClass& uc = a.cls[c];
@@ -342,9 +687,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
             off += cap;
         }
         __syncthreads();
-        if (tid < a.ncls) {
-            const int nu = sm.cls_units[tid];
-            sm.cls_groups[tid] = nu > 0 ? sm.units[sm.cls_off[tid] + nu - 1].w : 0;
+        if (warp < a.ncls) {
+            const int nu = sm.cls_units[warp];
+            const int tot = class_cost_prefix_warp(sm.units + sm.cls_off[warp], nu, cpre + sm.cls_off[warp]);
+            if (lane == 0) {
+                sm.cls_groups[warp] = nu > 0 ? sm.units[sm.cls_off[warp] + nu - 1].w : 0;
+                sm.cls_cost[warp] = tot;
+            }
         }
         __syncthreads();
     } else {
@@ -363,10 +712,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
                     const int A = uc.kind == kUnitDept ? a.ws.counts[1] : a.ws.counts[0];
                     kept = filter_units_warp(src, A, 1, a.max_tokens, kMT, sm.units + off, &groups);
                 }
+                __syncwarp();
+                const int tot = class_cost_prefix_warp(sm.units + off, kept, cpre + off);
                 if (lane == 0) {
                     sm.cls_units[c] = kept;
                     sm.cls_groups[c] = groups;
                     sm.cls_off[c] = off;
+                    sm.cls_cost[c] = tot;
                 }
                 off += class_capacity(uc, a.n, a.g);
             }
@@ -385,31 +737,23 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
     } else if (blockIdx.x == 0 && tid == 0) {
         a.ws.sync[1] = 0u;
     }
-    // CTA's share: equal work (rows weighted by their tokens) when the unit
-    // table is the dispatch's own (token prefixes valid), equal rows otherwise
+    // CTA's share: equal work (cost units, see cost_units), or equal rows
+    // when the cost total would not fit the 32-bit split search
     long long r_begin = grid_share(R, blockIdx.x, gridDim.x, a.grid_magic);
     long long r_end = grid_share(R, blockIdx.x + 1, gridDim.x, a.grid_magic);
-    if (R > 0 && a.max_tokens >= a.T) {
-        // every group holding one token (e.g. T = 1) makes the cost uniform per row
-        long long groups = 0, tokens = 0;
-        for (int c = 0; c < a.ncls; ++c) {
-            groups += sm.cls_groups[c];
-            tokens += class_tokens(sm.units + sm.cls_off[c], sm.cls_units[c]);
-        }
-        if (tokens != groups) {
-            __shared__ long long s_split[2];
-            const long long tot = split_total_cost(a, sm);
-            if (tot < (1ll << 31)) {
-                if (tid == 0 || tid == 32) {
-                    const unsigned b = blockIdx.x + (tid ? 1u : 0u);
-                    s_split[tid ? 1 : 0] =
-                        b == gridDim.x ? R
-                                       : split_row_at(a, sm, (int)grid_share(tot, b, gridDim.x, a.grid_magic));
-                }
-                __syncthreads();
-                r_begin = s_split[0];
-                r_end = s_split[1];
+    if (R > 0) {
+        __shared__ long long s_split[2];
+        const long long tot = split_total_cost(a, sm);
+        if (tot > 0 && tot < (1ll << 31)) {
+            if (tid == 0 || tid == 32) {
+                const unsigned b = blockIdx.x + (tid ? 1u : 0u);
+                s_split[tid ? 1 : 0] =
+                    b == gridDim.x ? R
+                                   : split_row_at(a, sm, cpre, (int)grid_share(tot, b, gridDim.x, a.grid_magic));
             }
+            __syncthreads();
+            r_begin = s_split[0];
+            r_end = s_split[1];
         }
     }
 
@@ -488,8 +832,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
     while (next_seg(a, sm, r, r_end, s)) {
         int tok[kMT], orow[kMT];
         float wt[kMT];
-        const int mg = group_tokens(a, sm.units[sm.cls_off[s.cls] + s.q], a.cls[s.cls].kind, s.grp,
-                                    tok, wt, orow);
+        const int4 rec = sm.units[sm.cls_off[s.cls] + s.q];
+        const int mg = a.local_route ? group_tokens_local(lr, rec, a.cls[s.cls].kind, s.grp, tok, wt, orow)
+                                     : group_tokens(a, rec, a.cls[s.cls].kind, s.grp, tok, wt, orow);
 
         // ---- phase A: gate / up dot products ----
         {
@@ -595,14 +940,46 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
     }
 }
 
+// Launch shape of one instantiation: weight type, consumer warps, 8-column
+// chunks per thread, rows per stage, CTAs per SM.
 template <typename WT, int NCW, int CH, int RMAX, int CPS>
-cudaError_t launch_ffn_t(const FfnArgs& a, cudaStream_t s) {
-    auto kern = ffn_stream_kernel<WT, NCW, CH, RMAX, CPS>;
+struct FfnCfg {};
+
+// Dynamic shared memory of a launch: ring, fixed carve-up, one unit record
+// per possible unit of every class, and the routing state of the local path.
+template <typename WT, int NCW, int CH, int RMAX, int CPS>
+constexpr int cps_of(FfnCfg<WT, NCW, CH, RMAX, CPS>) { return CPS; }
+template <typename WT, int NCW, int CH, int RMAX, int CPS>
+constexpr int threads_of(FfnCfg<WT, NCW, CH, RMAX, CPS>) { return (NCW + 1) * 32; }
+
+template <typename WT, int NCW, int CH, int RMAX, int CPS>
+size_t ffn_smem(const FfnArgs& a, FfnCfg<WT, NCW, CH, RMAX, CPS>) {
     constexpr int NS = kRingBytesPerSM / kStageBytes / CPS;
-    // unit table: one record per possible unit of every class
     int units = 0;
     for (int c = 0; c < a.ncls; ++c) units += class_capacity(a.cls[c], a.n, a.g);
-    const size_t smem = (size_t)NS * kStageBytes + sizeof(FfnSmem<NS>) + (size_t)units * sizeof(int4);
+    return (size_t)NS * kStageBytes + sizeof(FfnSmem<NS>) + (size_t)units * sizeof(int4) +
+           align16(4 * (size_t)units) + (a.local_route ? local_route_bytes(a.T, a.n, a.k, a.g, NCW + 1) : 0);
+}
+
+// Largest dynamic shared memory per CTA that still lets `cps` CTAs share an SM.
+size_t smem_per_cta_limit(int cps) {
+    static int cache[64][3] = {};   // per device: per-SM, reserved per block, opt-in maximum
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int* c = cache[dev];
+    if (c[0] == 0) {
+        cudaDeviceGetAttribute(&c[1], cudaDevAttrReservedSharedMemoryPerBlock, dev);
+        cudaDeviceGetAttribute(&c[2], cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        cudaDeviceGetAttribute(&c[0], cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    }
+    const long long lim = (long long)c[0] / cps - c[1];
+    return (size_t)(lim < c[2] ? (lim > 0 ? lim : 0) : c[2]);
+}
+
+template <typename WT, int NCW, int CH, int RMAX, int CPS>
+cudaError_t launch_ffn_t(const FfnArgs& a, cudaStream_t s, FfnCfg<WT, NCW, CH, RMAX, CPS> cfg_tag) {
+    auto kern = ffn_stream_kernel<WT, NCW, CH, RMAX, CPS>;
+    const size_t smem = ffn_smem(a, cfg_tag);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)(device_sm_count() * CPS);
@@ -679,15 +1056,33 @@ __global__ void zero_kernel(uint4* p, size_t n16) {
 #define MOE_CC_CPS 2
 #endif
 
-cudaError_t launch_ffn(const FfnArgs& a, cudaStream_t s) {
-    // Consumer warps x chunks per thread x 8 must cover d; RMAX is the most
-    // rows one 16 KB stage holds at that width.
+// Calls f with the launch shape for this dtype and hidden size: consumer
+// warps x chunks per thread x 8 must cover d; RMAX is the most rows one 16 KB
+// stage holds at that width.
+template <class F>
+auto with_ffn_cfg(const FfnArgs& a, F f) {
     if (a.dtype == MOE_DTYPE_BF16) {
-        if (a.d <= 2048) return launch_ffn_t<__nv_bfloat16, MOE_CC_NCW, MOE_CC_CH, MOE_CC_RMAX, MOE_CC_CPS>(a, s);
-        return launch_ffn_t<__nv_bfloat16, 15, 2, 1, 1>(a, s);
+        if (a.d <= 2048) return f(FfnCfg<__nv_bfloat16, MOE_CC_NCW, MOE_CC_CH, MOE_CC_RMAX, MOE_CC_CPS>{});
+        return f(FfnCfg<__nv_bfloat16, 15, 2, 1, 1>{});
     }
-    if (a.d <= 1024) return launch_ffn_t<float, 4, 1, 8, 1>(a, s);
-    return launch_ffn_t<float, 15, 2, 1, 1>(a, s);
+    if (a.d <= 1024) return f(FfnCfg<float, 4, 1, 8, 1>{});
+    return f(FfnCfg<float, 15, 2, 1, 1>{});
+}
+
+cudaError_t launch_ffn(const FfnArgs& a, cudaStream_t s) {
+    return with_ffn_cfg(a, [&](auto cfg) { return launch_ffn_t(a, s, cfg); });
+}
+
+bool ffn_local_route_fits(const FfnArgs& a) {
+    FfnArgs b = a;
+    b.local_route = 1;
+    const int m = a.g > 1 ? a.n / a.g : 0;
+    return with_ffn_cfg(b, [&](auto cfg) {
+        // one thread per unit: the experts, then the departments from the next warp on
+        // (and the top-k's lane-held candidates: n <= 256)
+        return a.n <= 256 && ((a.n + 31) / 32) * 32 + m <= threads_of(cfg) &&
+               ffn_smem(b, cfg) <= smem_per_cta_limit(cps_of(cfg));
+    });
 }
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {

@@ -28,6 +28,9 @@ struct RouteArgs {
     float* y_zero;           // zeroed by the route grid when non-null
     long long y_elems;
     int split_x;             // also write the bf16 hi/lo activations (ws.xb)
+    // Whole-layer path with routing in the FFN kernel: write the logits only
+    // (no top-k, no dispatch); the FFN CTAs take it from there.
+    int logits_only;
 };
 
 struct DispatchArgs {
@@ -64,6 +67,15 @@ struct FfnArgs {
     int auto_tc;          // both kernels launched; they pick one by prefer_tc()
     int sms;              // SMs of the device (grid of the tensor-core kernel)
     unsigned long long grid_magic;   // set by the launcher: ceil(2^64 / grid)
+    // Routing inside the CUDA-core kernel (whole-layer path, ACCUM mode, no
+    // tensor-core kernel): every CTA takes the top-k of ws.logits and builds
+    // its own unit records in shared memory; CTA 0 also stores the routing
+    // and the dispatch lists in the workspace.
+    int local_route;
+    const float* bias;    // selection bias or null
+    float scale;
+    int32_t* topk_idx;    // [T, k] routing outputs (written by CTA 0)
+    float* topk_w;
 };
 
 // ceil(2^64 / g) for g >= 2 (2^64 / g when g divides it); grid_share() divides
@@ -145,6 +157,9 @@ struct CombineArgs {
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s);
 cudaError_t launch_ffn(const FfnArgs& a, cudaStream_t s);
+// Whether the CUDA-core kernel's shared memory still holds the routing state
+// of the local path (a.local_route) at its usual CTAs per SM.
+bool ffn_local_route_fits(const FfnArgs& a);
 cudaError_t launch_ffn_tc(const TcArgs& a, cudaStream_t s);
 size_t ffn_tc_smem_bytes(int units);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);

@@ -166,86 +166,21 @@ __device__ void dispatch_block(const int32_t* idx, const float* wts, int T, int 
     }
 }
 
-// Top-k of one token's keys (logit + bias) by one warp; lane holds experts
-// lane + 32*j.  Descending key, equal keys -> lower expert index first.  The
-// weights are scale * softmax over the selected unbiased logits.
-//
-// Keys are mapped to unsigned integers that order like the floats (-0 folded
-// into +0 so that it ties with +0, as a float comparison does).  Each round
-// takes the warp maximum of the lanes' best remaining keys and then the
-// smallest expert index holding it, both with single-instruction warp
-// reductions.  0 marks a taken (or absent) entry; NaN and -inf keys map below
-// every finite key, and picking one flags the routing as bad.
-__device__ __forceinline__ uint32_t ordered_key(float v) {
-    if (v == 0.0f) v = 0.0f;
-    const uint32_t b = __float_as_uint(v);
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
+// Top-k of one token by one warp, written to the routing outputs (and to
+// the shared-memory copy the fused dispatch reads, when given).
 template <int J>
 __device__ void topk_warp(const float* logits_row, const float* bias, int n, int k, float scale,
                           int32_t* idx_out, float* w_out, int32_t* status, int32_t* idx_sm,
                           float* w_sm) {
     const int lane = threadIdx.x & 31;
-    constexpr uint32_t kLowest = 0x007fffffu;   // ordered_key(-inf)
-    uint32_t key[J];
-    float lg[J];
-#pragma unroll
-    for (int j = 0; j < J; ++j) {
-        const int e = lane + 32 * j;
-        lg[j] = 0.0f;
-        key[j] = 0u;
-        if (e < n) {
-            const float l = __ldcg(logits_row + e);
-            const float kv = bias ? l + __ldg(bias + e) : l;
-            lg[j] = l;
-            // finite keys rank above kLowest; -inf and NaN take kLowest (still
-            // selectable, after every finite key, lowest index first)
-            key[j] = (kv == kv && kv != -INFINITY) ? ordered_key(kv) : kLowest;
-        }
-    }
-    int my_idx = 0;
-    float my_lg = 0.0f;
-    bool bad = false;
-    for (int r = 0; r < k; ++r) {
-        uint32_t bk = 0u;
-        int bj = 0;
-#pragma unroll
-        for (int j = 0; j < J; ++j)
-            if (key[j] > bk) {
-                bk = key[j];
-                bj = j;
-            }
-        const uint32_t top = __reduce_max_sync(0xffffffffu, bk);
-        const uint32_t cand = (bk == top && top != 0u) ? (uint32_t)(lane + 32 * bj) : 0xffffffffu;
-        const uint32_t bi = __reduce_min_sync(0xffffffffu, cand);
-        if (top <= kLowest) bad = true;   // a non-finite key (or none) was selected
-        const int e = bi == 0xffffffffu ? 0 : (int)bi;
-        const int owner = e & 31, jb = e >> 5;
-        float v = 0.0f;
-#pragma unroll
-        for (int j = 0; j < J; ++j)
-            if (j == jb) {
-                v = lg[j];
-                if (lane == owner) key[j] = 0u;
-            }
-        v = __shfl_sync(0xffffffffu, v, owner);
-        if (lane == r) {
-            my_idx = e;
-            my_lg = v;
-        }
-    }
-    float mx = lane < k ? my_lg : -INFINITY;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    const float ex = lane < k ? expf(my_lg - mx) : 0.0f;
-    const float s = warp_sum(ex);
+    int e;
+    float wv;
+    const bool bad = topk_select_warp<J>(logits_row, bias, n, k, scale, e, wv);
     if (lane < k) {
-        const float wv = scale * (ex / s);
-        idx_out[lane] = my_idx;
+        idx_out[lane] = e;
         w_out[lane] = wv;
         if (idx_sm) {
-            idx_sm[lane] = my_idx;
+            idx_sm[lane] = e;
             w_sm[lane] = wv;
         }
     }
@@ -333,6 +268,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
         }
         __syncthreads();
     }
+    if (a.logits_only) return;
     // Count this block in.  The counter add is a GPU-scope release/acquire:
     // it publishes the block's logits (ordered before it by the CTA barrier
     // above) and lets the last block to arrive see every block's logits
