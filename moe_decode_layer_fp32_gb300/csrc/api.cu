@@ -221,11 +221,12 @@ bool prepare_tc(const moe::FfnArgs& a, int T, moe::TcArgs* t) {
     const int thr = tc_min_tokens();
     // Automatic mode launches the tensor-core kernel (which then decides on
     // the device) for wide rows always, and otherwise only when some class
-    // expects more than kGroupTokens tokens per unit: below that the CUDA-core
-    // stream reads each weight once, which the tensor cores do not beat at
-    // d <= kTcWideHidden, and an idle launch costs a few µs.
+    // expects at least two CUDA-core token groups per unit.  Below that the
+    // CUDA-core stream, with the routing inside its CTAs, measured faster
+    // (DeaMoE-7B layer at T = 8: 50 vs 55 µs), and an idle tensor-core launch
+    // also forces the routing kernel to build the dispatch itself.
     if (thr == 0 && a.d <= moe::kTcWideHidden &&
-        (T <= moe::kGroupTokens || expected_unit_tokens(a, T) <= moe::kGroupTokens))
+        (T <= moe::kGroupTokens || expected_unit_tokens(a, T) < 2 * moe::kGroupTokens))
         return false;
     const int mt = thr > 0 ? thr : 1;
     int units = 0;

@@ -112,31 +112,42 @@ __device__ __forceinline__ bool next_seg(const FfnArgs& a, const FfnSmem<NS>& sm
 // code path costs: groups of one or two tokens run the narrow register tiles,
 // groups of three or four the wide one, which was measured about 1.5x slower
 // per row (the weight stream is the same; the per-token dot products,
-// reductions and accumulations are not).  A unit of t tokens costs
-// rows * cost_units(t); every class keeps the exclusive prefix of its units'
-// cost units (cpre) next to the unit records.
+// reductions and accumulations are not).  Each token group also costs
+// kSegCost once, at its first row: a CTA whose range starts a new group pays
+// a segment switch (activation loads, the SwiGLU barrier, a drained ring).
+// A unit of t tokens costs rows * cost_units(t) + groups * kSegCost; every
+// class keeps the exclusive prefix of its units' costs (cpre) next to the
+// unit records.
 #ifndef MOE_COST_NARROW
 #define MOE_COST_NARROW 2
 #endif
 #ifndef MOE_COST_WIDE
 #define MOE_COST_WIDE 3
 #endif
+#ifndef MOE_COST_SEG
+#define MOE_COST_SEG 24
+#endif
 constexpr int kCostNarrow = MOE_COST_NARROW;
 constexpr int kCostWide = MOE_COST_WIDE;
+constexpr int kSegCost = MOE_COST_SEG;
 
 __device__ __forceinline__ int group_cost(int mg) { return mg > 2 ? kCostWide : kCostNarrow; }
 __device__ __forceinline__ int cost_units(int t) {
     return (t / kMT) * group_cost(kMT) + (t % kMT ? group_cost(t % kMT) : 0);
 }
+// Cost of a unit of t tokens whose rows are `rows` long.
+__device__ __forceinline__ int unit_cost(int t, int rows) {
+    return rows * cost_units(t) + ((t + kMT - 1) / kMT) * kSegCost;
+}
 
-// One warp: exclusive prefix of the records' cost units into cpre; returns
+// One warp: exclusive prefix of the records' unit costs into cpre; returns
 // the class total (on every lane).
-__device__ __forceinline__ int class_cost_prefix_warp(const int4* u, int nu, int* cpre) {
+__device__ __forceinline__ int class_cost_prefix_warp(const int4* u, int nu, int rows, int* cpre) {
     const int lane = threadIdx.x & 31;
     int carry = 0;
     for (int b = 0; b < nu; b += 32) {
         const int q = b + lane;
-        const int c = q < nu ? cost_units(u[q].z) : 0;
+        const int c = q < nu ? unit_cost(u[q].z, rows) : 0;
         int inc = c;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -152,7 +163,7 @@ __device__ __forceinline__ int class_cost_prefix_warp(const int4* u, int nu, int
 template <int NS>
 __device__ __forceinline__ long long split_total_cost(const FfnArgs& a, const FfnSmem<NS>& sm) {
     long long tot = 0;
-    for (int c = 0; c < a.ncls; ++c) tot += (long long)a.cls[c].rows * sm.cls_cost[c];
+    for (int c = 0; c < a.ncls; ++c) tot += sm.cls_cost[c];
     return tot;
 }
 
@@ -167,22 +178,22 @@ __device__ __forceinline__ int split_row_at(const FfnArgs& a, const FfnSmem<NS>&
         const int nu = sm.cls_units[c];
         const int4* u = sm.units + sm.cls_off[c];
         const int* cpre = cpre_all + sm.cls_off[c];
-        const int cc = rows * sm.cls_cost[c];
+        const int cc = sm.cls_cost[c];
         if (C < cc || c == a.ncls - 1) {
             if (nu == 0) return row_base;
             if (C >= cc) return row_base + rows * sm.cls_groups[c];
-            int lo = 0, hi = nu - 1;    // last q with rows * cpre[q] <= C
+            int lo = 0, hi = nu - 1;    // last q with cpre[q] <= C
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
-                if (rows * cpre[mid] <= C) lo = mid; else hi = mid - 1;
+                if (cpre[mid] <= C) lo = mid; else hi = mid - 1;
             }
             const int t = u[lo].z;
             const int G = (t + kMT - 1) / kMT;
-            const int Cq = C - rows * cpre[lo];
-            const int full = rows * group_cost(kMT);   // every group but the last is full
+            const int Cq = C - cpre[lo];
+            const int full = rows * group_cost(kMT) + kSegCost;   // every group but the last is full
             const int g = min(Cq / full, G - 1);
             const int mg = min(kMT, t - g * kMT);
-            const int i = min((Cq - g * full) / group_cost(mg), rows);
+            const int i = min(max(Cq - g * full - kSegCost, 0) / group_cost(mg), rows);
             const int gpre = lo > 0 ? u[lo - 1].w : 0;
             return row_base + (gpre + g) * rows + i;
         }
@@ -403,7 +414,7 @@ __device__ void local_tables(const FfnArgs& a, FfnSmem<NS>& sm, int* cpre, const
                 const int kind = a.cls[c].kind;
                 if ((isx && kind == kUnitExpert) || (isd && kind == kUnitDept)) {
                     sm.units[sm.cls_off[c] + pre.y] = r;
-                    cpre[sm.cls_off[c] + pre.y] = pre.w;
+                    cpre[sm.cls_off[c] + pre.y] = a.cls[c].rows * pre.w + kSegCost * pre.z;
                 }
             }
             if (writer) {
@@ -424,7 +435,7 @@ __device__ void local_tables(const FfnArgs& a, FfnSmem<NS>& sm, int* cpre, const
                 if ((isx && kind == kUnitExpert) || (isd && kind == kUnitDept)) {
                     sm.cls_units[c] = tot.y;
                     sm.cls_groups[c] = tot.z;
-                    sm.cls_cost[c] = tot.w;
+                    sm.cls_cost[c] = a.cls[c].rows * tot.w + kSegCost * tot.z;
                 }
             }
             if (writer) {
@@ -441,7 +452,7 @@ __device__ void local_tables(const FfnArgs& a, FfnSmem<NS>& sm, int* cpre, const
                 cpre[sm.cls_off[c]] = 0;
                 sm.cls_units[c] = 1;
                 sm.cls_groups[c] = G;
-                sm.cls_cost[c] = cost_units(a.T);
+                sm.cls_cost[c] = unit_cost(a.T, a.cls[c].rows);
             }
         if (writer && m == 0) {
             a.ws.counts[1] = 0;
@@ -689,7 +700,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
         __syncthreads();
         if (warp < a.ncls) {
             const int nu = sm.cls_units[warp];
-            const int tot = class_cost_prefix_warp(sm.units + sm.cls_off[warp], nu, cpre + sm.cls_off[warp]);
+            const int tot = class_cost_prefix_warp(sm.units + sm.cls_off[warp], nu, a.cls[warp].rows,
+                                                   cpre + sm.cls_off[warp]);
             if (lane == 0) {
                 sm.cls_groups[warp] = nu > 0 ? sm.units[sm.cls_off[warp] + nu - 1].w : 0;
                 sm.cls_cost[warp] = tot;
@@ -713,7 +725,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
                     kept = filter_units_warp(src, A, 1, a.max_tokens, kMT, sm.units + off, &groups);
                 }
                 __syncwarp();
-                const int tot = class_cost_prefix_warp(sm.units + off, kept, cpre + off);
+                const int tot = class_cost_prefix_warp(sm.units + off, kept, uc.rows, cpre + off);
                 if (lane == 0) {
                     sm.cls_units[c] = kept;
                     sm.cls_groups[c] = groups;

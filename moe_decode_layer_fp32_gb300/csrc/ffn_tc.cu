@@ -49,12 +49,18 @@ namespace {
 constexpr int kTcRows = kTcBoxRows;               // 128
 constexpr int kChunkBytes = kTcRows * 128;        // 16 KB: one 64-column chunk
 constexpr int kAStage = 2 * kChunkBytes;          // 32 KB
-constexpr int kTcStages = 4;                      // weight ring
+#ifndef MOE_TC_STAGES
+#define MOE_TC_STAGES 4
+#endif
+#ifndef MOE_TC_BPAIRS
+#define MOE_TC_BPAIRS 3
+#endif
+constexpr int kTcStages = MOE_TC_STAGES;          // weight ring
 constexpr int kTcTokens = kTcGroupTokens;         // tokens per group (hi + lo rows: N <= 64)
 constexpr int kTcMaxN = 2 * kTcTokens;
 constexpr int kBBlock = kTcMaxN * 128;            // activations of one K-block: N rows x 128 B
 constexpr int kBPair = 2 * kBBlock;               // ... of one K-pair
-constexpr int kTcBPairs = 3;                      // activation ring (K-pairs)
+constexpr int kTcBPairs = MOE_TC_BPAIRS;         // activation ring (K-pairs)
 constexpr int kHChunk = kTcMaxN * 128;            // H: [K chunk][N rows][128 B]
 constexpr int kHTile = 2 * kHChunk;               // K = 128 tile rows
 constexpr int kTmemCols = 512;

@@ -106,7 +106,8 @@ def expected_auto_choice(shape, T, exp_count, dept_count, sms):
     wide = shape.d > 4096
     if T <= 4 and not wide:
         return 0
-    # launched only when some class expects more than 4 tokens per unit
+    # launched only when some class expects at least two CUDA-core groups
+    # (8 tokens) per unit
     expect = []
     if shape.I_sh > 0:
         miss = 1.0
@@ -117,7 +118,7 @@ def expected_auto_choice(shape, T, exp_count, dept_count, sms):
         expect.append(T * shape.k / shape.n)
     if shape.I_s > 0:
         expect.append(T)
-    if max(expect) <= 4 and not wide:
+    if max(expect) < 8 and not wide:
         return 0
     rows_cc = sum(r * sum(-(-int(c) // 4) for c in cnt) for r, cnt in classes)
     tiles = sum(r // 128 * sum(-(-int(c) // 32) for c in cnt) for r, cnt in classes)
