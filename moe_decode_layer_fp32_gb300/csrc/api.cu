@@ -269,9 +269,18 @@ int run_ffn(moe::FfnArgs& a, int T, int n, int k, int g, int has_shared, bool tc
     a.auto_tc = tc && tc_min_tokens() == 0;
     a.sms = moe::device_sm_count();
     a.max_tokens = tc && !a.auto_tc ? t.min_tokens - 1 : INT_MAX;
+    // Automatic choice: the tensor-core kernel goes first (the host launches
+    // it only when it is expected to win) and records the choice; the
+    // CUDA-core kernel follows it and returns at once when it lost.
+    a.tc_first = a.auto_tc ? 1 : 0;
+    if (a.tc_first) {
+        t.f = a;
+        e = moe::launch_ffn_tc(t, as_stream(stream));
+        if (e != cudaSuccess) return cuda_fail(e, who);
+    }
     e = moe::launch_ffn(a, as_stream(stream));
     if (e != cudaSuccess) return cuda_fail(e, who);
-    if (tc) {
+    if (tc && !a.tc_first) {
         t.f = a;
         e = moe::launch_ffn_tc(t, as_stream(stream));
         if (e != cudaSuccess) return cuda_fail(e, who);

@@ -670,6 +670,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
 
     // Everything below reads what the routing / dispatch kernel wrote.
     pdl_wait_primary();
+    // The tensor-core kernel ran first and took the step: nothing to do.
+    if (a.tc_first && *reinterpret_cast<volatile uint32_t*>(a.ws.sync + 1) == 2u) return;
 
     // ---- unit table: built here from the router logits (whole-layer path),
     // the dispatch's per-unit records (one coalesced load), or, when units
@@ -739,7 +741,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
     }
     long long R = 0;
     for (int c = 0; c < a.ncls; ++c) R += (long long)a.cls[c].rows * sm.cls_groups[c];
-    if (a.auto_tc) {
+    if (a.tc_first) {
+        // the tensor-core kernel ran first and kept the step (its choice
+        // was read right after the PDL wait, see the unit-table code)
+    } else if (a.auto_tc) {
         // the tensor-core kernel takes the whole step when it is the faster one
         __shared__ int s_tc;
         if (tid == 0) s_tc = prefer_tc(a) ? 1 : 0;

@@ -187,7 +187,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
     // warp c filters class c.  With auto_tc the kernel takes every unit when
     // prefer_tc() holds and none otherwise (the CUDA-core kernel decides alike). ----
     __shared__ int s_min_tok;
-    if (tid == 0) s_min_tok = a.f.auto_tc ? (prefer_tc(a.f) ? 1 : INT_MAX) : a.min_tokens;
+    if (tid == 0) {
+        const bool take = a.f.auto_tc && prefer_tc(a.f);
+        s_min_tok = a.f.auto_tc ? (take ? 1 : INT_MAX) : a.min_tokens;
+        // launched first: record the choice for the CUDA-core kernel that follows
+        if (a.f.tc_first && blockIdx.x == 0) a.f.ws.sync[1] = take ? 2u : 1u;
+    }
     __syncthreads();
     const int min_tok = s_min_tok;
     if (warp < a.f.ncls) {

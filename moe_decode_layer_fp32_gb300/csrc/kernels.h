@@ -65,6 +65,10 @@ struct FfnArgs {
     int pdl;              // launch as a programmatic dependent
     int max_tokens;       // CUDA-core kernel: units with more tokens are skipped
     int auto_tc;          // both kernels launched; they pick one by prefer_tc()
+    // auto_tc with the tensor-core kernel launched first: it records its
+    // choice in ws.sync[1] (1 CUDA cores, 2 tensor cores) and the CUDA-core
+    // kernel, its programmatic dependent, follows it.
+    int tc_first;
     int sms;              // SMs of the device (grid of the tensor-core kernel)
     unsigned long long grid_magic;   // set by the launcher: ceil(2^64 / grid)
     // Routing inside the CUDA-core kernel (whole-layer path, ACCUM mode, no
