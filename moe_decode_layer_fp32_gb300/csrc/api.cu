@@ -34,6 +34,10 @@ constexpr int kMaxHidden = 15 * 32 * 2 * 8;
 constexpr int kMaxRouterHidden = 128 * 16 * 4;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+// Workspace counters of the routing kernel and the FFN kernels: [0] token
+// blocks done (split top-k), [1] FFN path choice, [2 + b] blocks done on
+// token block b (every block counts on [2] when the top-k is not split).
+constexpr int kSyncWords = 2 + moe::kMaxT / 8;
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool layout_of(int T, int n, int k, int g, moe_ws_layout* L) {
@@ -66,7 +70,7 @@ bool layout_of(int T, int n, int k, int g, moe_ws_layout* L) {
     L->act_dept = take((size_t)m * sizeof(int32_t));
     L->exp_units = take((size_t)n * 4 * sizeof(int32_t));
     L->dept_units = take((size_t)m * 4 * sizeof(int32_t));
-    L->sync = take(4 * sizeof(uint32_t));
+    L->sync = take(kSyncWords * sizeof(uint32_t));
     L->xb = take((size_t)2 * T * moe::kMaxXbHidden * 2);
     L->total = off;
     return true;
@@ -311,7 +315,7 @@ int device_sm_count() {
 // this array, which the loader reserves with the module.  Its size bounds the
 // step to T * n <= kNoAllocMaxLogits.
 constexpr int kNoAllocMaxLogits = 64 * 1024;          // T * n router logits (256 KB)
-constexpr size_t kNoAllocHeader = 256;                // [0] status word, [128] block counter
+constexpr size_t kNoAllocHeader = 256;                // [0] status word, [128] block counters
 static __device__ __align__(256) unsigned char g_route_scratch[kNoAllocHeader +
                                                                (size_t)kNoAllocMaxLogits * sizeof(float)];
 

@@ -187,25 +187,49 @@ __device__ void topk_warp(const float* logits_row, const float* bias, int n, int
     if (bad && lane == 0) set_status(status, kDevErrRouting);
 }
 
+// Top-k of tokens [t0, t1), one warp per token.
 template <int J>
-__device__ __forceinline__ void topk_rows(const RouteArgs& a, int warp, int32_t* idx_sm, float* w_sm) {
-    for (int t = warp; t < a.T; t += kRouteWarps)
+__device__ __forceinline__ void topk_rows(const RouteArgs& a, int warp, int t0, int t1, int32_t* idx_sm,
+                                          float* w_sm) {
+    for (int t = t0 + warp; t < t1; t += kRouteWarps)
         topk_warp<J>(a.ws.logits + (size_t)t * a.n, a.bias, a.n, a.k, a.scale,
                      a.topk_idx + (size_t)t * a.k, a.topk_w + (size_t)t * a.k, a.ws.status,
                      idx_sm ? idx_sm + t * a.k : nullptr, idx_sm ? w_sm + t * a.k : nullptr);
 }
 
-// Router logits: block e computes expert e's logit for every token; each
-// thread holds RCH float4 chunks of the router row, all loaded up front so
-// the row arrives in one memory round trip.  The last block to finish picks
-// the top-k of every token (one warp per token) and, on the whole-layer path,
-// builds the dispatch lists.
-template <int RCH>
+template <int J>
+__device__ __forceinline__ void topk_range(const RouteArgs& a, int warp, int t0, int t1, int32_t* idx_sm,
+                                           float* w_sm) {
+    topk_rows<J>(a, warp, t0, t1, idx_sm, w_sm);
+}
+__device__ __forceinline__ void topk_any(const RouteArgs& a, int warp, int t0, int t1, int32_t* idx_sm,
+                                         float* w_sm) {
+    const int J = (a.n + 31) / 32;
+    if (J <= 1) topk_range<1>(a, warp, t0, t1, idx_sm, w_sm);
+    else if (J <= 2) topk_range<2>(a, warp, t0, t1, idx_sm, w_sm);
+    else if (J <= 4) topk_range<4>(a, warp, t0, t1, idx_sm, w_sm);
+    else if (J <= 8) topk_range<8>(a, warp, t0, t1, idx_sm, w_sm);
+    else if (J <= 16) topk_range<16>(a, warp, t0, t1, idx_sm, w_sm);
+    else topk_range<32>(a, warp, t0, t1, idx_sm, w_sm);
+}
+
+// Router logits: block (expert group, token block) computes the logits of EB
+// experts for 8 tokens; each thread holds RCH float4 chunks of each router
+// row, all loaded up front so the rows arrive in one memory round trip, and
+// every activation chunk it loads serves the EB experts.  Blocks of one
+// expert group are adjacent so that its router rows are read from HBM once
+// and then from L2.  Unless only the logits are wanted, the last block to
+// finish picks the top-k, one warp per token, and on the whole-layer path
+// builds the dispatch lists.  Beyond two token blocks (more tokens than one
+// block's warps take in one round) the top-k is split: the last block of
+// each token block to finish (a per-token-block counter) picks that block's
+// tokens, and the last token block to finish builds the dispatch.
+template <int RCH, int EB>
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
     __shared__ DispatchSmem sm;
     __shared__ int32_t s_idx[kStagedAssignments];   // top-k results for the fused dispatch
     __shared__ float s_w[kStagedAssignments];
-    __shared__ float red[kRouteWarps][8];
+    __shared__ float red[kRouteWarps][8 * EB];
     __shared__ int s_last;
     // Let the FFN grid (launched as a programmatic dependent) start its prologue.
     pdl_allow_dependents();
@@ -222,25 +246,28 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
             y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 
-    // block = (expert e, block of 8 tokens); blocks of one expert are adjacent
-    // so that its router row is read from HBM once and then from L2
     const int tblocks = (a.T + 7) >> 3;
-    const int e = blockIdx.x / tblocks;
-    const int tb = blockIdx.x - e * tblocks;
+    const int groups = a.n / EB;
+    const int eg = blockIdx.x / tblocks;
+    const int tb = blockIdx.x - eg * tblocks;
+    const int t0 = tb * 8;
     const int d4 = a.d >> 2;
-    const float4* wr = reinterpret_cast<const float4*>(a.w_router + (size_t)e * a.d);
-    float4 w[RCH];
+    float4 w[EB][RCH];
 #pragma unroll
-    for (int i = 0; i < RCH; ++i) {
-        const int c = tid + i * kRouteThreads;
-        w[i] = c < d4 ? __ldg(wr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int ee = 0; ee < EB; ++ee) {
+        const float4* wr = reinterpret_cast<const float4*>(a.w_router + (size_t)(eg * EB + ee) * a.d);
+#pragma unroll
+        for (int i = 0; i < RCH; ++i) {
+            const int c = tid + i * kRouteThreads;
+            w[ee][i] = c < d4 ? __ldg(wr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
     {
-        const int t0 = tb * 8;
-        float acc[8];
+        float acc[8 * EB];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            acc[q] = 0.f;
+#pragma unroll
+            for (int ee = 0; ee < EB; ++ee) acc[ee * 8 + q] = 0.f;
             if (t0 + q < a.T) {
                 const float4* xr = reinterpret_cast<const float4*>(a.x + (size_t)(t0 + q) * a.d);
 #pragma unroll
@@ -248,50 +275,57 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
                     const int c = tid + i * kRouteThreads;
                     if (c < d4) {
                         const float4 xv = __ldg(xr + c);
-                        acc[q] = fmaf(w[i].x, xv.x, acc[q]);
-                        acc[q] = fmaf(w[i].y, xv.y, acc[q]);
-                        acc[q] = fmaf(w[i].z, xv.z, acc[q]);
-                        acc[q] = fmaf(w[i].w, xv.w, acc[q]);
+#pragma unroll
+                        for (int ee = 0; ee < EB; ++ee) {
+                            float& r = acc[ee * 8 + q];
+                            r = fmaf(w[ee][i].x, xv.x, r);
+                            r = fmaf(w[ee][i].y, xv.y, r);
+                            r = fmaf(w[ee][i].z, xv.z, r);
+                            r = fmaf(w[ee][i].w, xv.w, r);
+                        }
                     }
                 }
             }
         }
         int vi;
-        const float v = warp_reduce_spread<8>(acc, lane, vi);
-        if ((lane & 3) == 0) red[warp][vi] = v;
+        const float v = warp_reduce_spread<8 * EB>(acc, lane, vi);
+        if ((lane & (32 / (8 * EB) - 1)) == 0) red[warp][vi] = v;
         __syncthreads();
-        if (tid < 8 && t0 + tid < a.T) {
+        if (tid < 8 * EB && t0 + (tid & 7) < a.T) {
             float s = 0.f;
 #pragma unroll
             for (int w_ = 0; w_ < kRouteWarps; ++w_) s += red[w_][tid];
-            a.ws.logits[(size_t)(t0 + tid) * a.n + e] = s;
+            a.ws.logits[(size_t)(t0 + (tid & 7)) * a.n + eg * EB + (tid >> 3)] = s;
         }
         __syncthreads();
     }
     if (a.logits_only) return;
-    // Count this block in.  The counter add is a GPU-scope release/acquire:
-    // it publishes the block's logits (ordered before it by the CTA barrier
-    // above) and lets the last block to arrive see every block's logits
-    // (ordered for its other threads by the barrier below).
-    if (tid == 0) s_last = atomic_add_acq_rel_gpu(&a.ws.sync[0], 1u) == gridDim.x - 1;
+    // Count this block in (on its token block when the top-k is split).  The
+    // counter add is a GPU-scope release/acquire: it publishes the block's
+    // logits (ordered before it by the CTA barrier above) and lets the last
+    // block to arrive see every counted block's logits (ordered for its
+    // other threads by the barrier below).
+    const bool split = tblocks > 2;
+    const int ctr = split ? 2 + tb : 2;
+    const uint32_t arrivals = (uint32_t)(split ? groups : groups * tblocks);
+    if (tid == 0) s_last = atomic_add_acq_rel_gpu(&a.ws.sync[ctr], 1u) == arrivals - 1;
     __syncthreads();
     if (!s_last) return;
-    const int J = (a.n + 31) / 32;
-    // the fused dispatch reads the top-k results from shared memory when they fit
-    const bool staged = a.fuse_dispatch && a.T * a.k <= kStagedAssignments;
-    int32_t* idx_sm = staged ? s_idx : nullptr;
-    if (J <= 1) topk_rows<1>(a, warp, idx_sm, s_w);
-    else if (J <= 2) topk_rows<2>(a, warp, idx_sm, s_w);
-    else if (J <= 4) topk_rows<4>(a, warp, idx_sm, s_w);
-    else if (J <= 8) topk_rows<8>(a, warp, idx_sm, s_w);
-    else if (J <= 16) topk_rows<16>(a, warp, idx_sm, s_w);
-    else topk_rows<32>(a, warp, idx_sm, s_w);
-    if (tid == 0) a.ws.sync[0] = 0u;  // ready for the next call
-    if (a.fuse_dispatch) {
-        __syncthreads();
-        dispatch_block<kRouteThreads>(staged ? s_idx : a.topk_idx, staged ? s_w : a.topk_w, a.T, a.n,
-                                      a.k, a.g, a.ws, sm);
-    }
+    // the fused dispatch reads the top-k results from shared memory when one
+    // block picked them all and they fit
+    const bool staged = a.fuse_dispatch && !split && a.T * a.k <= kStagedAssignments;
+    topk_any(a, warp, split ? t0 : 0, split ? min(t0 + 8, a.T) : a.T, staged ? s_idx : nullptr, s_w);
+    if (tid == 0) a.ws.sync[ctr] = 0u;  // ready for the next call
+    if (!a.fuse_dispatch) return;
+    // With a split top-k the last token block to finish builds the dispatch;
+    // same ordering argument, one level up, for the other blocks' outputs.
+    __syncthreads();
+    if (tid == 0) s_last = !split || atomic_add_acq_rel_gpu(&a.ws.sync[0], 1u) == (uint32_t)tblocks - 1;
+    __syncthreads();
+    if (!s_last) return;
+    if (tid == 0) a.ws.sync[0] = 0u;
+    dispatch_block<kRouteThreads>(staged ? s_idx : a.topk_idx, staged ? s_w : a.topk_w, a.T, a.n, a.k,
+                                  a.g, a.ws, sm);
 }
 
 __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs a) {
@@ -301,13 +335,22 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
 
 }  // namespace
 
+template <int EB>
+void launch_route_eb(const RouteArgs& a, int rch, int blocks, cudaStream_t s) {
+    if (rch <= 1) route_kernel<1, EB><<<blocks, kRouteThreads, 0, s>>>(a);
+    else if (rch <= 2) route_kernel<2, EB><<<blocks, kRouteThreads, 0, s>>>(a);
+    else route_kernel<4, EB><<<blocks, kRouteThreads, 0, s>>>(a);
+}
+
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
     // float4 chunks of a router row per thread: ceil(d / 4 / threads)
     const int rch = (a.d / 4 + kRouteThreads - 1) / kRouteThreads;
-    const int blocks = a.n * ((a.T + 7) / 8);
-    if (rch <= 1) route_kernel<1><<<blocks, kRouteThreads, 0, s>>>(a);
-    else if (rch <= 2) route_kernel<2><<<blocks, kRouteThreads, 0, s>>>(a);
-    else route_kernel<4><<<blocks, kRouteThreads, 0, s>>>(a);
+    const int tblocks = (a.T + 7) / 8;
+    // from four token blocks on, 4 experts per block so that each activation
+    // chunk serves 4; below, one expert per block for parallelism
+    const int eb = a.n % 4 == 0 && tblocks >= 4 ? 4 : 1;
+    if (eb == 4) launch_route_eb<4>(a, rch, a.n / 4 * tblocks, s);
+    else launch_route_eb<1>(a, rch, a.n * tblocks, s);
     return cudaGetLastError();
 }
 
