@@ -252,38 +252,64 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
     const int tb = blockIdx.x - eg * tblocks;
     const int t0 = tb * 8;
     const int d4 = a.d >> 2;
-    float4 w[EB][RCH];
-#pragma unroll
-    for (int ee = 0; ee < EB; ++ee) {
-        const float4* wr = reinterpret_cast<const float4*>(a.w_router + (size_t)(eg * EB + ee) * a.d);
-#pragma unroll
-        for (int i = 0; i < RCH; ++i) {
-            const int c = tid + i * kRouteThreads;
-            w[ee][i] = c < d4 ? __ldg(wr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    }
     {
         float acc[8 * EB];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 0; q < 8 * EB; ++q) acc[q] = 0.f;
+        if constexpr (EB == 1) {
+            // one expert: its router chunks are loaded up front (one round
+            // trip), then the tokens' activations chunk by chunk
+            float4 w[RCH];
+            const float4* wr = reinterpret_cast<const float4*>(a.w_router + (size_t)eg * a.d);
 #pragma unroll
-            for (int ee = 0; ee < EB; ++ee) acc[ee * 8 + q] = 0.f;
-            if (t0 + q < a.T) {
-                const float4* xr = reinterpret_cast<const float4*>(a.x + (size_t)(t0 + q) * a.d);
+            for (int i = 0; i < RCH; ++i) {
+                const int c = tid + i * kRouteThreads;
+                w[i] = c < d4 ? __ldg(wr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
 #pragma unroll
-                for (int i = 0; i < RCH; ++i) {
-                    const int c = tid + i * kRouteThreads;
-                    if (c < d4) {
-                        const float4 xv = __ldg(xr + c);
+            for (int q = 0; q < 8; ++q) {
+                if (t0 + q < a.T) {
+                    const float4* xr = reinterpret_cast<const float4*>(a.x + (size_t)(t0 + q) * a.d);
+#pragma unroll
+                    for (int i = 0; i < RCH; ++i) {
+                        const int c = tid + i * kRouteThreads;
+                        if (c < d4) {
+                            const float4 xv = __ldg(xr + c);
+                            acc[q] = fmaf(w[i].x, xv.x, acc[q]);
+                            acc[q] = fmaf(w[i].y, xv.y, acc[q]);
+                            acc[q] = fmaf(w[i].z, xv.z, acc[q]);
+                            acc[q] = fmaf(w[i].w, xv.w, acc[q]);
+                        }
+                    }
+                }
+            }
+        } else {
+            // several experts: chunk by chunk, the EB router chunks and the 8
+            // tokens' activation chunks of a step are loaded together, so a
+            // wide row costs one round trip per chunk, not per token; per
+            // logit the sum runs over the chunks in the same order
+#pragma unroll
+            for (int i = 0; i < RCH; ++i) {
+                const int c = tid + i * kRouteThreads;
+                if (c < d4) {
+                    float4 wv[EB], xv[8];
+#pragma unroll
+                    for (int ee = 0; ee < EB; ++ee)
+                        wv[ee] = __ldg(reinterpret_cast<const float4*>(a.w_router + (size_t)(eg * EB + ee) * a.d) + c);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        xv[q] = t0 + q < a.T ? __ldg(reinterpret_cast<const float4*>(a.x + (size_t)(t0 + q) * a.d) + c)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
 #pragma unroll
                         for (int ee = 0; ee < EB; ++ee) {
                             float& r = acc[ee * 8 + q];
-                            r = fmaf(w[ee][i].x, xv.x, r);
-                            r = fmaf(w[ee][i].y, xv.y, r);
-                            r = fmaf(w[ee][i].z, xv.z, r);
-                            r = fmaf(w[ee][i].w, xv.w, r);
+                            r = fmaf(wv[ee].x, xv[q].x, r);
+                            r = fmaf(wv[ee].y, xv[q].y, r);
+                            r = fmaf(wv[ee].z, xv[q].z, r);
+                            r = fmaf(wv[ee].w, xv[q].w, r);
                         }
-                    }
                 }
             }
         }
