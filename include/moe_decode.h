@@ -296,14 +296,16 @@ int moe_combine(const float* rows, int T, int d, int n, int k, int experts_per_d
 /*
  * route -> dispatch -> FFN (MOE_OUT_ACCUM) in two or three launches.  The
  * router kernel also zeroes y; the FFN launches as its programmatic dependent.
- * When the step runs on the CUDA-core FFN kernel alone (no tensor-core
- * launch, n <= 256), the router kernel writes the logits only and every CTA
- * of the FFN kernel takes the top-k and builds the dispatch itself in shared
- * memory; otherwise the router kernel's last block does both for the FFN
- * kernels to read.  Either way topk_idx / topk_w receive the routing like
- * moe_route_topk, and the workspace afterwards holds the dispatch lists of
- * moe_dispatch (so an FFN step in MOE_OUT_ROWS mode and moe_combine can
- * follow on the same workspace).
+ * When the step runs on one FFN kernel alone (n <= 256) the router kernel
+ * writes the logits only and every CTA of that FFN kernel takes the top-k
+ * and builds the dispatch itself in shared memory: the CUDA-core kernel
+ * when the tensor-core kernel is not launched, the tensor-core kernel when
+ * rows are at most 4096 wide, T <= 32 and the automatic choice launches it.
+ * Otherwise the router kernel builds the dispatch for the FFN kernels to read
+ * (and both run, one of them choosing on the device).  Either way topk_idx /
+ * topk_w receive the routing like moe_route_topk, and the workspace
+ * afterwards holds the dispatch lists of moe_dispatch (so an FFN step in
+ * MOE_OUT_ROWS mode and moe_combine can follow on the same workspace).
  */
 int moe_layer_forward(const float* x, int T, int d, int n, int k, float scale,
                       const float* w_router, const float* bias,

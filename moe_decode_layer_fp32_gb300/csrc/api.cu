@@ -236,7 +236,7 @@ bool prepare_tc(const moe::FfnArgs& a, int T, moe::TcArgs* t) {
     int units = 0;
     for (int c = 0; c < a.ncls; ++c) units += moe::class_capacity(a.cls[c], a.n, a.g);
     if (a.dtype != MOE_DTYPE_BF16 || a.d % moe::kTcHiddenQuantum != 0 || a.d > moe::kMaxXbHidden || T < mt ||
-        moe::ffn_tc_smem_bytes(units) > 227 * 1024)
+        moe::ffn_tc_smem_bytes(units, nullptr) > 227 * 1024)
         return false;
     for (int c = 0; c < a.ncls; ++c)
         if (a.cls[c].rows % moe::kTcBoxRows != 0) return false;
@@ -597,6 +597,47 @@ int moe_combine(const float* rows, int T, int d, int n, int k, int experts_per_d
     return MOE_OK;
 }
 
+// How the whole-layer step runs its FFN:
+//  - kLayerCudaLocal: the CUDA-core kernel alone, routing inside its CTAs;
+//  - kLayerTcLocal: the tensor-core kernel alone, routing inside its CTAs
+//    (automatic mode, rows up to kTcWideHidden wide, T <= 32, when the host
+//    rule expects the tensor cores to win: at least two CUDA-core groups per
+//    unit);
+//  - kLayerGlobal: the routing kernel builds the dispatch, and the FFN kernels
+//    read it (automatic choice on the device for wide rows, or a fixed
+//    tensor-core threshold).
+enum { kLayerCudaLocal = 0, kLayerTcLocal = 1, kLayerGlobal = 2 };
+
+static int layer_path(const moe::FfnArgs& a, bool tc, const moe::TcArgs& t) {
+    (void)t;
+    if (!tc) return moe::ffn_local_route_fits(a) ? kLayerCudaLocal : kLayerGlobal;
+    // beyond 32 tokens one CTA's top-k (a warp per token) takes more rounds
+    // than the routing kernel's split top-k saves
+    if (tc_min_tokens() == 0 && a.d <= moe::kTcWideHidden && a.T <= 32) {
+        moe::FfnArgs b = a;
+        b.local_route = 1;
+        if (moe::ffn_tc_local_route_fits(b)) return kLayerTcLocal;
+    }
+    return kLayerGlobal;
+}
+
+// FFN step of the whole-layer path (after layer_route).
+static int layer_ffn(moe::FfnArgs& a, int T, int n, int k, int g, int has_shared, bool tc, moe::TcArgs& t,
+                     int path, void* stream, const char* who) {
+    if (path != kLayerTcLocal) return run_ffn(a, T, n, k, g, has_shared, tc, t, true, stream, who);
+    a.rows_dept_base = T * k;
+    a.rows_shared_base = (int)rows_count(T, n, k, g, 0);
+    a.auto_tc = 0;
+    a.tc_first = 0;
+    a.max_tokens = INT_MAX;
+    a.sms = moe::device_sm_count();
+    t.f = a;
+    t.min_tokens = 1;
+    cudaError_t e = moe::launch_ffn_tc(t, as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    return MOE_OK;
+}
+
 // Routing step of the whole-layer path.  With `local` the routing kernel
 // writes the logits only and the CUDA-core FFN kernel (a.local_route) takes
 // the top-k and builds the dispatch in every CTA; otherwise the routing
@@ -648,11 +689,11 @@ int moe_layer_forward(const float* x, int T, int d, int n, int k, float scale,
     layout_of(T, n, k, 1, &L);
     moe::TcArgs t;
     const bool tc = prepare_tc(a, T, &t);
-    const bool local = !tc && moe::ffn_local_route_fits(a);
+    const int path = layer_path(a, tc, t);
     if ((rc = layer_route(x, T, d, n, k, scale, w_router, bias, 1, L, ws, topk_idx, topk_w, y, tc,
-                          local, a, stream, who)))
+                          path != kLayerGlobal, a, stream, who)))
         return rc;
-    return run_ffn(a, T, n, k, 1, I_s > 0, tc, t, true, stream, who);
+    return layer_ffn(a, T, n, k, 1, I_s > 0, tc, t, path, stream, who);
 }
 
 int deamoe_layer_forward(const float* x, int T, int d, int n, int k, float scale,
@@ -672,11 +713,11 @@ int deamoe_layer_forward(const float* x, int T, int d, int n, int k, float scale
     layout_of(T, n, k, experts_per_dept, &L);
     moe::TcArgs t;
     const bool tc = prepare_tc(a, T, &t);
-    const bool local = !tc && moe::ffn_local_route_fits(a);
+    const int path = layer_path(a, tc, t);
     if ((rc = layer_route(x, T, d, n, k, scale, w_router, bias, experts_per_dept, L, ws, topk_idx,
-                          topk_w, y, tc, local, a, stream, who)))
+                          topk_w, y, tc, path != kLayerGlobal, a, stream, who)))
         return rc;
-    return run_ffn(a, T, n, k, experts_per_dept, I_s > 0, tc, t, true, stream, who);
+    return layer_ffn(a, T, n, k, experts_per_dept, I_s > 0, tc, t, path, stream, who);
 }
 
 int64_t moe_unique_weight_bytes_vanilla(int d, int n, int I, int I_s, int dtype, int A_e) {

@@ -23,6 +23,7 @@
 
 #include "../../include/moe_decode.h"
 #include "kernels.h"
+#include "local_route.cuh"
 
 namespace moe {
 
@@ -118,28 +119,6 @@ __device__ __forceinline__ bool next_seg(const FfnArgs& a, const FfnSmem<NS>& sm
 // A unit of t tokens costs rows * cost_units(t) + groups * kSegCost; every
 // class keeps the exclusive prefix of its units' costs (cpre) next to the
 // unit records.
-#ifndef MOE_COST_NARROW
-#define MOE_COST_NARROW 2
-#endif
-#ifndef MOE_COST_WIDE
-#define MOE_COST_WIDE 3
-#endif
-#ifndef MOE_COST_SEG
-#define MOE_COST_SEG 24
-#endif
-constexpr int kCostNarrow = MOE_COST_NARROW;
-constexpr int kCostWide = MOE_COST_WIDE;
-constexpr int kSegCost = MOE_COST_SEG;
-
-__device__ __forceinline__ int group_cost(int mg) { return mg > 2 ? kCostWide : kCostNarrow; }
-__device__ __forceinline__ int cost_units(int t) {
-    return (t / kMT) * group_cost(kMT) + (t % kMT ? group_cost(t % kMT) : 0);
-}
-// Cost of a unit of t tokens whose rows are `rows` long.
-__device__ __forceinline__ int unit_cost(int t, int rows) {
-    return rows * cost_units(t) + ((t + kMT - 1) / kMT) * kSegCost;
-}
-
 // One warp: exclusive prefix of the records' unit costs into cpre; returns
 // the class total (on every lane).
 __device__ __forceinline__ int class_cost_prefix_warp(const int4* u, int nu, int rows, int* cpre) {
@@ -235,306 +214,6 @@ __device__ __forceinline__ int group_tokens(const FfnArgs& a, const int4 rec, in
             wt[i] = w;
             orow[i] = a.out_mode == MOE_OUT_ACCUM ? t : row;
         }
-    }
-    return mg;
-}
-
-// ---- routing inside the CTA (whole-layer path) ------------------------------
-// Every CTA takes the top-k of every token from the router logits and builds
-// its own unit records and per-unit token lists in shared memory, so that no
-// single block serialises the dispatch and nothing is read back from global
-// memory.  Order and content match the dispatch kernel's: ascending unit id,
-// then ascending token id; a department's token set X^j is the union of its
-// experts' sets, with weight omega = sum of the token's routing weights on
-// that department's experts, in slot order.  Units sit one per thread (the
-// experts, then the departments from the next warp boundary on), so the host
-// takes this path only when roundup32(n) + m fits the block.
-struct LocalRoute {
-    uint32_t* emask;   // [n][W]: bit t of row e = token t chose expert e
-    uint32_t* dmask;   // [m][W]: union over the department's experts
-    int16_t* idx;      // [T*k] selected experts
-    int16_t* didx;     // [T*k] their departments
-    float* w;          // [T*k] routing weights
-    int* off;          // [n + m] first list entry of each expert, then each department
-    int16_t* etok;     // [T*k] expert lists (ascending expert, then token): token
-    float* ew;         //       and routing weight
-    int16_t* dtok;     // [T*min(k, m)] department lists: token
-    float* dw;         //       and department weight omega
-    int4* wtot;        // per warp: totals of the unit scan
-    int* tcg;          // [2] tensor-core group totals (experts, departments)
-    int W, m;
-};
-
-__host__ __device__ __forceinline__ size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
-
-// Bytes of the local routing state for a block of nwarps warps.
-__host__ __device__ __forceinline__ size_t local_route_bytes(int T, int n, int k, int g, int nwarps) {
-    const size_t W = (size_t)(T + 31) / 32;
-    const size_t m = g > 1 ? (size_t)(n / g) : 0;
-    const size_t TK = (size_t)T * k;
-    const size_t DK = m ? (size_t)T * ((size_t)k < m ? (size_t)k : m) : 0;
-    return align16(4 * n * W) + align16(4 * m * W) + align16(2 * TK) * 2 + align16(4 * TK) +
-           align16(4 * (n + m)) + align16(2 * TK) + align16(4 * TK) + align16(2 * DK) + align16(4 * DK) +
-           align16(16 * (size_t)nwarps) + 16;
-}
-
-__device__ __forceinline__ LocalRoute local_route_at(unsigned char* p, int T, int n, int k, int g,
-                                                     int nwarps) {
-    LocalRoute lr;
-    lr.W = (T + 31) >> 5;
-    lr.m = g > 1 ? n / g : 0;
-    const size_t TK = (size_t)T * k;
-    const size_t DK = lr.m ? (size_t)T * (k < lr.m ? k : lr.m) : 0;
-    auto take = [&](size_t bytes) {
-        unsigned char* q = p;
-        p += align16(bytes);
-        return q;
-    };
-    lr.emask = reinterpret_cast<uint32_t*>(take(4 * (size_t)n * lr.W));
-    lr.dmask = reinterpret_cast<uint32_t*>(take(4 * (size_t)lr.m * lr.W));
-    lr.idx = reinterpret_cast<int16_t*>(take(2 * TK));
-    lr.didx = reinterpret_cast<int16_t*>(take(2 * TK));
-    lr.w = reinterpret_cast<float*>(take(4 * TK));
-    lr.off = reinterpret_cast<int*>(take(4 * (size_t)(n + lr.m)));
-    lr.etok = reinterpret_cast<int16_t*>(take(2 * TK));
-    lr.ew = reinterpret_cast<float*>(take(4 * TK));
-    lr.dtok = reinterpret_cast<int16_t*>(take(2 * DK));
-    lr.dw = reinterpret_cast<float*>(take(4 * DK));
-    lr.wtot = reinterpret_cast<int4*>(take(16 * (size_t)nwarps));
-    lr.tcg = reinterpret_cast<int*>(take(16));
-    return lr;
-}
-
-// Rank of token t among the tokens of a mask row (ascending).
-__device__ __forceinline__ int row_rank(const uint32_t* row, int t) {
-    int r = __popc(row[t >> 5] & ((1u << (t & 31)) - 1u));
-    for (int w = 0; w < (t >> 5); ++w) r += __popc(row[w]);
-    return r;
-}
-
-// Top-k of every token, one warp per token: selections into shared memory,
-// the expert bitmasks (zeroed by the caller) and department ids; CTA 0 also
-// stores them as the routing outputs.  Ends with a barrier.
-template <int J, int NT>
-__device__ void local_topk_rows(const FfnArgs& a, const LocalRoute& lr, bool writer) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int t = warp; t < a.T; t += NT / 32) {
-        int e;
-        float w;
-        const bool bad =
-            topk_select_warp<J>(a.ws.logits + (size_t)t * a.n, a.bias, a.n, a.k, a.scale, e, w);
-        if (lane < a.k) {
-            lr.idx[t * a.k + lane] = (int16_t)e;
-            lr.didx[t * a.k + lane] = (int16_t)(a.g > 1 ? e / a.g : e);
-            lr.w[t * a.k + lane] = w;
-            atomicOr(&lr.emask[e * lr.W + (t >> 5)], 1u << (t & 31));
-            if (writer) {
-                a.topk_idx[(size_t)t * a.k + lane] = e;
-                a.topk_w[(size_t)t * a.k + lane] = w;
-            }
-        }
-        if (bad && writer && lane == 0) set_status(a.ws.status, kDevErrRouting);
-    }
-    __syncthreads();
-}
-
-template <int NT>
-__device__ __forceinline__ void local_topk(const FfnArgs& a, const LocalRoute& lr, bool writer) {
-    const int J = (a.n + 31) / 32;
-    if (J <= 1) local_topk_rows<1, NT>(a, lr, writer);
-    else if (J <= 2) local_topk_rows<2, NT>(a, lr, writer);
-    else if (J <= 4) local_topk_rows<4, NT>(a, lr, writer);
-    else local_topk_rows<8, NT>(a, lr, writer);
-}
-
-// Inclusive warp scan of four counters.
-__device__ __forceinline__ int4 warp_inclusive_scan4(int4 v) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int tx = __shfl_up_sync(0xffffffffu, v.x, o);
-        const int ty = __shfl_up_sync(0xffffffffu, v.y, o);
-        const int tz = __shfl_up_sync(0xffffffffu, v.z, o);
-        const int tw = __shfl_up_sync(0xffffffffu, v.w, o);
-        if (lane >= o) {
-            v.x += tx;
-            v.y += ty;
-            v.z += tz;
-            v.w += tw;
-        }
-    }
-    return v;
-}
-
-// After the top-k (every thread of the CTA; ends with a barrier): unit
-// counts, records and cost prefixes of every class, then the per-unit token
-// lists.  Expert u sits on thread u, department j on thread roundup32(n) + j,
-// so each kind's prefix sums are warp scans plus the totals of its earlier
-// warps.  CTA 0 (`writer`) also stores the dispatch in the workspace in the
-// layout moe_dispatch writes.
-template <int NS, int NT>
-__device__ void local_tables(const FfnArgs& a, FfnSmem<NS>& sm, int* cpre, const LocalRoute& lr,
-                             bool writer) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int n = a.n, m = lr.m, W = lr.W;
-    const int n_pad = (n + 31) & ~31;
-    const bool isx = tid < n;
-    const bool isd = m > 0 && tid >= n_pad && tid < n_pad + m;
-    const int u = isx ? tid : tid - n_pad;
-    int cnt = 0;
-    if (isx) {
-        for (int w = 0; w < W; ++w) cnt += __popc(lr.emask[u * W + w]);
-    } else if (isd) {
-        for (int w = 0; w < W; ++w) {
-            uint32_t v = 0u;
-            for (int e = u * a.g; e < (u + 1) * a.g; ++e) v |= lr.emask[e * W + w];
-            lr.dmask[u * W + w] = v;
-            cnt += __popc(v);
-        }
-    }
-    // tokens, active units, groups, cost units
-    const int4 mine = make_int4(cnt, cnt > 0 ? 1 : 0, (cnt + kMT - 1) / kMT, cost_units(cnt));
-    const int4 inc = warp_inclusive_scan4(mine);
-    if (lane == 31) lr.wtot[warp] = inc;
-    if (tid < 2) lr.tcg[tid] = 0;
-    __syncthreads();
-    int4 pre = make_int4(inc.x - mine.x, inc.y - mine.y, inc.z - mine.z, inc.w - mine.w);
-    for (int w2 = isd ? n_pad / 32 : 0; w2 < warp; ++w2) {
-        const int4 t = lr.wtot[w2];
-        pre.x += t.x;
-        pre.y += t.y;
-        pre.z += t.z;
-        pre.w += t.w;
-    }
-    if (isx || isd) {
-        lr.off[isx ? u : n + u] = pre.x;
-        if (cnt > 0) {
-            const int4 r = make_int4(u, pre.x, cnt, pre.z + mine.z);
-            for (int c = 0; c < a.ncls; ++c) {
-                const int kind = a.cls[c].kind;
-                if ((isx && kind == kUnitExpert) || (isd && kind == kUnitDept)) {
-                    sm.units[sm.cls_off[c] + pre.y] = r;
-                    cpre[sm.cls_off[c] + pre.y] = a.cls[c].rows * pre.w + kSegCost * pre.z;
-                }
-            }
-            if (writer) {
-                (isd ? a.ws.act_dept : a.ws.act_exp)[pre.y] = u;
-                (isd ? a.ws.dept_units : a.ws.exp_units)[pre.y] = r;
-                atomicAdd(&lr.tcg[isd ? 1 : 0], (cnt + kTcGroupTokens - 1) / kTcGroupTokens);
-            }
-        }
-        if (writer) {
-            (isd ? a.ws.dept_count : a.ws.exp_count)[u] = cnt;
-            (isd ? a.ws.dept_off : a.ws.exp_off)[u] = pre.x;
-        }
-        // the last unit of each kind holds the kind's totals
-        if (u == (isd ? m : n) - 1) {
-            const int4 tot = make_int4(pre.x + mine.x, pre.y + mine.y, pre.z + mine.z, pre.w + mine.w);
-            for (int c = 0; c < a.ncls; ++c) {
-                const int kind = a.cls[c].kind;
-                if ((isx && kind == kUnitExpert) || (isd && kind == kUnitDept)) {
-                    sm.cls_units[c] = tot.y;
-                    sm.cls_groups[c] = tot.z;
-                    sm.cls_cost[c] = a.cls[c].rows * tot.w + kSegCost * tot.z;
-                }
-            }
-            if (writer) {
-                (isd ? a.ws.dept_off : a.ws.exp_off)[isd ? m : n] = tot.x;
-                a.ws.counts[isd ? 1 : 0] = tot.y;
-            }
-        }
-    }
-    if (tid == 0) {
-        for (int c = 0; c < a.ncls; ++c)
-            if (a.cls[c].kind == kUnitShared) {
-                const int G = (a.T + kMT - 1) / kMT;
-                sm.units[sm.cls_off[c]] = make_int4(0, 0, a.T, G);
-                cpre[sm.cls_off[c]] = 0;
-                sm.cls_units[c] = 1;
-                sm.cls_groups[c] = G;
-                sm.cls_cost[c] = unit_cost(a.T, a.cls[c].rows);
-            }
-        if (writer && m == 0) {
-            a.ws.counts[1] = 0;
-            a.ws.counts[3] = 0;
-        }
-    }
-    __syncthreads();
-    if (writer && tid == 0) {
-        a.ws.counts[2] = lr.tcg[0];
-        if (m > 0) a.ws.counts[3] = lr.tcg[1];
-    }
-    // token lists: expert lists from every assignment, department lists from
-    // the first slot of each token on each department
-    const int TK = a.T * a.k;
-    for (int i = tid; i < TK; i += NT) {
-        const int t = i / a.k, sl = i - t * a.k;
-        const int e = lr.idx[i];
-        const float wv = lr.w[i];
-        const int pos = lr.off[e] + row_rank(lr.emask + e * W, t);
-        lr.etok[pos] = (int16_t)t;
-        lr.ew[pos] = wv;
-        if (writer) {
-            a.ws.asg_tok[pos] = t;
-            a.ws.asg_slot[pos] = sl;
-            a.ws.asg_w[pos] = wv;
-            a.ws.tok_asg[i] = pos;
-        }
-        if (m > 0) {
-            const int j = lr.didx[i];
-            bool first = true;
-            float om = 0.0f;   // omega: the token's weights on department j, slot order
-            for (int q = 0; q < a.k; ++q)
-                if (lr.didx[t * a.k + q] == j) {
-                    if (q < sl) first = false;
-                    om += lr.w[t * a.k + q];
-                }
-            if (first) {
-                const int pd = lr.off[n + j] + row_rank(lr.dmask + j * W, t);
-                lr.dtok[pd] = (int16_t)t;
-                lr.dw[pd] = om;
-                if (writer) {
-                    a.ws.dept_tok[pd] = t;
-                    a.ws.dept_w[pd] = om;
-                    a.ws.tok_dpos[t * m + j] = pd;
-                }
-            }
-        }
-    }
-    if (writer && m > 0)
-        for (int i = tid; i < a.T * m; i += NT) {
-            const int t = i / m, j = i - t * m;
-            if (!((lr.dmask[j * W + (t >> 5)] >> (t & 31)) & 1u)) a.ws.tok_dpos[i] = -1;
-        }
-    __syncthreads();
-}
-
-// Tokens of group `grp` of a unit from the shared-memory lists, with their
-// weights (ACCUM mode: the output row is the token).
-__device__ __forceinline__ int group_tokens_local(const LocalRoute& lr, const int4 rec, int kind, int grp,
-                                                  int (&tok)[kMT], float (&wt)[kMT], int (&orow)[kMT]) {
-    const int first = grp * kMT;
-    const int mg = min(kMT, rec.z - first);
-    const int p0 = rec.y + first;
-#pragma unroll
-    for (int i = 0; i < kMT; ++i) {
-        int t = 0;
-        float w = 0.0f;
-        if (i < mg) {
-            if (kind == kUnitShared) {
-                t = first + i;
-                w = 1.0f;
-            } else if (kind == kUnitDept) {
-                t = lr.dtok[p0 + i];
-                w = lr.dw[p0 + i];
-            } else {
-                t = lr.etok[p0 + i];
-                w = lr.ew[p0 + i];
-            }
-        }
-        tok[i] = t;
-        wt[i] = w;
-        orow[i] = t;
     }
     return mg;
 }
@@ -680,7 +359,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
     if (a.local_route) {
         const bool writer = blockIdx.x == 0;
         local_topk<kNT>(a, lr, writer);
-        local_tables<NS, kNT>(a, sm, cpre, lr, writer);
+        const UnitTableView view = {sm.units, sm.cls_off, sm.cls_units, sm.cls_groups, sm.cls_cost, cpre};
+        local_tables<kNT, kMT, true>(a, view, lr, writer);
     } else if (a.max_tokens >= a.T) {
         int off = 0;
         for (int c = 0; c < a.ncls; ++c) {

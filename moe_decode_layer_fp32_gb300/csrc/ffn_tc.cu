@@ -36,6 +36,7 @@
 
 #include "../../include/moe_decode.h"
 #include "kernels.h"
+#include "local_route.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -115,9 +116,16 @@ __device__ __forceinline__ bool next_tile(const TcArgs& a, const TcSmem& sm, int
     return true;
 }
 
-// Token t, routing weight and output row of entry j of a unit's token list.
-__device__ __forceinline__ void tile_token(const TcArgs& a, int kind, int entry, int& t,
-                                           float& w, int& row) {
+// Token t, routing weight and output row of entry j of a unit's token list
+// (from the CTA's own lists on the in-CTA routing path, LOCAL).
+template <bool LOCAL>
+__device__ __forceinline__ void tile_token(const TcArgs& a, const LocalRoute& lr, int kind, int entry,
+                                           int& t, float& w, int& row) {
+    if (LOCAL) {
+        local_entry(lr, kind, entry, t, w);
+        row = t;
+        return;
+    }
     if (kind == kUnitShared) {
         t = entry;
         w = 1.0f;
@@ -134,6 +142,9 @@ __device__ __forceinline__ void tile_token(const TcArgs& a, int kind, int entry,
     if (a.f.out_mode == MOE_OUT_ACCUM) row = t;
 }
 
+// LOCAL: the in-CTA routing path (a.f.local_route); a separate instantiation
+// so that the path reading the dispatch from global memory keeps its code.
+template <bool LOCAL>
 __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_constant__ TcArgs a) {
     extern __shared__ unsigned char smem_dyn[];
     // 1024-byte aligned tile regions (128 B swizzle atoms)
@@ -175,6 +186,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
         tmem_alloc(&sm.tmem_base, kTmemCols);
         tmem_relinquish();
     }
+    // in-CTA routing: its state follows the unit table
+    LocalRoute lr = {};
+    if (LOCAL) {
+        int cap = 0;
+        for (int c = 0; c < a.f.ncls; ++c) cap += class_capacity(a.f.cls[c], a.f.n, a.f.g);
+        lr = local_route_at(reinterpret_cast<unsigned char*>(sm.units + cap), a.f.T, a.f.n, a.f.k, a.f.g,
+                            kTcWarps);
+        for (int i = tid; i < a.f.n * lr.W; i += kTcThreads) lr.emask[i] = 0u;
+        if (tid == 0) {
+            int off = 0;
+            for (int c = 0; c < a.f.ncls; ++c) {
+                sm.cls_off[c] = off;
+                off += class_capacity(a.f.cls[c], a.f.n, a.f.g);
+            }
+        }
+    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -183,9 +210,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
     // Everything below reads what the routing / dispatch kernel wrote.
     pdl_wait_primary();
 
-    // ---- unit table: this kernel's units (>= min_tokens tokens), groups of kTcTokens;
+    // ---- unit table: on the in-CTA routing path every unit, built here from
+    // the router logits (CTA 0 also stores the routing and the dispatch).
+    // Otherwise this kernel's units (>= min_tokens tokens), groups of kTcTokens;
     // warp c filters class c.  With auto_tc the kernel takes every unit when
     // prefer_tc() holds and none otherwise (the CUDA-core kernel decides alike). ----
+    if (LOCAL) {
+        const bool writer = blockIdx.x == 0;
+        local_topk<kTcThreads>(a.f, lr, writer);
+        const UnitTableView view = {sm.units, sm.cls_off, sm.cls_units, sm.cls_groups, nullptr, nullptr};
+        local_tables<kTcThreads, kTcTokens, false>(a.f, view, lr, writer);
+        if (writer && tid == 0) a.f.ws.sync[1] = 2u;
+    } else {
     __shared__ int s_min_tok;
     if (tid == 0) {
         const bool take = a.f.auto_tc && prefer_tc(a.f);
@@ -221,6 +257,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
         }
     }
     __syncthreads();
+    }
 
     // CTA's share of the row space, in whole tiles
     int Q = 0;
@@ -357,7 +394,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
             if (lane < mg) {
                 int t, row;
                 float w;
-                tile_token(a, kind, first + lane, t, w, row);
+                tile_token<LOCAL>(a, lr, kind, first + lane, t, w, row);
                 sm.ep_row[quarter][lane] = row;
                 sm.ep_w[quarter][lane] = w;
             }
@@ -447,7 +484,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                 if (item < items && j < mg) {
                     int t, row;
                     float w;
-                    tile_token(a, kind, first + j, t, w, row);
+                    tile_token<LOCAL>(a, lr, kind, first + j, t, w, row);
                     src[k4] = (n < Mp ? xh : xl) + (size_t)t * d + c * 8;
                 }
             }
@@ -504,17 +541,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
 
 }  // namespace
 
-size_t ffn_tc_smem_bytes(int units) {
+size_t ffn_tc_smem_bytes(int units, const FfnArgs* local) {
     return 1024 + (size_t)kTcStages * kAStage + (size_t)kTcBPairs * kBPair + kHTile + sizeof(TcSmem) +
-           (size_t)units * sizeof(int4);
+           (size_t)units * sizeof(int4) +
+           (local ? local_route_bytes(local->T, local->n, local->k, local->g, kTcWarps) : 0);
+}
+
+bool ffn_tc_local_route_fits(const FfnArgs& a) {
+    int units = 0;
+    for (int c = 0; c < a.ncls; ++c) units += class_capacity(a.cls[c], a.n, a.g);
+    const int m = a.g > 1 ? a.n / a.g : 0;
+    // one thread per unit: the experts, then the departments from the next
+    // warp on; the top-k's lane-held candidates: n <= 256
+    return a.n <= 256 && ((a.n + 31) / 32) * 32 + m <= kTcThreads &&
+           ffn_tc_smem_bytes(units, &a) <= 227 * 1024;
 }
 
 cudaError_t launch_ffn_tc(const TcArgs& a, cudaStream_t s) {
     int units = 0;
     for (int c = 0; c < a.f.ncls; ++c) units += class_capacity(a.f.cls[c], a.f.n, a.f.g);
-    const size_t smem = ffn_tc_smem_bytes(units);
-    cudaError_t e = cudaFuncSetAttribute(ffn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    const size_t smem = ffn_tc_smem_bytes(units, a.f.local_route ? &a.f : nullptr);
+    auto kern = a.f.local_route ? ffn_tc_kernel<true> : ffn_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)device_sm_count();
     TcArgs args = a;
@@ -529,7 +577,7 @@ cudaError_t launch_ffn_tc(const TcArgs& a, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, ffn_tc_kernel, args);
+    return cudaLaunchKernelEx(&cfg, kern, args);
 }
 
 }  // namespace moe

@@ -165,7 +165,9 @@ cudaError_t launch_ffn(const FfnArgs& a, cudaStream_t s);
 // of the local path (a.local_route) at its usual CTAs per SM.
 bool ffn_local_route_fits(const FfnArgs& a);
 cudaError_t launch_ffn_tc(const TcArgs& a, cudaStream_t s);
-size_t ffn_tc_smem_bytes(int units);
+size_t ffn_tc_smem_bytes(int units, const FfnArgs* local);
+// Whether the tensor-core kernel can route inside its CTAs (a.local_route).
+bool ffn_tc_local_route_fits(const FfnArgs& a);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
 cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t s);
 cudaError_t launch_split_x(const float* x, long long elems, __nv_bfloat16* xb, cudaStream_t s);

@@ -90,8 +90,10 @@ def test_zipf_large_batch_tc(B, threshold, T):
 
 
 def expected_auto_choice(shape, T, exp_count, dept_count, sms):
-    """Host restatement of the per-call kernel choice: 0 no choice (the step is
-    not eligible for the tensor-core kernel), 1 CUDA cores, 2 tensor cores."""
+    """Host restatement of the whole-layer kernel choice: 0 the CUDA-core
+    kernel alone (the step is not eligible for the tensor-core kernel, or not
+    expected to gain from it), 1 CUDA cores and 2 tensor cores as chosen on the
+    device (rows wider than 4096), 2 the tensor-core kernel alone."""
     classes = []
     if shape.I_sh > 0:
         classes.append((shape.I_sh, dept_count))
@@ -120,6 +122,10 @@ def expected_auto_choice(shape, T, exp_count, dept_count, sms):
         expect.append(T)
     if max(expect) < 8 and not wide:
         return 0
+    if not wide and T <= 32:
+        # launched for rows up to 4096 wide and up to 32 tokens: the
+        # tensor-core kernel alone, with the routing inside its CTAs
+        return 2
     rows_cc = sum(r * sum(-(-int(c) // 4) for c in cnt) for r, cnt in classes)
     tiles = sum(r // 128 * sum(-(-int(c) // 32) for c in cnt) for r, cnt in classes)
     tc_rows = -(-tiles // sms) * 128
