@@ -223,14 +223,14 @@ double expected_unit_tokens(const moe::FfnArgs& a, int T) {
 
 bool prepare_tc(const moe::FfnArgs& a, int T, moe::TcArgs* t) {
     const int thr = tc_min_tokens();
-    // Automatic mode launches the tensor-core kernel (which then decides on
-    // the device) for wide rows always, and otherwise only when some class
-    // expects at least two CUDA-core token groups per unit.  Below that the
-    // CUDA-core stream, with the routing inside its CTAs, measured faster
-    // (DeaMoE-7B layer at T = 8: 50 vs 55 µs), and an idle tensor-core launch
-    // also forces the routing kernel to build the dispatch itself.
+    // Automatic mode launches the tensor-core kernel for wide rows always
+    // (both kernels run and choose on the device), and otherwise only when
+    // some class expects more than one CUDA-core group of tokens per unit:
+    // then the CUDA-core stream would read those rows once per group, and the
+    // tensor-core kernel runs alone with the routing inside its CTAs
+    // (DeaMoE-7B layer at T = 8: 43.5 vs 50.1 µs on the CUDA cores).
     if (thr == 0 && a.d <= moe::kTcWideHidden &&
-        (T <= moe::kGroupTokens || expected_unit_tokens(a, T) < 2 * moe::kGroupTokens))
+        (T <= moe::kGroupTokens || expected_unit_tokens(a, T) <= moe::kGroupTokens))
         return false;
     const int mt = thr > 0 ? thr : 1;
     int units = 0;

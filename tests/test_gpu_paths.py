@@ -108,8 +108,8 @@ def expected_auto_choice(shape, T, exp_count, dept_count, sms):
     wide = shape.d > 4096
     if T <= 4 and not wide:
         return 0
-    # launched only when some class expects at least two CUDA-core groups
-    # (8 tokens) per unit
+    # launched only when some class expects more than one CUDA-core group
+    # (4 tokens) per unit
     expect = []
     if shape.I_sh > 0:
         miss = 1.0
@@ -120,7 +120,7 @@ def expected_auto_choice(shape, T, exp_count, dept_count, sms):
         expect.append(T * shape.k / shape.n)
     if shape.I_s > 0:
         expect.append(T)
-    if max(expect) < 8 and not wide:
+    if max(expect) <= 4 and not wide:
         return 0
     if not wide and T <= 32:
         # launched for rows up to 4096 wide and up to 32 tokens: the
