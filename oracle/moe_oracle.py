@@ -39,6 +39,10 @@ Readings where the pages are silent (each also listed in the design doc):
   residual ``u_t`` of the [DSMoE] formula.
 * R5 form P (eq. 4) uses sigma = SiLU at all three interfaces ([DeaMoE] §3.4).
 * R6 expert e belongs to department floor(e / g).
+* R7 group-limited top-k: a department's score is its best expert key.
+* R8 strict coverage: the replaced expert is the lowest-ranked one whose
+  department keeps another selected expert (otherwise the coverage would not
+  grow), and the uncovered departments are among the k_dept kept ones.
 """
 
 from __future__ import annotations
@@ -122,6 +126,70 @@ def route(x, w_router, k: int, bias=None, scale: float = 1.0):
             gap_adjacent[t] = min(ks[i] - ks[i + 1] for i in range(k - 1))
     info = {"logits": l64, "key32": key32, "key64": key64,
             "gap_boundary": gap_boundary, "gap_adjacent": gap_adjacent}
+    return idx, p, info
+
+
+def route_grouped(x, w_router, k: int, g: int, k_dept: int, bias=None, scale: float = 1.0,
+                  strict: bool = False):
+    """Group-limited top-k of [DeaMoE] §3.3 ("we use group top-k routing to cap
+    the activated FLOPs per token associated with department matrices"), with
+    the strict-coverage variant of its appendix ablation.
+
+    Per token, with the fp32 keys of ``route`` (R1):
+
+    1. department j's score is its best expert key, ``max_{e in j} key[e]``
+       (R7: the pages do not define the score);
+    2. the k_dept departments with the best scores are kept (score descending,
+       equal scores -> lower department first);
+    3. the top-k of the experts of the kept departments, as in ``route``;
+    4. strict only (R8): while the selection covers fewer than k_dept
+       departments, the best expert (largest key, lower index on ties) of the
+       best-scored uncovered kept department replaces the lowest-ranked
+       selected expert among those whose department holds another selected
+       expert; the selection is then re-ordered by key;
+    5. weights: ``scale * softmax`` over the selected unbiased logits (R2).
+
+    Returns ``(idx [T,k] int32, p [T,k] float64, info)`` like ``route``; info
+    adds the kept departments ``kept [T,k_dept]`` and the fp64 department
+    scores ``dscore64``.
+    """
+    l64 = router_logits(x, w_router)
+    T, n = l64.shape
+    if g < 1 or n % g:
+        raise ValueError("need g >= 1 dividing n")
+    m = n // g
+    if not 1 <= k_dept <= m or not 1 <= k <= k_dept * g:
+        raise ValueError("need 1 <= k_dept <= n/g and 1 <= k <= k_dept * g")
+    if strict and k < k_dept:
+        raise ValueError("strict coverage needs k >= k_dept")
+    b32 = np.zeros(n, np.float32) if bias is None else to_f64(bias).astype(np.float32)
+    key32 = (l64.astype(np.float32) + b32[None, :]).astype(np.float32)
+    key64 = l64 + b32.astype(np.float64)[None, :]
+    idx = np.empty((T, k), np.int32)
+    p = np.empty((T, k), np.float64)
+    kept_all = np.empty((T, k_dept), np.int32)
+    dscore64 = np.empty((T, m))
+    for t in range(T):
+        rank = lambda e: (-float(key32[t, e]), e)                      # noqa: E731
+        score = [max(float(key32[t, e]) for e in range(j * g, (j + 1) * g)) for j in range(m)]
+        dscore64[t] = [max(key64[t, e] for e in range(j * g, (j + 1) * g)) for j in range(m)]
+        kept = sorted(range(m), key=lambda j: (-score[j], j))[:k_dept]
+        kept_all[t] = kept
+        cand = [e for j in kept for e in range(j * g, (j + 1) * g)]
+        sel = sorted(cand, key=rank)[:k]
+        if strict:
+            while len({e // g for e in sel}) < k_dept:
+                covered = {e // g for e in sel}
+                j_new = min((j for j in kept if j not in covered), key=lambda j: (-score[j], j))
+                e_new = min(range(j_new * g, (j_new + 1) * g), key=rank)
+                shared = [e for e in sel if sum(1 for f in sel if f // g == e // g) > 1]
+                e_out = max(shared, key=rank)                           # lowest ranked
+                sel = sorted([e for e in sel if e != e_out] + [e_new], key=rank)
+        idx[t] = sel
+        ls = l64[t, sel]
+        ex = np.exp(ls - ls.max())
+        p[t] = scale * ex / ex.sum()
+    info = {"logits": l64, "key32": key32, "key64": key64, "kept": kept_all, "dscore64": dscore64}
     return idx, p, info
 
 

@@ -171,6 +171,150 @@ def test_k_equals_n_routes_everything():
 
 
 # ---------------------------------------------------------------------------
+# Group-limited top-k ([DeaMoE] §3.3 k_dept; strict coverage of its Table 4)
+# ---------------------------------------------------------------------------
+
+
+def _rand_router(rng, T, d, n, ties=False):
+    x = rng.standard_normal((T, d))
+    wr = rng.standard_normal((n, d)) * 0.3
+    if ties:
+        wr[n // 2] = wr[0]
+        wr[n - 1] = wr[1]
+    return x, wr
+
+
+def test_grouped_all_departments_is_plain_topk():
+    # k_dept = m keeps every department: plain top-k, weights included
+    rng = np.random.default_rng(11)
+    for trial in range(60):
+        g = int(rng.choice([1, 2, 4]))
+        n = g * int(rng.integers(2, 6))
+        k = int(rng.integers(1, n + 1))
+        x, wr = _rand_router(rng, 3, 8, n, ties=trial % 3 == 0)
+        bias = rng.standard_normal(n) * 0.1 if trial % 2 else None
+        i0, p0, _ = O.route(x, wr, k, bias=bias, scale=1.5)
+        i1, p1, _ = O.route_grouped(x, wr, k, g, n // g, bias=bias, scale=1.5)
+        np.testing.assert_array_equal(i1, i0)
+        np.testing.assert_array_equal(p1, p0)
+
+
+def test_grouped_single_expert_departments_is_plain_topk():
+    # g = 1: the k_dept >= k best departments are the k_dept best experts
+    rng = np.random.default_rng(12)
+    for trial in range(40):
+        n = int(rng.integers(4, 12))
+        k = int(rng.integers(1, n + 1))
+        k_dept = int(rng.integers(k, n + 1))
+        x, wr = _rand_router(rng, 2, 8, n, ties=trial % 2 == 0)
+        for strict in (False, True):
+            i0, p0, _ = O.route(x, wr, k)
+            # strict needs k >= k_dept, and k <= k_dept * g = k_dept
+            i1, p1, _ = O.route_grouped(x, wr, k, 1, k if strict else k_dept, strict=strict)
+            np.testing.assert_array_equal(i1, i0)
+            np.testing.assert_array_equal(p1, p0)
+
+
+def _keys32(x, wr, bias):
+    b = np.zeros(wr.shape[0], np.float32) if bias is None else np.asarray(bias, np.float32)
+    return (np.asarray(x, np.float64) @ np.asarray(wr, np.float64).T).astype(np.float32) + b
+
+
+@pytest.mark.parametrize("strict", [False, True])
+def test_grouped_matches_bruteforce(strict):
+    # Distinct keys (continuous random inputs).  Kept departments: the k_dept-
+    # subset with the largest summed department score (score = best key).
+    # Soft: the k-subset of the kept departments' experts with the largest key
+    # sum.  Strict: the same, over the k-subsets that cover every kept
+    # department.  Order: descending key.
+    rng = np.random.default_rng(13 + strict)
+    for trial in range(80):
+        g = int(rng.choice([2, 3]))
+        m = int(rng.integers(2, 5))
+        n = g * m
+        k_dept = int(rng.integers(1, m + 1))
+        k = int(rng.integers(k_dept if strict else 1, k_dept * g + 1))
+        x, wr = _rand_router(rng, 2, 6, n)
+        bias = rng.standard_normal(n) * 0.2 if trial % 2 else None
+        idx, p, _ = O.route_grouped(x, wr, k, g, k_dept, bias=bias, strict=strict)
+        key = _keys32(x, wr, bias)
+        for t in range(2):
+            score = [key[t, j * g:(j + 1) * g].max() for j in range(m)]
+            kept = max(itertools.combinations(range(m), k_dept), key=lambda c: sum(score[j] for j in c))
+            pool = [e for e in range(n) if e // g in kept]
+            subsets = [c for c in itertools.combinations(pool, k)
+                       if not strict or {e // g for e in c} == set(kept)]
+            best = max(subsets, key=lambda c: sum(float(key[t, e]) for e in c))
+            assert sorted(idx[t]) == sorted(best)
+            assert all(key[t, a] > key[t, b] for a, b in zip(idx[t], idx[t][1:]))
+            l = np.asarray(x[t], np.float64) @ np.asarray(wr, np.float64).T
+            ex = np.exp(l[idx[t]])
+            np.testing.assert_allclose(p[t], ex / ex.sum(), rtol=1e-13)
+
+
+def test_grouped_hand_example():
+    # Logits of one token over 8 experts in 4 departments of 2 (x = e_0, so the
+    # router's first column gives the logits).
+    #   logits  [5, 1 | 4.9, 0 | 4.8, 4.7 | 0, 0]
+    #   department scores 5, 4.9, 4.8, 0 -> k_dept = 2 keeps departments 0, 1
+    #   plain top-3: 0, 2, 4; group-limited top-3 (soft): 0, 2, 1
+    l = np.array([5.0, 1.0, 4.9, 0.0, 4.8, 4.7, 0.0, 0.0])
+    wr = np.zeros((8, 4))
+    wr[:, 0] = l
+    x = np.array([[1.0, 0.0, 0.0, 0.0]])
+    assert list(O.route(x, wr, 3)[0][0]) == [0, 2, 4]
+    idx, p, info = O.route_grouped(x, wr, 3, 2, 2)
+    assert list(idx[0]) == [0, 2, 1]
+    assert list(info["kept"][0]) == [0, 1]
+    ex = np.exp(np.array([5.0, 4.9, 1.0]))
+    np.testing.assert_allclose(p[0], ex / ex.sum(), rtol=1e-14)
+    # Strict, k = 3, k_dept = 3: departments 0, 1, 2 kept.  Soft picks 0, 2, 4
+    # (3 departments): already covered, strict leaves it.
+    assert list(O.route_grouped(x, wr, 3, 2, 3, strict=True)[0][0]) == [0, 2, 4]
+    # logits [5, 4.9 | 4.8, 4.7 | 1, 0 | 0.5, 0.2], k = 3, k_dept = 3: kept 0, 1, 2;
+    # soft picks 0, 1, 2 (departments 0, 1); strict swaps the lowest-ranked
+    # expert of a doubly covered department (1) for department 2's leader (4).
+    wr[:, 0] = [5.0, 4.9, 4.8, 4.7, 1.0, 0.0, 0.5, 0.2]
+    assert list(O.route_grouped(x, wr, 3, 2, 3)[0][0]) == [0, 1, 2]
+    idx, p, _ = O.route_grouped(x, wr, 3, 2, 3, strict=True)
+    assert list(idx[0]) == [0, 2, 4]
+    ex = np.exp(np.array([5.0, 4.8, 1.0]))
+    np.testing.assert_allclose(p[0], ex / ex.sum(), rtol=1e-14)
+
+
+def test_grouped_coverage_invariants():
+    rng = np.random.default_rng(14)
+    for trial in range(60):
+        g = int(rng.choice([2, 4, 8]))
+        m = int(rng.integers(2, 9))
+        n = g * m
+        k_dept = int(rng.integers(1, m + 1))
+        k = int(rng.integers(k_dept, min(k_dept * g, 16) + 1))
+        x, wr = _rand_router(rng, 4, 8, n, ties=trial % 4 == 0)
+        bias = rng.standard_normal(n) * 0.1 if trial % 2 else None
+        soft, ps, info = O.route_grouped(x, wr, k, g, k_dept, bias=bias, scale=2.0)
+        strict, pt, _ = O.route_grouped(x, wr, k, g, k_dept, bias=bias, scale=2.0, strict=True)
+        for t in range(4):
+            kept = set(info["kept"][t])
+            assert len(set(soft[t])) == k and len(set(strict[t])) == k
+            assert {e // g for e in soft[t]} <= kept
+            assert {e // g for e in strict[t]} == kept
+            if len({e // g for e in soft[t]}) == k_dept:
+                np.testing.assert_array_equal(strict[t], soft[t])
+            assert ps[t].sum() == pytest.approx(2.0, abs=1e-13)
+            assert pt[t].sum() == pytest.approx(2.0, abs=1e-13)
+
+
+def test_grouped_rejects_bad_arguments():
+    x, wr = np.ones((1, 4)), np.ones((8, 4))
+    for args in [(3, 3, 1), (3, 2, 0), (3, 2, 5), (5, 2, 2), (9, 8, 1)]:
+        with pytest.raises(ValueError):
+            O.route_grouped(x, wr, *args)
+    with pytest.raises(ValueError):
+        O.route_grouped(x, wr, 1, 2, 2, strict=True)
+
+
+# ---------------------------------------------------------------------------
 # Dense brute force vs the gathered per-token evaluation
 # ---------------------------------------------------------------------------
 
