@@ -21,6 +21,10 @@ Sources (cited by title and section):
   section "Mathematical Formulation of the DeepSeekMoE Forward Pass" (shared
   expert with weight 1; routing bias used for selection only; softmax over
   the selected affinities).
+* [DSMoE-ALF] the same guide, section "Algorithmic Mechanics: Auxiliary-Loss-Free
+  Dynamic Load Balancing" (step 4 of its routing loop: the sign update of the
+  router bias; its part 2: the proportional update; its part 3: the imbalance
+  ratio).
 * [MoE-inf] "MoE inference engineering, clearly explained", sections "How a
   batch becomes expert-specific matrices" (dispatch / combine) and "Local MoE
   execution pipeline" (permutation with an inverse map).
@@ -43,6 +47,10 @@ Readings where the pages are silent (each also listed in the design doc):
 * R8 strict coverage: the replaced expert is the lowest-ranked one whose
   department keeps another selected expert (otherwise the coverage would not
   grow), and the uncovered departments are among the k_dept kept ones.
+* R9 bias update: the target load of an expert is the batch's mean load,
+  (sum of the expert token counts) / n; the bias is fp32 state, updated once
+  per call from fp64 arithmetic rounded to fp32 once.  With no routed token
+  the imbalance ratio (0 / 0) is reported as 0 and no bias moves.
 """
 
 from __future__ import annotations
@@ -191,6 +199,57 @@ def route_grouped(x, w_router, k: int, g: int, k_dept: int, bias=None, scale: fl
         p[t] = scale * ex / ex.sum()
     info = {"logits": l64, "key32": key32, "key64": key64, "kept": kept_all, "dscore64": dscore64}
     return idx, p, info
+
+
+# ---------------------------------------------------------------------------
+# Router-bias load balancing: [DSMoE-ALF]
+# ---------------------------------------------------------------------------
+
+BIAS_SIGN = 0           # b_i -/+ gamma when expert i is over / under its target
+BIAS_PROPORTIONAL = 1   # b_i + gamma * (target - tokens_i)
+
+
+def bias_update(counts, bias, gamma: float, rule: int = BIAS_SIGN) -> np.ndarray:
+    """One gradient-free update of the selection-only router bias from the
+    tokens each expert received ([DSMoE-ALF] step 4 and part 2).
+
+    ``counts[i]`` is the number of tokens routed to expert i in the batch,
+    ``bias`` the fp32 bias before the update.  The target is the mean load
+    sum(counts) / n (R9).  Sign rule: an expert above its target loses gamma,
+    one below it gains gamma, one exactly on it keeps its bias.  Proportional
+    rule: ``b_i + gamma * (target - counts_i)``.  Returns the new fp32 bias.
+    """
+    c = [int(v) for v in np.asarray(counts).reshape(-1)]
+    b = np.asarray(bias, np.float32).reshape(-1)
+    n = len(c)
+    if b.shape[0] != n:
+        raise ValueError("counts and bias differ in length")
+    total = sum(c)
+    out = np.empty(n, np.float32)
+    for i in range(n):
+        bi = float(b[i])
+        if rule == BIAS_SIGN:
+            # compare counts_i with total / n exactly: counts_i * n vs total
+            if c[i] * n > total:
+                bi = bi - float(gamma)
+            elif c[i] * n < total:
+                bi = bi + float(gamma)
+        elif rule == BIAS_PROPORTIONAL:
+            bi = bi + float(gamma) * (total / n - c[i])
+        else:
+            raise ValueError("unknown rule")
+        out[i] = np.float32(bi)
+    return out
+
+
+def imbalance_ratio(counts) -> float:
+    """[DSMoE-ALF] part 3: max_j tokens_j / ((1/n) sum_j tokens_j); 0 when no
+    token was routed (R9)."""
+    c = [int(v) for v in np.asarray(counts).reshape(-1)]
+    total = sum(c)
+    if total == 0:
+        return 0.0
+    return max(c) / (total / len(c))
 
 
 # ---------------------------------------------------------------------------

@@ -315,6 +315,90 @@ def test_grouped_rejects_bad_arguments():
 
 
 # ---------------------------------------------------------------------------
+# Router-bias load balancing (DeepSeekMoE guide, auxiliary-loss-free section)
+# ---------------------------------------------------------------------------
+
+
+def test_bias_sign_rule_hand_example():
+    # 8 tokens over 4 experts: target 2; expert 0 is over (-gamma), expert 1
+    # under (+gamma), experts 2 and 3 on target (unchanged); dyadic values so
+    # that every result is exact
+    b = O.bias_update([3, 1, 2, 2], np.array([0.5, -0.25, 0.0, 1.0], np.float32), 0.125)
+    np.testing.assert_array_equal(b, np.array([0.375, -0.125, 0.0, 1.0], np.float32))
+    # a target that is not an integer: 1 token over 3 experts (target 1/3)
+    b = O.bias_update([1, 0, 0], np.zeros(3, np.float32), 0.5)
+    np.testing.assert_array_equal(b, np.array([-0.5, 0.5, 0.5], np.float32))
+
+
+def test_bias_proportional_rule_hand_example():
+    b = O.bias_update([4, 0, 2, 2], np.zeros(4, np.float32), 0.125, rule=O.BIAS_PROPORTIONAL)
+    np.testing.assert_array_equal(b, np.array([-0.25, 0.25, 0.0, 0.0], np.float32))
+    # target 1/3: deltas gamma * (1/3 - 1), gamma / 3, gamma / 3 with gamma = 0.75
+    b = O.bias_update([1, 0, 0], np.zeros(3, np.float32), 0.75, rule=O.BIAS_PROPORTIONAL)
+    np.testing.assert_allclose(b, [-0.5, 0.25, 0.25], rtol=2 ** -23)
+
+
+def test_bias_update_invariants():
+    rng = np.random.default_rng(21)
+    for trial in range(50):
+        n = int(rng.integers(1, 300))
+        c = rng.integers(0, 40, n)
+        b = (rng.standard_normal(n) * 0.1).astype(np.float32)
+        gamma = float(rng.uniform(1e-4, 1e-2))
+        # proportional: the deltas sum to zero, so the bias sum is kept
+        bp = O.bias_update(c, b, gamma, rule=O.BIAS_PROPORTIONAL)
+        assert abs(float(bp.astype(np.float64).sum() - b.astype(np.float64).sum())) \
+            <= n * 2 ** -23 * (np.abs(b).max() + gamma * c.max() + 1)
+        # sign: every bias moves by exactly 0 or +-gamma (before fp32 rounding)
+        bs = O.bias_update(c, b, gamma)
+        mean = c.sum() / n
+        for i in range(n):
+            bi = float(b[i])
+            want = bi - gamma if c[i] > mean else bi + gamma if c[i] < mean else bi
+            assert bs[i] == np.float32(want)
+    # balanced load: nothing moves under either rule, the ratio is 1
+    for rule in (O.BIAS_SIGN, O.BIAS_PROPORTIONAL):
+        b = np.arange(8, dtype=np.float32)
+        np.testing.assert_array_equal(O.bias_update([5] * 8, b, 0.1, rule=rule), b)
+        np.testing.assert_array_equal(O.bias_update([0] * 8, b, 0.1, rule=rule), b)
+    assert O.imbalance_ratio([5] * 8) == 1.0
+
+
+def test_imbalance_ratio_closed_forms():
+    assert O.imbalance_ratio([3, 1, 2, 2]) == 1.5
+    assert O.imbalance_ratio([0, 0, 7, 0, 0]) == 5.0        # one expert takes all: n
+    assert O.imbalance_ratio([0, 0, 0]) == 0.0               # nothing routed
+    rng = np.random.default_rng(22)
+    for _ in range(20):
+        c = rng.integers(0, 50, int(rng.integers(1, 64)))
+        if c.sum():
+            r = O.imbalance_ratio(c)
+            assert 1.0 <= r <= len(c)
+
+
+def test_sign_rule_reduces_imbalance():
+    # The guide's claim: the per-step sign update balances the load.  A router
+    # skewed towards the low expert ids (a logit offset from 1.5 down to -1.5)
+    # starts near 2.3x the mean load on its busiest expert; after 150 steps of
+    # 256 tokens the ratio is near the sampling noise of a balanced router.
+    rng = np.random.default_rng(0)
+    n, k, T, d = 16, 2, 256, 16
+    wr = np.concatenate([rng.standard_normal((n, d)) * 0.5, np.linspace(1.5, -1.5, n)[:, None]], 1)
+    b = np.zeros(n, np.float32)
+    hist = []
+    for step in range(150):
+        x = np.concatenate([rng.standard_normal((T, d)), np.ones((T, 1))], 1)
+        idx, _, _ = O.route(x, wr, k, bias=b)
+        c = np.bincount(idx.reshape(-1), minlength=n)
+        hist.append(O.imbalance_ratio(c))
+        b = O.bias_update(c, b, 0.02)
+    assert hist[0] > 2.0
+    assert np.mean(hist[-20:]) < 1.5
+    # the bias ends up lowest where the skew was strongest
+    assert b[0] < b[-1]
+
+
+# ---------------------------------------------------------------------------
 # Dense brute force vs the gathered per-token evaluation
 # ---------------------------------------------------------------------------
 
