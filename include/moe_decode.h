@@ -177,6 +177,33 @@ int moe_route_topk(const float* x, const float* w_router, const float* bias,
                    void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Group-limited top-k: [DeaMoE] §3.3 caps the departments a token activates
+ * at k_dept; the strict variant (its appendix ablation, Table 4) makes the
+ * selection cover exactly k_dept departments.  Expert e belongs to department
+ * e / experts_per_dept.  Per token:
+ *   1. a department's score is the best key (logit + bias) of its experts;
+ *      the k_dept best-scored departments are kept (equal scores -> lower
+ *      department first);
+ *   2. soft (strict == 0): the top-k of the kept departments' experts, by key
+ *      as in moe_route_topk;
+ *      strict (strict != 0): each kept department's best expert, plus the best
+ *      k - k_dept other experts of the kept departments (the end point of
+ *      replacing the lowest-ranked expert whose department holds another
+ *      selected expert by the best expert of an uncovered kept department);
+ *   3. topk_idx by descending key (equal keys -> lower index), topk_w =
+ *      scale * softmax over the selected unbiased logits.
+ * Other arguments, the workspace and the device status as moe_route_topk.
+ * Limits: those of moe_route_topk; experts_per_dept divides n;
+ * 1 <= k_dept <= n / experts_per_dept; k <= k_dept * experts_per_dept;
+ * strict needs k >= k_dept.  Violations return MOE_ERR_INVALID_ARG and
+ * launch nothing.
+ */
+int moe_route_topk_grouped(const float* x, const float* w_router, const float* bias,
+                           int T, int d, int n, int k, int experts_per_dept, int k_dept,
+                           int strict, float scale, int32_t* topk_idx, float* topk_w,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/*
  * moe_route_topk without a workspace and without allocating.  The paper has no
  * counterpart: this is a library convenience.
  *
@@ -323,6 +350,34 @@ int deamoe_layer_forward(const float* x, int T, int d, int n, int k, float scale
                          int I_s, const void* s_gate, const void* s_up, const void* s_down,
                          void* ws, size_t ws_bytes, int32_t* topk_idx, float* topk_w,
                          float* y, void* stream);
+
+/* ------------------------------------------------------------------------- */
+/* Router-bias load balancing                                                */
+/* ------------------------------------------------------------------------- */
+
+#define MOE_BIAS_SIGN         0  /* b_i - gamma over the target, + gamma under it */
+#define MOE_BIAS_PROPORTIONAL 1  /* b_i + gamma * (target - counts_i)             */
+
+/*
+ * One gradient-free update of the selection-only router bias from a batch's
+ * expert loads: [DSMoE] "Algorithmic Mechanics: Auxiliary-Loss-Free Dynamic
+ * Load Balancing", step 4 of its routing loop (sign rule) and its part 2
+ * (proportional rule), with the imbalance ratio of its part 3.
+ *   counts    int32[n] device: tokens routed to each expert in the batch (the
+ *             workspace's exp_count after a dispatch or a layer forward)
+ *   n         1 <= n <= 1024
+ *   gamma     step size, finite and >= 0
+ *   rule      MOE_BIAS_SIGN or MOE_BIAS_PROPORTIONAL
+ *   bias      float[n] device, updated in place; NULL to only measure
+ *   imbalance float[1] device or NULL: max_i counts_i / mean_i counts_i
+ *             (0 when no token was routed)
+ * The target load is the mean, sum(counts) / n; an expert exactly on it keeps
+ * its bias under the sign rule.  The arithmetic is fp64 (IEEE, one rounding
+ * to fp32 at the end), so results are the same on every run.  One kernel of
+ * one block, stream-ordered; bias and imbalance may not both be NULL.
+ */
+int moe_bias_update(const int32_t* counts, int n, float gamma, int rule,
+                    float* bias, float* imbalance, void* stream);
 
 /* ------------------------------------------------------------------------- */
 /* Byte accounting (host only)                                               */

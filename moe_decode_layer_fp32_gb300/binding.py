@@ -54,6 +54,8 @@ _SIGS = {
     "moe_read_status": (_I, [_P, _SZ, C.POINTER(C.c_int32), C.POINTER(C.c_int32), _P]),
     "moe_route_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _SZ, _P]),
     "moe_route_topk_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
+    "moe_bias_update": (_I, [_P, _I, _F, _I, _P, _P, _P]),
+    "moe_route_topk_grouped": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _SZ, _P]),
     "moe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _P, _SZ, _P]),
     "moe_rows_count": (_I64, [_I, _I, _I, _I, _I]),
     "moe_ffn_vanilla": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P,
@@ -177,6 +179,32 @@ def moe_route_topk_noalloc(x, w_router, bias, k: int, scale: float, topk_idx, to
     _check("moe_route_topk_noalloc", lib().moe_route_topk_noalloc(
         _ptr(x), _ptr(w_router), _ptr(bias), T, d, n, k, scale, _ptr(topk_idx), _ptr(topk_w),
         _ptr(status), _stream()))
+
+
+def moe_route_topk_grouped(x, w_router, bias, k: int, experts_per_dept: int, k_dept: int, strict: bool,
+                           scale: float, topk_idx, topk_w, ws):
+    T, d = x.shape
+    n = w_router.shape[0]
+    _check("moe_route_topk_grouped", lib().moe_route_topk_grouped(
+        _ptr(x), _ptr(w_router), _ptr(bias), T, d, n, k, experts_per_dept, k_dept, int(bool(strict)), scale,
+        _ptr(topk_idx), _ptr(topk_w), _ptr(ws), ws.numel(), _stream()))
+
+
+MOE_BIAS_SIGN = 0
+MOE_BIAS_PROPORTIONAL = 1
+
+
+def moe_bias_update(counts, gamma: float, rule: int, bias=None, imbalance=None):
+    """``counts``: int32 CUDA tensor [n]; ``bias`` float32 [n] (updated in
+    place) and/or ``imbalance`` float32 [1]."""
+    _check("moe_bias_update", lib().moe_bias_update(
+        _ptr(counts), counts.numel(), gamma, rule, _ptr(bias), _ptr(imbalance), _stream()))
+
+
+def workspace_counts(ws, T: int, n: int, k: int, experts_per_dept: int):
+    """The workspace's per-expert token counts (int32 [n]) as a view of ws."""
+    off = moe_workspace_layout(T, n, k, experts_per_dept)["exp_count"]
+    return ws[off: off + 4 * n].view(torch.int32)
 
 
 def moe_dispatch(topk_idx, topk_w, n: int, experts_per_dept: int, ws):

@@ -422,6 +422,63 @@ int moe_route_topk(const float* x, const float* w_router, const float* bias, int
     return MOE_OK;
 }
 
+int moe_route_topk_grouped(const float* x, const float* w_router, const float* bias, int T, int d, int n,
+                           int k, int experts_per_dept, int k_dept, int strict, float scale,
+                           int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, void* stream) {
+    const char* who = "moe_route_topk_grouped";
+    if (experts_per_dept < 1 || n < 1 || n % experts_per_dept)
+        return fail(MOE_ERR_INVALID_ARG, "%s: experts_per_dept=%d must divide n=%d", who, experts_per_dept, n);
+    const int m = n / experts_per_dept;
+    if (k_dept < 1 || k_dept > m)
+        return fail(MOE_ERR_INVALID_ARG, "%s: k_dept=%d outside [1, %d]", who, k_dept, m);
+    if ((long long)k > (long long)k_dept * experts_per_dept)
+        return fail(MOE_ERR_INVALID_ARG, "%s: k=%d exceeds the %d experts of k_dept=%d departments", who, k,
+                    k_dept * experts_per_dept, k_dept);
+    if (strict && k < k_dept)
+        return fail(MOE_ERR_INVALID_ARG, "%s: strict coverage needs k >= k_dept (k=%d, k_dept=%d)", who, k,
+                    k_dept);
+    moe_ws_layout L;
+    int rc = check_ws(ws, ws_bytes, T, n, k, 1, &L, who);
+    if (rc) return rc;
+    if ((rc = check_hidden(x, d, who))) return rc;
+    if (d > kMaxRouterHidden)
+        return fail(MOE_ERR_UNSUPPORTED, "%s: d=%d exceeds the router kernel's %d", who, d, kMaxRouterHidden);
+    if (!w_router || !aligned16(w_router)) return fail(MOE_ERR_INVALID_ARG, "%s: w_router null or unaligned", who);
+    if (!topk_idx || !topk_w) return fail(MOE_ERR_INVALID_ARG, "%s: outputs are null", who);
+    moe::RouteArgs a = {};
+    a.x = x;
+    a.w_router = w_router;
+    a.bias = bias;
+    a.T = T; a.d = d; a.n = n; a.k = k;
+    a.scale = scale;
+    a.topk_idx = topk_idx;
+    a.topk_w = topk_w;
+    a.ws = resolve(ws, L);
+    a.fuse_dispatch = 0;
+    a.g = 1;
+    a.route_g = experts_per_dept;
+    a.k_dept = k_dept;
+    a.strict = strict ? 1 : 0;
+    cudaError_t e = moe::launch_route(a, as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    return MOE_OK;
+}
+
+int moe_bias_update(const int32_t* counts, int n, float gamma, int rule, float* bias, float* imbalance,
+                    void* stream) {
+    const char* who = "moe_bias_update";
+    if (n < 1 || n > moe::kMaxN) return fail(MOE_ERR_INVALID_ARG, "%s: n=%d outside [1, %d]", who, n, moe::kMaxN);
+    if (!counts) return fail(MOE_ERR_INVALID_ARG, "%s: counts is null", who);
+    if (!bias && !imbalance) return fail(MOE_ERR_INVALID_ARG, "%s: bias and imbalance are both null", who);
+    if (rule != MOE_BIAS_SIGN && rule != MOE_BIAS_PROPORTIONAL)
+        return fail(MOE_ERR_INVALID_ARG, "%s: unknown rule %d", who, rule);
+    if (!(gamma >= 0.0f) || gamma == INFINITY)
+        return fail(MOE_ERR_INVALID_ARG, "%s: gamma must be finite and >= 0", who);
+    cudaError_t e = moe::launch_bias_update(counts, n, gamma, rule, bias, imbalance, as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    return MOE_OK;
+}
+
 int moe_route_topk_noalloc(const float* x, const float* w_router, const float* bias, int T, int d,
                            int n, int k, float scale, int32_t* topk_idx, float* topk_w,
                            int32_t* status, void* stream) {

@@ -321,6 +321,123 @@ __device__ __forceinline__ bool topk_select_warp(const float* logits_row, const 
     return bad;
 }
 
+// Group-limited top-k of "DeaMoE: Efficient MoE Structure for Fast Small-Batch
+// Decoding" §3.3 (at most k_dept departments per token), with the strict
+// department-coverage variant of its appendix ablation (Table 4).  Expert e
+// belongs to department e / g; a department's score is its best key.
+//
+// Round r of the department stage takes the best key among the experts of the
+// departments not kept yet (ties -> lower expert index, hence lower
+// department): that expert leads its department, which is kept.  The soft
+// selection is then the top-k over the kept departments' experts.  The strict
+// selection is every kept department's leader plus the best k - k_dept other
+// experts of the kept departments; this is what replacing, one at a time, the
+// lowest-ranked expert whose department keeps another selected expert by the
+// leader of the best uncovered kept department ends with, because such an
+// expert is never a leader and a new leader is never replaced.  Either way the
+// selected experts come out by descending key.  Same lane layout and result as
+// topk_select_warp (k <= k_dept * g; strict needs k >= k_dept).
+template <int J>
+__device__ __forceinline__ bool topk_select_warp_grouped(const float* logits_row, const float* bias, int n,
+                                                         int k, int g, int k_dept, bool strict, float scale,
+                                                         int& out_idx, float& out_w) {
+    const int lane = threadIdx.x & 31;
+    constexpr uint32_t kLowest = 0x007fffffu;   // ordered_key(-inf)
+    uint32_t key[J];
+    float lg[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const int e = lane + 32 * j;
+        lg[j] = 0.0f;
+        key[j] = 0u;
+        if (e < n) {
+            const float l = __ldcg(logits_row + e);
+            const float kv = bias ? l + __ldg(bias + e) : l;
+            lg[j] = l;
+            key[j] = (kv == kv && kv != -INFINITY) ? ordered_key(kv) : kLowest;
+        }
+    }
+    // Warp-wide best (key, then lowest index) among the entries whose bit is
+    // set in the lane's mask; -1 when there is none.
+    auto best = [&](uint32_t mask, uint32_t& top) -> int {
+        uint32_t bk = 0u;
+        int bj = 0;
+#pragma unroll
+        for (int j = 0; j < J; ++j)
+            if (((mask >> j) & 1u) && key[j] > bk) {
+                bk = key[j];
+                bj = j;
+            }
+        top = __reduce_max_sync(0xffffffffu, bk);
+        const uint32_t cand = (bk == top && top != 0u) ? (uint32_t)(lane + 32 * bj) : 0xffffffffu;
+        const uint32_t bi = __reduce_min_sync(0xffffffffu, cand);
+        return bi == 0xffffffffu ? -1 : (int)bi;
+    };
+    uint32_t all = 0u;
+#pragma unroll
+    for (int j = 0; j < J; ++j)
+        if (lane + 32 * j < n) all |= 1u << j;
+    uint32_t kept = 0u, lead = 0u;
+    bool bad = false;
+    for (int r = 0; r < k_dept; ++r) {
+        uint32_t top;
+        const int e = best(all & ~kept, top);
+        if (e < 0) {
+            bad = true;
+            break;
+        }
+        const int dep = e / g;
+#pragma unroll
+        for (int j = 0; j < J; ++j)
+            if ((all >> j & 1u) && (lane + 32 * j) / g == dep) kept |= 1u << j;
+        if (lane == (e & 31)) lead |= 1u << (e >> 5);
+    }
+    // the experts to output: soft, the whole kept pool (top-k taken below);
+    // strict, the leaders plus the best k - k_dept non-leaders
+    uint32_t pool = kept;
+    if (strict) {
+        pool = lead;
+        for (int r = k_dept; r < k; ++r) {
+            uint32_t top;
+            const int e = best(kept & ~pool, top);
+            if (e < 0) {
+                bad = true;
+                break;
+            }
+            if (lane == (e & 31)) pool |= 1u << (e >> 5);
+        }
+    }
+    int my_idx = 0;
+    float my_lg = 0.0f;
+    for (int r = 0; r < k; ++r) {
+        uint32_t top;
+        const int e = best(pool, top);
+        if (e < 0 || top <= kLowest) bad = true;
+        const int ee = e < 0 ? 0 : e;
+        const int owner = ee & 31, jb = ee >> 5;
+        float v = 0.0f;
+#pragma unroll
+        for (int j = 0; j < J; ++j)
+            if (j == jb) v = lg[j];
+        if (lane == owner && e >= 0) pool &= ~(1u << jb);
+        v = __shfl_sync(0xffffffffu, v, owner);
+        if (lane == r) {
+            my_idx = ee;
+            my_lg = v;
+        }
+    }
+    float mx = lane < k ? my_lg : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float ex = lane < k ? expf(my_lg - mx) : 0.0f;
+    float s = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    out_idx = my_idx;
+    out_w = lane < k ? scale * (ex / s) : 0.0f;
+    return bad;
+}
+
 // Exclusive prefix sum of data[0..len) in place; returns the total.  All NT
 // threads of the block must call it.
 template <int NT>

@@ -31,6 +31,9 @@ struct RouteArgs {
     // Whole-layer path with routing in the FFN kernel: write the logits only
     // (no top-k, no dispatch); the FFN CTAs take it from there.
     int logits_only;
+    // Group-limited top-k: k_dept > 0 keeps at most k_dept departments of
+    // route_g experts per token (strict != 0: exactly k_dept); 0 = plain top-k.
+    int route_g, k_dept, strict;
 };
 
 struct DispatchArgs {
@@ -160,6 +163,9 @@ struct CombineArgs {
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s);
+// Router-bias update and imbalance ratio over n <= 1024 expert counts.
+cudaError_t launch_bias_update(const int32_t* counts, int n, float gamma, int rule, float* bias,
+                               float* imbalance, cudaStream_t s);
 cudaError_t launch_ffn(const FfnArgs& a, cudaStream_t s);
 // Whether the CUDA-core kernel's shared memory still holds the routing state
 // of the local path (a.local_route) at its usual CTAs per SM.

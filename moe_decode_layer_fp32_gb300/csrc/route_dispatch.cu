@@ -168,14 +168,18 @@ __device__ void dispatch_block(const int32_t* idx, const float* wts, int T, int 
 
 // Top-k of one token by one warp, written to the routing outputs (and to
 // the shared-memory copy the fused dispatch reads, when given).
-template <int J>
+// GROUPED: the selection is group-limited (k_dept departments of g experts
+// at most; strict: exactly k_dept).
+template <int J, bool GROUPED>
 __device__ void topk_warp(const float* logits_row, const float* bias, int n, int k, float scale,
-                          int32_t* idx_out, float* w_out, int32_t* status, int32_t* idx_sm,
-                          float* w_sm) {
+                          int g, int k_dept, bool strict, int32_t* idx_out, float* w_out,
+                          int32_t* status, int32_t* idx_sm, float* w_sm) {
     const int lane = threadIdx.x & 31;
     int e;
     float wv;
-    const bool bad = topk_select_warp<J>(logits_row, bias, n, k, scale, e, wv);
+    const bool bad = GROUPED
+                         ? topk_select_warp_grouped<J>(logits_row, bias, n, k, g, k_dept, strict, scale, e, wv)
+                         : topk_select_warp<J>(logits_row, bias, n, k, scale, e, wv);
     if (lane < k) {
         idx_out[lane] = e;
         w_out[lane] = wv;
@@ -188,29 +192,30 @@ __device__ void topk_warp(const float* logits_row, const float* bias, int n, int
 }
 
 // Top-k of tokens [t0, t1), one warp per token.
-template <int J>
+template <int J, bool GROUPED>
 __device__ __forceinline__ void topk_rows(const RouteArgs& a, int warp, int t0, int t1, int32_t* idx_sm,
                                           float* w_sm) {
     for (int t = t0 + warp; t < t1; t += kRouteWarps)
-        topk_warp<J>(a.ws.logits + (size_t)t * a.n, a.bias, a.n, a.k, a.scale,
-                     a.topk_idx + (size_t)t * a.k, a.topk_w + (size_t)t * a.k, a.ws.status,
+        topk_warp<J, GROUPED>(a.ws.logits + (size_t)t * a.n, a.bias, a.n, a.k, a.scale, a.route_g, a.k_dept,
+                     a.strict != 0, a.topk_idx + (size_t)t * a.k, a.topk_w + (size_t)t * a.k, a.ws.status,
                      idx_sm ? idx_sm + t * a.k : nullptr, idx_sm ? w_sm + t * a.k : nullptr);
 }
 
-template <int J>
+template <int J, bool GROUPED>
 __device__ __forceinline__ void topk_range(const RouteArgs& a, int warp, int t0, int t1, int32_t* idx_sm,
                                            float* w_sm) {
-    topk_rows<J>(a, warp, t0, t1, idx_sm, w_sm);
+    topk_rows<J, GROUPED>(a, warp, t0, t1, idx_sm, w_sm);
 }
+template <bool GROUPED>
 __device__ __forceinline__ void topk_any(const RouteArgs& a, int warp, int t0, int t1, int32_t* idx_sm,
                                          float* w_sm) {
     const int J = (a.n + 31) / 32;
-    if (J <= 1) topk_range<1>(a, warp, t0, t1, idx_sm, w_sm);
-    else if (J <= 2) topk_range<2>(a, warp, t0, t1, idx_sm, w_sm);
-    else if (J <= 4) topk_range<4>(a, warp, t0, t1, idx_sm, w_sm);
-    else if (J <= 8) topk_range<8>(a, warp, t0, t1, idx_sm, w_sm);
-    else if (J <= 16) topk_range<16>(a, warp, t0, t1, idx_sm, w_sm);
-    else topk_range<32>(a, warp, t0, t1, idx_sm, w_sm);
+    if (J <= 1) topk_range<1, GROUPED>(a, warp, t0, t1, idx_sm, w_sm);
+    else if (J <= 2) topk_range<2, GROUPED>(a, warp, t0, t1, idx_sm, w_sm);
+    else if (J <= 4) topk_range<4, GROUPED>(a, warp, t0, t1, idx_sm, w_sm);
+    else if (J <= 8) topk_range<8, GROUPED>(a, warp, t0, t1, idx_sm, w_sm);
+    else if (J <= 16) topk_range<16, GROUPED>(a, warp, t0, t1, idx_sm, w_sm);
+    else topk_range<32, GROUPED>(a, warp, t0, t1, idx_sm, w_sm);
 }
 
 // Router logits: block (expert group, token block) computes the logits of EB
@@ -224,7 +229,7 @@ __device__ __forceinline__ void topk_any(const RouteArgs& a, int warp, int t0, i
 // block's warps take in one round) the top-k is split: the last block of
 // each token block to finish (a per-token-block counter) picks that block's
 // tokens, and the last token block to finish builds the dispatch.
-template <int RCH, int EB>
+template <int RCH, int EB, bool GROUPED>
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
     __shared__ DispatchSmem sm;
     __shared__ int32_t s_idx[kStagedAssignments];   // top-k results for the fused dispatch
@@ -340,7 +345,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
     // the fused dispatch reads the top-k results from shared memory when one
     // block picked them all and they fit
     const bool staged = a.fuse_dispatch && !split && a.T * a.k <= kStagedAssignments;
-    topk_any(a, warp, split ? t0 : 0, split ? min(t0 + 8, a.T) : a.T, staged ? s_idx : nullptr, s_w);
+    topk_any<GROUPED>(a, warp, split ? t0 : 0, split ? min(t0 + 8, a.T) : a.T, staged ? s_idx : nullptr, s_w);
     if (tid == 0) a.ws.sync[ctr] = 0u;  // ready for the next call
     if (!a.fuse_dispatch) return;
     // With a split top-k the last token block to finish builds the dispatch;
@@ -361,11 +366,13 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
 
 }  // namespace
 
-template <int EB>
+// The group-limited selection is its own instantiation, which leaves the
+// plain kernel's registers as they are.
+template <int EB, bool GROUPED>
 void launch_route_eb(const RouteArgs& a, int rch, int blocks, cudaStream_t s) {
-    if (rch <= 1) route_kernel<1, EB><<<blocks, kRouteThreads, 0, s>>>(a);
-    else if (rch <= 2) route_kernel<2, EB><<<blocks, kRouteThreads, 0, s>>>(a);
-    else route_kernel<4, EB><<<blocks, kRouteThreads, 0, s>>>(a);
+    if (rch <= 1) route_kernel<1, EB, GROUPED><<<blocks, kRouteThreads, 0, s>>>(a);
+    else if (rch <= 2) route_kernel<2, EB, GROUPED><<<blocks, kRouteThreads, 0, s>>>(a);
+    else route_kernel<4, EB, GROUPED><<<blocks, kRouteThreads, 0, s>>>(a);
 }
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
@@ -375,8 +382,14 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
     // from four token blocks on, 4 experts per block so that each activation
     // chunk serves 4; below, one expert per block for parallelism
     const int eb = a.n % 4 == 0 && tblocks >= 4 ? 4 : 1;
-    if (eb == 4) launch_route_eb<4>(a, rch, a.n / 4 * tblocks, s);
-    else launch_route_eb<1>(a, rch, a.n * tblocks, s);
+    const bool grouped = a.k_dept > 0 && !a.logits_only;
+    if (eb == 4) {
+        if (grouped) launch_route_eb<4, true>(a, rch, a.n / 4 * tblocks, s);
+        else launch_route_eb<4, false>(a, rch, a.n / 4 * tblocks, s);
+    } else {
+        if (grouped) launch_route_eb<1, true>(a, rch, a.n * tblocks, s);
+        else launch_route_eb<1, false>(a, rch, a.n * tblocks, s);
+    }
     return cudaGetLastError();
 }
 

@@ -58,6 +58,39 @@ def compare_routing(g_idx, g_w, o_idx, o_p, info, x, w_router, w_rtol=1e-5):
     return ties
 
 
+def compare_grouped_routing(g_idx, g_w, o_idx, o_p, info, x, w_router, g, k_dept, strict,
+                            w_rtol=1e-5):
+    """Group-limited routing: indices bit-exact, except tokens where the
+    oracle shows a near-tie (a department-score gap at the k_dept boundary or
+    a key gap inside the kept departments within twice the fp32 summation
+    error) and the device's selection is still a valid one: k distinct
+    experts, at most (strict: exactly) k_dept departments, keys descending
+    within the error.  Returns those token ids."""
+    g_idx = np.asarray(g_idx)
+    g_w = np.asarray(g_w, np.float64)
+    eps = near_tie_bound(x, w_router)
+    key, dscore = info["key64"], info["dscore64"]
+    k = g_idx.shape[1]
+    ties = []
+    for t in range(g_idx.shape[0]):
+        if np.array_equal(g_idx[t], o_idx[t]):
+            np.testing.assert_allclose(g_w[t], o_p[t], rtol=w_rtol, atol=1e-7,
+                                       err_msg=f"routing weights of token {t}")
+            continue
+        ds = np.sort(dscore[t])[::-1]
+        near = k_dept < len(ds) and ds[k_dept - 1] - ds[k_dept] <= 2 * eps[t]
+        pool = np.sort([key[t, e] for e in range(key.shape[1]) if e // g in set(info["kept"][t])])
+        near = near or (np.diff(pool).min() if len(pool) > 1 else np.inf) <= 2 * eps[t]
+        sel = [int(e) for e in g_idx[t]]
+        deps = {e // g for e in sel}
+        valid = (len(set(sel)) == k and (len(deps) == k_dept if strict else len(deps) <= k_dept)
+                 and all(key[t, a] >= key[t, b] - 2 * eps[t] for a, b in zip(sel, sel[1:])))
+        assert near and valid, (f"token {t}: device {sel} vs oracle {o_idx[t].tolist()} "
+                                f"(near-tie {near}, valid {valid})")
+        ties.append(t)
+    return ties
+
+
 def dispatch_lists(binding, ws, T, n, k, g):
     """Read every dispatch list out of a device workspace (host numpy)."""
     L = binding.moe_workspace_layout(T, n, k, g)

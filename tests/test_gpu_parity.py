@@ -112,6 +112,164 @@ def test_route_k_equals_n_and_bias(B):
 
 
 # ---------------------------------------------------------------------------
+# Group-limited top-k ([DeaMoE] §3.3 k_dept; strict coverage of its Table 4)
+# ---------------------------------------------------------------------------
+
+
+def grouped_on_gpu(B, x, wr, bias, k, g, k_dept, strict, scale=1.0):
+    T = x.shape[0]
+    n = wr.shape[0]
+    ws = B.new_workspace(T, n, k, 1)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    B.moe_route_topk_grouped(x, wr, bias, k, g, k_dept, strict, scale, idx, w, ws)
+    torch.cuda.synchronize()
+    st, _, _ = B.moe_read_status(ws)
+    assert st == 0
+    return idx.cpu().numpy(), w.cpu().numpy()
+
+
+# (d, n, g, k, k_dept): the DeaMoE-7B router with 2, 4 and all 8 departments,
+# the 256-expert router in 16 departments, one expert per department, and the
+# widest router (1024 experts) in 8 departments of 128
+GROUPED_CASES = [(2048, 64, 8, 8, 2), (2048, 64, 8, 8, 4), (2048, 64, 8, 8, 8), (7168, 256, 16, 8, 4),
+                 (512, 32, 1, 6, 6), (256, 1024, 128, 32, 3), (256, 48, 3, 5, 4)]
+
+
+@pytest.mark.parametrize("case", GROUPED_CASES, ids=lambda c: "d%d-n%d-g%d-k%d-kd%d" % c)
+@pytest.mark.parametrize("strict", [False, True], ids=["soft", "strict"])
+def test_route_grouped_matches_oracle(B, case, strict):
+    d, n, g, k, k_dept = case
+    ties = 0
+    for T in (1, 5, 33, 128):
+        for seed in (0, 1):
+            wr = synth.router(d, n, seed, DEV)
+            bias = synth.zipf_bias(n, g, 1.1, seed).to(DEV) if seed else None
+            x = synth.hidden(T, d, seed + 100 * T, DEV)
+            gi, gw = grouped_on_gpu(B, x, wr, bias, k, g, k_dept, strict, scale=1.25)
+            oi, op, info = O.route_grouped(x, wr, k, g, k_dept, bias=bias, scale=1.25, strict=strict)
+            ties += len(H.compare_grouped_routing(gi, gw, oi, op, info, x, wr, g, k_dept, strict))
+    assert ties <= 1
+
+
+@pytest.mark.parametrize("strict", [False, True], ids=["soft", "strict"])
+def test_route_grouped_exact_ties(B, strict):
+    # equal logits; a bias that is constant within departments and repeats
+    # across them: every decision is a tie broken by index
+    T, d, n, g = 4, 16, 64, 8
+    x = torch.ones((T, d), device=DEV)
+    wr = torch.zeros((n, d), device=DEV)
+    for bias in (None, torch.tensor([float((e // g) % 3) for e in range(n)], device=DEV)):
+        for k, k_dept in ((8, 2), (5, 5), (16, 3)):
+            gi, gw = grouped_on_gpu(B, x, wr, bias, k, g, k_dept, strict)
+            oi, op, _ = O.route_grouped(x, wr, k, g, k_dept, bias=bias, strict=strict)
+            np.testing.assert_array_equal(gi, oi)
+            np.testing.assert_allclose(gw, op, rtol=1e-6)
+
+
+def test_route_grouped_hand_example(B):
+    # the oracle pin's example: logits [5, 1 | 4.9, 0 | 4.8, 4.7 | 0, 0] and
+    # [5, 4.9 | 4.8, 4.7 | 1, 0 | 0.5, 0.2] (x = e_0, d padded to 8)
+    x = torch.zeros((2, 8), device=DEV)
+    x[:, 0] = 1.0
+    wr = torch.zeros((8, 8), device=DEV)
+    wr[:, 0] = torch.tensor([5.0, 1.0, 4.9, 0.0, 4.8, 4.7, 0.0, 0.0])
+    assert grouped_on_gpu(B, x, wr, None, 3, 2, 2, False)[0][0].tolist() == [0, 2, 1]
+    wr[:, 0] = torch.tensor([5.0, 4.9, 4.8, 4.7, 1.0, 0.0, 0.5, 0.2])
+    assert grouped_on_gpu(B, x, wr, None, 3, 2, 3, False)[0][0].tolist() == [0, 1, 2]
+    gi, gw = grouped_on_gpu(B, x, wr, None, 3, 2, 3, True)
+    assert gi[0].tolist() == [0, 2, 4]
+    ex = np.exp(np.array([5.0, 4.8, 1.0]))
+    np.testing.assert_allclose(gw[0], ex / ex.sum(), rtol=1e-6)
+
+
+def test_route_grouped_rejects_bad_arguments(B):
+    x = torch.zeros((2, 8), device=DEV)
+    wr = torch.zeros((8, 8), device=DEV)
+    ws = B.new_workspace(2, 8, 4, 1)
+    idx = torch.empty((2, 4), dtype=torch.int32, device=DEV)
+    w = torch.empty((2, 4), dtype=torch.float32, device=DEV)
+    for g, k_dept, strict in ((3, 1, False), (2, 0, False), (2, 5, False), (2, 1, False), (1, 3, True)):
+        with pytest.raises(RuntimeError):
+            B.moe_route_topk_grouped(x, wr, None, 4, g, k_dept, strict, 1.0, idx, w, ws)
+
+
+# ---------------------------------------------------------------------------
+# Router-bias update and imbalance ratio (DeepSeekMoE guide, auxiliary-loss-
+# free section): fp64 arithmetic on both sides, so the fp32 results agree
+# bit for bit
+# ---------------------------------------------------------------------------
+
+
+def bias_update_on_gpu(B, counts, bias, gamma, rule):
+    c = torch.tensor(np.asarray(counts, np.int32), device=DEV)
+    b = torch.tensor(np.asarray(bias, np.float32), device=DEV)
+    r = torch.full((1,), -1.0, device=DEV)
+    B.moe_bias_update(c, gamma, rule, b, r)
+    torch.cuda.synchronize()
+    return b.cpu().numpy(), float(r.item())
+
+
+@pytest.mark.parametrize("n", [1, 7, 64, 256, 1000, 1024])
+@pytest.mark.parametrize("rule", [0, 1], ids=["sign", "proportional"])
+def test_bias_update_matches_oracle(B, n, rule):
+    rng = np.random.default_rng(n + 17 * rule)
+    for trial in range(4):
+        if trial == 0:
+            counts = np.zeros(n, np.int32)                       # nothing routed
+        elif trial == 1:
+            counts = np.full(n, 3, np.int32)                     # on target everywhere
+        else:
+            counts = rng.zipf(1.3, n).clip(max=5000).astype(np.int32)
+        bias = (rng.standard_normal(n) * 0.05).astype(np.float32)
+        gamma = float(np.float32(rng.uniform(1e-4, 1e-2)))
+        gb, gr = bias_update_on_gpu(B, counts, bias, gamma, rule)
+        np.testing.assert_array_equal(gb, O.bias_update(counts, bias, gamma, rule=rule))
+        assert gr == float(np.float32(O.imbalance_ratio(counts)))
+
+
+def test_bias_update_hand_example(B):
+    gb, gr = bias_update_on_gpu(B, [3, 1, 2, 2], [0.5, -0.25, 0.0, 1.0], 0.125, 0)
+    np.testing.assert_array_equal(gb, np.array([0.375, -0.125, 0.0, 1.0], np.float32))
+    assert gr == 1.5
+
+
+def test_bias_update_after_layer_forward(B):
+    # the layer leaves its expert loads in the workspace; the update reads them
+    # there (no host round trip) and matches the oracle's routing of the step
+    shape = synth.DEAMOE_7B
+    L = synth.make_layer(shape, 4, DEV)
+    L["bias"] = (torch.randn(shape.n, generator=torch.Generator().manual_seed(4)) * 0.01).to(DEV)
+    for T in (1, 16, 64):
+        x = synth.hidden(T, shape.d, 40 + T, DEV)
+        ws, gi, gw, _ = H.run_layer_forward(B, shape, L, x)
+        counts = B.workspace_counts(ws, T, shape.n, shape.k, shape.g)
+        b = L["bias"].clone()
+        r = torch.empty(1, device=DEV)
+        B.moe_bias_update(counts, 1e-3, 0, b, r)
+        torch.cuda.synchronize()
+        oi, op, info = O.route(x, L["router"], shape.k, bias=L["bias"])
+        assert not H.compare_routing(gi.cpu().numpy(), gw.cpu().numpy(), oi, op, info, x, L["router"])
+        oc = np.bincount(oi.reshape(-1), minlength=shape.n)
+        np.testing.assert_array_equal(counts.cpu().numpy(), oc)
+        np.testing.assert_array_equal(b.cpu().numpy(),
+                                      O.bias_update(oc, L["bias"].cpu().numpy(), float(np.float32(1e-3))))
+        assert r.item() == float(np.float32(O.imbalance_ratio(oc)))
+
+
+def test_bias_update_rejects_bad_arguments(B):
+    c = torch.zeros(8, dtype=torch.int32, device=DEV)
+    b = torch.zeros(8, device=DEV)
+    for gamma, rule, bias, imb in ((0.1, 2, b, None), (-1.0, 0, b, None), (float("inf"), 0, b, None),
+                                   (float("nan"), 1, b, None), (0.1, 0, None, None)):
+        with pytest.raises(RuntimeError):
+            B.moe_bias_update(c, gamma, rule, bias, imb)
+    with pytest.raises(RuntimeError):
+        B.moe_bias_update(torch.zeros(1025, dtype=torch.int32, device=DEV), 0.1, 0, None,
+                          torch.zeros(1, device=DEV))
+
+
+# ---------------------------------------------------------------------------
 # Dispatch (fed the oracle's routing: bit-exact lists)
 # ---------------------------------------------------------------------------
 
