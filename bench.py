@@ -201,6 +201,14 @@ class Workload:
                 self.idx[key] = torch.empty((T, s.k), dtype=torch.int32, device=device)
                 self.w[key] = torch.empty((T, s.k), dtype=torch.float32, device=device)
                 self.y[key] = torch.empty((T, s.d), dtype=torch.float32, device=device)
+        # group-limited routing: the departments, or n/8 groups of a vanilla
+        # layer; half of them kept per token
+        self.rg = s.g if s.I_sh > 0 and s.g > 1 else max(1, s.n // 8)
+        self.k_dept = max(1, (s.n // self.rg) // 2)
+        self.gidx = {T: torch.empty((T, s.k), dtype=torch.int32, device=device) for T in batches}
+        self.gw = {T: torch.empty((T, s.k), dtype=torch.float32, device=device) for T in batches}
+        self.bias_copy = [torch.zeros(s.n, device=device) for _ in range(replicas)]
+        self.imbalance = {key: torch.zeros(1, device=device) for key in self.x}
         self.unique = {}
         self.ffn_bytes = {}
         self.counts = {}
@@ -226,6 +234,20 @@ class Workload:
         L, key = self.layers[r], (r, T)
         self.B.moe_route_topk(self.x[key], L["router"], L["bias"], self.shape.k, 1.0,
                               self.idx[key], self.w[key], self.ws[key])
+
+    def grouped_only(self, r, T, strict: bool):
+        """Group-limited routing of the same inputs (k_dept of the departments,
+        or of n/8 expert groups on a vanilla layer) into scratch outputs."""
+        L, key = self.layers[r], (r, T)
+        self.B.moe_route_topk_grouped(self.x[key], L["router"], L["bias"], self.shape.k, self.rg,
+                                      self.k_dept, strict, 1.0, self.gidx[T], self.gw[T], self.ws[key])
+
+    def bias_only(self, r, T):
+        """Router-bias update (sign rule) and imbalance ratio from the loads the
+        layer pass left in the workspace, on a copy of the bias."""
+        key = (r, T)
+        counts = self.B.workspace_counts(self.ws[key], T, self.shape.n, self.shape.k, self.g)
+        self.B.moe_bias_update(counts, 1e-3, self.B.MOE_BIAS_SIGN, self.bias_copy[r], self.imbalance[key])
 
     def dispatch_only(self, r, T):
         key = (r, T)
@@ -344,7 +366,10 @@ def run_ours(args, rank, world, local):
         scratch_T = {r: torch.zeros_like(W.y[(r, T)]) for r in range(R)}
         for name, fn in (("route_topk", lambda T=T: [W.route_only(r, T) for r in range(R)]),
                          ("dispatch", lambda T=T: [W.dispatch_only(r, T) for r in range(R)]),
-                         ("ffn", lambda T=T: [W.ffn_only(r, T, scratch_T[r]) for r in range(R)])):
+                         ("ffn", lambda T=T: [W.ffn_only(r, T, scratch_T[r]) for r in range(R)]),
+                         ("route_topk_grouped", lambda T=T: [W.grouped_only(r, T, False) for r in range(R)]),
+                         ("route_topk_grouped_strict", lambda T=T: [W.grouped_only(r, T, True) for r in range(R)]),
+                         ("bias_update", lambda T=T: [W.bias_only(r, T) for r in range(R)])):
             gs = capture(fn)
             time_graphs([gs], [0] * 3, world, device)
             stage_us[name] = round(time_graphs([gs], [0] * reps, world, device) / (reps * R) * 1e6, 2)
@@ -353,6 +378,8 @@ def run_ours(args, rank, world, local):
                          else "split") for r in range(R)})
         per_batch[str(T)] = {"us_per_layer": round(us, 2), "unique_MB": round(U / 1e6, 2),
                              "GBps": round(U / us / 1e3, 1), "stage_us": stage_us,
+                             "grouped_routing": f"{W.k_dept} of {shape.n // W.rg} groups of {W.rg}",
+                             "imbalance": round(sum(W.imbalance[(r, T)].item() for r in range(R)) / R, 3),
                              "ffn_path": "/".join(paths),
                              "active_experts": round(sum(W.counts[(r, T)][0] for r in range(R)) / R, 2)}
         if shape.I_sh > 0:

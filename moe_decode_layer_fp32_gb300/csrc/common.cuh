@@ -386,10 +386,11 @@ __device__ __forceinline__ bool topk_select_warp_grouped(const float* logits_row
             bad = true;
             break;
         }
-        const int dep = e / g;
+        const int first = e - e % g;   // the department's first expert (warp-uniform)
 #pragma unroll
         for (int j = 0; j < J; ++j)
-            if ((all >> j & 1u) && (lane + 32 * j) / g == dep) kept |= 1u << j;
+            if ((uint32_t)(lane + 32 * j - first) < (uint32_t)g) kept |= 1u << j;
+        kept &= all;
         if (lane == (e & 31)) lead |= 1u << (e >> 5);
     }
     // the experts to output: soft, the whole kept pool (top-k taken below);
