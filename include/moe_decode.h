@@ -88,16 +88,23 @@ int moe_set_tc_min_tokens(int min_tokens);
 /* ------------------------------------------------------------------------- */
 
 /*
- * Byte offsets of the workspace arrays for a (T, n, k, experts_per_dept) step.
+ * Byte offsets of the workspace arrays for a (T, n, k, experts_per_dept) step,
+ * in the order they are laid out.
  * The dispatch lists follow [MoE-inf] "How a batch becomes expert-specific
  * matrices" (group the T*k assignments by expert, keep each token id and an
  * inverse map for the combine) and the department token sets X^j of [DeaMoE]
  * §3.2.  Canonical order everywhere: ascending expert (department) id, then
  * ascending token id.
  *
- *   status    int32[4]   [0] first device error code (0 = none)
- *   counts    int32[4]   [0] active experts A_e, [1] active departments A_d,
- *                        [2], [3] their totals of ceil(tokens / 32)
+ *   status    int32[4]   offset 0: [0] first device error code (0 = none)
+ *   counts    int32[4]   offset 256: [0] active experts A_e, [1] active
+ *                        departments A_d, [2], [3] their totals of
+ *                        ceil(tokens / 32)
+ *   sync      uint32[18] offset 512: [0], [2..17] internal counters (kept at
+ *                        zero between calls); [1] FFN kernel choice of the
+ *                        last FFN step: 0 none made (fixed threshold, or the
+ *                        step is not eligible for the tensor-core kernel),
+ *                        1 CUDA cores, 2 tensor cores
  *   logits    float[T*n] router logits (scratch of moe_route_topk)
  *   exp_count int32[n]   assignments per expert
  *   exp_off   int32[n+1] exclusive prefix sum of exp_count
@@ -106,24 +113,24 @@ int moe_set_tc_min_tokens(int min_tokens);
  *   asg_w     float[T*k] routing weight of each assignment
  *   tok_asg   int32[T*k] inverse map: (token, slot) -> assignment position
  *   act_exp   int32[n]   active experts, ascending (first A_e valid)
+ *   exp_units int32[n][4] per active expert q < A_e: {expert, first assignment,
+ *                        assignments, inclusive prefix over active experts of
+ *                        ceil(assignments / 4)} -- the FFN's work table
+ *   xb        bf16[2][T][8192] activations split as x = hi + lo (scratch of the
+ *                        tensor-core FFN; rows packed at the call's d)
  *   dept_count int32[m]  tokens per department (m = n / experts_per_dept)
  *   dept_off  int32[m+1] exclusive prefix sum of dept_count
  *   dept_tok  int32[T*min(k,m)] tokens of each department (X^j), each once
  *   dept_w    float[T*min(k,m)] sum of the token's routing weights inside X^j
  *   tok_dpos  int32[T*m] (token, department) -> position in dept_tok, or -1
  *   act_dept  int32[m]   active departments, ascending (first A_d valid)
- *   exp_units int32[n][4] per active expert q < A_e: {expert, first assignment,
- *                        assignments, inclusive prefix over active experts of
- *                        ceil(assignments / 4)} -- the FFN's work table
- *   dept_units int32[m][4] the same per active department over X^j
- *   sync      uint32[4]  [0] internal counter (kept at zero between calls);
- *                        [1] FFN kernel choice of the last FFN step: 0 none
- *                        made (fixed threshold, or the step is not eligible
- *                        for the tensor-core kernel), 1 CUDA cores, 2 tensor
- *                        cores
- *   xb        bf16[2][T][8192] activations split as x = hi + lo (scratch of the
- *                        tensor-core FFN; rows packed at the call's d)
- * The department arrays are present only when experts_per_dept > 1.
+ *   dept_units int32[m][4] the same as exp_units per active department over X^j
+ * The department arrays are present only when experts_per_dept > 1.  status,
+ * counts and sync do not move with the sizes, and the offsets of the arrays
+ * before the department arrays depend on T, n and k only.  So a workspace
+ * sized for (T_max, n, k, g) serves every call with T <= T_max, and a call
+ * that takes no experts_per_dept (routing) may use a department workspace.
+ * A step's calls (route, dispatch, FFN, combine) use the same T.
  */
 typedef struct moe_ws_layout {
     size_t total;

@@ -52,8 +52,14 @@ bool layout_of(int T, int n, int k, int g, moe_ws_layout* L) {
         off = align_up(off + bytes, 256);
         return o;
     };
-    L->status = take(4 * sizeof(int32_t));
-    L->counts = take(4 * sizeof(int32_t));
+    // The words that persist between calls (status, counts, the counters) sit
+    // at fixed offsets, whatever the step's sizes, so that one workspace serves
+    // steps of any T up to the one it was sized for, and a routing call (laid
+    // out for g = 1) on a department workspace finds the same counters.  The
+    // arrays every layout has come next; the department arrays come last.
+    L->status = take(4 * sizeof(int32_t));                 // offset 0
+    L->counts = take(4 * sizeof(int32_t));                 // offset 256
+    L->sync = take(kSyncWords * sizeof(uint32_t));         // offset 512
     L->logits = take((size_t)T * n * sizeof(float));
     L->exp_count = take((size_t)n * sizeof(int32_t));
     L->exp_off = take((size_t)(n + 1) * sizeof(int32_t));
@@ -62,16 +68,15 @@ bool layout_of(int T, int n, int k, int g, moe_ws_layout* L) {
     L->asg_w = take((size_t)T * k * sizeof(float));
     L->tok_asg = take((size_t)T * k * sizeof(int32_t));
     L->act_exp = take((size_t)n * sizeof(int32_t));
+    L->exp_units = take((size_t)n * 4 * sizeof(int32_t));
+    L->xb = take((size_t)2 * T * moe::kMaxXbHidden * 2);
     L->dept_count = take((size_t)m * sizeof(int32_t));
     L->dept_off = take((size_t)(m + 1) * sizeof(int32_t));
     L->dept_tok = take((size_t)dk * sizeof(int32_t));
     L->dept_w = take((size_t)dk * sizeof(float));
     L->tok_dpos = take((size_t)T * m * sizeof(int32_t));
     L->act_dept = take((size_t)m * sizeof(int32_t));
-    L->exp_units = take((size_t)n * 4 * sizeof(int32_t));
     L->dept_units = take((size_t)m * 4 * sizeof(int32_t));
-    L->sync = take(kSyncWords * sizeof(uint32_t));
-    L->xb = take((size_t)2 * T * moe::kMaxXbHidden * 2);
     L->total = off;
     return true;
 }

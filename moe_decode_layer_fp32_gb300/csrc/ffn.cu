@@ -210,6 +210,13 @@ __device__ __forceinline__ int group_tokens(const FfnArgs& a, const int4 rec, in
                 w = a.ws.asg_w[p];
                 row = p;
             }
+            // a token id outside [0, T) (a workspace the dispatch did not
+            // write for this step) is reported, never used as an address
+            if ((unsigned)t >= (unsigned)a.T) {
+                set_status(a.ws.status, kDevErrRouting);
+                t = 0;
+                w = 0.0f;
+            }
             tok[i] = t;
             wt[i] = w;
             orow[i] = a.out_mode == MOE_OUT_ACCUM ? t : row;

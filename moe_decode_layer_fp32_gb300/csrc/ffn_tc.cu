@@ -139,6 +139,13 @@ __device__ __forceinline__ void tile_token(const TcArgs& a, const LocalRoute& lr
         w = a.f.ws.asg_w[entry];
         row = entry;
     }
+    // a token id from the workspace outside [0, T) (a workspace the dispatch
+    // did not write for this step) is reported, never used as an address
+    if ((unsigned)t >= (unsigned)a.f.T) {
+        set_status(a.f.ws.status, kDevErrRouting);
+        t = 0;
+        w = 0.0f;
+    }
     if (a.f.out_mode == MOE_OUT_ACCUM) row = t;
 }
 

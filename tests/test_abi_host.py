@@ -48,15 +48,41 @@ def test_version_and_error_string(B):
     assert isinstance(B.lib().moe_last_error(), bytes)
 
 
+# memory order of the workspace arrays (the header lists them in this order)
+WS_ORDER = ("status", "counts", "sync", "logits", "exp_count", "exp_off", "asg_tok", "asg_slot", "asg_w",
+            "tok_asg", "act_exp", "exp_units", "xb", "dept_count", "dept_off", "dept_tok", "dept_w",
+            "tok_dpos", "act_dept", "dept_units")
+WS_SHARED = WS_ORDER[:WS_ORDER.index("dept_count")]
+
+
 def test_workspace_layout_is_ordered_and_aligned(B):
     for (T, n, k, g) in [(1, 16, 2, 1), (4, 16, 2, 4), (16, 128, 8, 1), (128, 64, 8, 8), (64, 256, 8, 16)]:
         L = B.moe_workspace_layout(T, n, k, g)
-        offs = [L[f] for f in B.WS_FIELDS[1:]]
+        offs = [L[f] for f in WS_ORDER]
         assert offs == sorted(offs)
         assert all(o % 256 == 0 for o in offs)
         assert L["total"] == B.moe_workspace_bytes(T, n, k, g)
-        assert L["counts"] == 256  # documented position read by moe_read_status
-        assert L["total"] >= L["sync"] + 16
+        # documented fixed positions (moe_read_status reads status and counts)
+        assert (L["status"], L["counts"], L["sync"]) == (0, 256, 512)
+        assert L["logits"] >= L["sync"] + 18 * 4
+        assert L["total"] >= L["dept_units"]
+
+
+def test_workspace_serves_smaller_steps_and_routing_views(B):
+    """A workspace sized for (T_max, n, k, g) holds every smaller step's layout,
+    and the g = 1 layout a routing call uses has the same offsets as the
+    department workspace for every array it has (the counters above all)."""
+    for (T, n, k, g) in [(128, 64, 8, 8), (64, 256, 8, 16), (32, 16, 2, 4), (128, 1024, 32, 2)]:
+        big = B.moe_workspace_layout(T, n, k, g)
+        for t in (1, 3, 16, T):
+            if t > T:
+                continue
+            small = B.moe_workspace_layout(t, n, k, g)
+            assert small["total"] <= big["total"]
+            view = B.moe_workspace_layout(t, n, k, 1)
+            assert {f: view[f] for f in WS_SHARED} == {f: small[f] for f in WS_SHARED}
+            assert view["total"] <= small["total"]
+            assert (small["status"], small["counts"], small["sync"]) == (0, 256, 512)
 
 
 @pytest.mark.parametrize("args", [(0, 16, 2, 1), (129, 16, 2, 1), (4, 16, 0, 1), (4, 16, 17, 1),

@@ -449,6 +449,60 @@ def test_invariant_zero_private_is_department_ffn(B):
     assert H.rel_err(y.cpu().numpy(), ref) <= H.TOL["f32"]
 
 
+def test_one_workspace_for_routing_calls_and_smaller_steps(B):
+    """A DeaMoE workspace sized for 128 tokens: after a full layer step, the
+    routing calls (plain and group-limited) on it run their top-k (their
+    counters are the layer's, kept at zero) and leave the department lists
+    alone; then layer steps with fewer tokens on the same buffer match the
+    oracle."""
+    shape = synth.ZIPF_DEAMOE
+    L = synth.make_layer(shape, 12, DEV)
+    Tm = 128
+    ws = B.new_workspace(Tm, shape.n, shape.k, shape.g)
+    lay = B.moe_workspace_layout(Tm, shape.n, shape.k, shape.g)
+    x = synth.hidden(Tm, shape.d, 12, DEV)
+    idx = torch.empty((Tm, shape.k), dtype=torch.int32, device=DEV)
+    w = torch.empty((Tm, shape.k), device=DEV)
+    y = torch.empty((Tm, shape.d), device=DEV)
+    priv = (L["pgate"], L["pup"], L["pdown"])
+    dept = (L["dgate"], L["dup"], L["ddown"])
+    B.deamoe_layer_forward(x, shape.k, 1.0, L["router"], L["bias"], shape.g, dept, priv, None, ws, idx, w, y)
+    torch.cuda.synchronize()
+    lo, hi = lay["dept_count"], lay["total"]
+    dept_bytes = ws[lo:hi].clone()
+    for T in (Tm, 16, 1):
+        xt = x[:T].contiguous()
+        for grouped in (False, True):
+            gi = torch.empty((T, shape.k), dtype=torch.int32, device=DEV)
+            gw = torch.empty((T, shape.k), device=DEV)
+            if grouped:
+                B.moe_route_topk_grouped(xt, L["router"], L["bias"], shape.k, shape.g, 4, False, 1.0, gi, gw, ws)
+                oi, op, info = O.route_grouped(xt, L["router"], shape.k, shape.g, 4, bias=L["bias"])
+                torch.cuda.synchronize()
+                assert len(H.compare_grouped_routing(gi.cpu().numpy(), gw.cpu().numpy(), oi, op, info, xt,
+                                                     L["router"], shape.g, 4, False)) <= 1
+            else:
+                B.moe_route_topk(xt, L["router"], L["bias"], shape.k, 1.0, gi, gw, ws)
+                oi, op, info = O.route(xt, L["router"], shape.k, bias=L["bias"])
+                torch.cuda.synchronize()
+                assert len(H.compare_routing(gi.cpu().numpy(), gw.cpu().numpy(), oi, op, info, xt,
+                                             L["router"])) <= 1
+    assert torch.equal(ws[lo:hi], dept_bytes)
+    assert B.moe_read_status(ws)[0] == 0
+    # smaller layer steps on the same buffer
+    for T in (16, 3):
+        xt = x[:T].contiguous()
+        it = torch.empty((T, shape.k), dtype=torch.int32, device=DEV)
+        wt = torch.empty((T, shape.k), device=DEV)
+        yt = torch.empty((T, shape.d), device=DEV)
+        B.deamoe_layer_forward(xt, shape.k, 1.0, L["router"], L["bias"], shape.g, dept, priv, None, ws, it, wt, yt)
+        torch.cuda.synchronize()
+        oi, op, info = O.route(xt, L["router"], shape.k, bias=L["bias"])
+        assert not H.compare_routing(it.cpu().numpy(), wt.cpu().numpy(), oi, op, info, xt, L["router"])
+        ref = H.oracle_layer(shape, L, xt, oi, op)
+        assert H.rel_err(yt.cpu().numpy(), ref) <= H.TOL[shape.dtype]
+
+
 def test_repeated_calls_reuse_workspace(B):
     shape = synth.VANILLA_128E
     L = synth.make_layer(shape, 3, DEV)
