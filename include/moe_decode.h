@@ -359,6 +359,51 @@ int deamoe_layer_forward(const float* x, int T, int d, int n, int k, float scale
                          float* y, void* stream);
 
 /* ------------------------------------------------------------------------- */
+/* DeaMoE layer in the paper's parameterisation ("form P")                   */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * [DeaMoE] §3.1 eq. (4) with sigma = SiLU at all three interfaces (§3.4):
+ * department j holds W_g^j, W_u^j, W_d^j, expert i (of department i / g)
+ * holds A_g^i, A_u^i, A_d^i, and
+ *     g^ = SiLU(A_g SiLU(W_g x)),   u^ = A_u SiLU(W_u x),
+ *     DeaMoE_i(x) = W_d^T SiLU(A_d^T (g^ * u^)),
+ *     y_t = sum over the token's selected experts of p_i DeaMoE_i(x_t)
+ * (eq. (3)), with the routing of moe_route_topk, or of
+ * moe_route_topk_grouped (soft) when k_dept > 0 (the paper's configurations
+ * cap the departments per token, §3.3 and Table 1).
+ *   x, T, d (= h), n, k, scale, w_router, bias, topk_idx, topk_w: as for
+ *            deamoe_layer_forward
+ *   experts_per_dept  g >= 2 dividing n (m = n / g departments)
+ *   k_dept   0 for plain top-k, else 1 <= k_dept <= m with k <= k_dept * g
+ *   r        department / expert width (hffn): a multiple of 16, <= 2048
+ *   dtype    MOE_DTYPE_BF16 only (others: MOE_ERR_UNSUPPORTED)
+ *   dept_gate, dept_up, dept_down  bf16[m][r][d]: the rows of W_g^j, W_u^j
+ *            and of W_d^j in the paper's [hffn, h] shape (applied
+ *            transposed)
+ *   a_gate, a_up, a_down  bf16[n][r][r]: A_g^i, A_u^i and A_d^i, row-major
+ *            (A_d^i is applied transposed)
+ *   ws       moe_formp_workspace_bytes(T, n, k, g, r) bytes: the layout of
+ *            moe_workspace_layout(T, n, k, g) followed by fp32 scratch for
+ *            SiLU(W_g x) and SiLU(W_u x) per department entry and for
+ *            A_d^T Y per assignment
+ *   y        float[T, d] out (overwritten)
+ * d <= 7680; every pointer 16-byte aligned.  Four launches: routing with the
+ * fused dispatch, then three weight passes chained by programmatic dependent
+ * launches (department up-projection, expert A matrices, department
+ * down-projection).  The workspace holds the dispatch lists afterwards.
+ */
+size_t moe_formp_workspace_bytes(int T, int n, int k, int experts_per_dept, int r);
+
+int deamoe_p_layer_forward(const float* x, int T, int d, int n, int k, float scale,
+                           const float* w_router, const float* bias,
+                           int experts_per_dept, int k_dept, int r, int dtype,
+                           const void* dept_gate, const void* dept_up, const void* dept_down,
+                           const void* a_gate, const void* a_up, const void* a_down,
+                           void* ws, size_t ws_bytes, int32_t* topk_idx, float* topk_w,
+                           float* y, void* stream);
+
+/* ------------------------------------------------------------------------- */
 /* Router-bias load balancing                                                */
 /* ------------------------------------------------------------------------- */
 
@@ -400,6 +445,8 @@ int moe_bias_update(const int32_t* counts, int n, float gamma, int rule,
 int64_t moe_unique_weight_bytes_vanilla(int d, int n, int I, int I_s, int dtype, int A_e);
 int64_t moe_unique_weight_bytes_deamoe(int d, int n, int I_sh, int I_pr, int I_s,
                                        int dtype, int A_d, int A_e);
+/* Form P (bf16 weights): 4*d*n + 2*(A_d*3*d*r + A_e*3*r*r). */
+int64_t moe_unique_weight_bytes_formp(int d, int n, int r, int A_d, int A_e);
 
 #ifdef __cplusplus
 }

@@ -55,6 +55,10 @@ _SIGS = {
     "moe_route_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _SZ, _P]),
     "moe_route_topk_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
     "moe_bias_update": (_I, [_P, _I, _F, _I, _P, _P, _P]),
+    "moe_formp_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "deamoe_p_layer_forward": (_I, [_P, _I, _I, _I, _I, _F, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P,
+                                    _P, _P, _P, _SZ, _P, _P, _P, _P]),
+    "moe_unique_weight_bytes_formp": (C.c_int64, [_I, _I, _I, _I, _I]),
     "moe_route_topk_grouped": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _SZ, _P]),
     "moe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _P, _SZ, _P]),
     "moe_rows_count": (_I64, [_I, _I, _I, _I, _I]),
@@ -280,6 +284,36 @@ def deamoe_layer_forward(x, k: int, scale: float, w_router, bias, experts_per_de
         _dtype_code(dept[0]), _ptr(dept[0]), _ptr(dept[1]), _ptr(dept[2]), _ptr(pg), _ptr(pu),
         _ptr(pd), I_s, _ptr(sg), _ptr(su), _ptr(sd), _ptr(ws), ws.numel(), _ptr(topk_idx),
         _ptr(topk_w), _ptr(y), _stream()))
+
+
+def moe_formp_workspace_bytes(T: int, n: int, k: int, experts_per_dept: int, r: int) -> int:
+    return int(lib().moe_formp_workspace_bytes(T, n, k, experts_per_dept, r))
+
+
+def new_formp_workspace(T: int, n: int, k: int, experts_per_dept: int, r: int, device="cuda") -> torch.Tensor:
+    """Allocate (torch) and zero (library kernel) a form-P workspace."""
+    nbytes = moe_formp_workspace_bytes(T, n, k, experts_per_dept, r)
+    if nbytes == 0:
+        raise MoeError("moe_formp_workspace_bytes", -1, "invalid sizes")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    moe_workspace_init(ws)
+    return ws
+
+
+def deamoe_p_layer_forward(x, k: int, scale: float, w_router, bias, experts_per_dept: int, k_dept: int,
+                           dept, amat, ws, topk_idx, topk_w, y):
+    """``dept`` = (gate, up, down) [m, r, d]; ``amat`` = (A_g, A_u, A_d) [n, r, r]."""
+    T, d = x.shape
+    n = w_router.shape[0]
+    r = dept[0].shape[1]
+    _check("deamoe_p_layer_forward", lib().deamoe_p_layer_forward(
+        _ptr(x), T, d, n, k, scale, _ptr(w_router), _ptr(bias), experts_per_dept, k_dept, r,
+        _dtype_code(dept[0]), _ptr(dept[0]), _ptr(dept[1]), _ptr(dept[2]), _ptr(amat[0]), _ptr(amat[1]),
+        _ptr(amat[2]), _ptr(ws), ws.numel(), _ptr(topk_idx), _ptr(topk_w), _ptr(y), _stream()))
+
+
+def moe_unique_weight_bytes_formp(d, n, r, A_d, A_e) -> int:
+    return int(lib().moe_unique_weight_bytes_formp(d, n, r, A_d, A_e))
 
 
 def moe_unique_weight_bytes_vanilla(d, n, I, I_s, dtype_code, A_e) -> int:

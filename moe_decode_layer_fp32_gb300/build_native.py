@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_gb300.so")
-SOURCES = ("api.cu", "route_dispatch.cu", "ffn.cu", "ffn_tc.cu", "balance.cu")
+SOURCES = ("api.cu", "route_dispatch.cu", "ffn.cu", "ffn_tc.cu", "balance.cu", "formp.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -782,6 +782,102 @@ int deamoe_layer_forward(const float* x, int T, int d, int n, int k, float scale
     return layer_ffn(a, T, n, k, experts_per_dept, I_s > 0, tc, t, path, stream, who);
 }
 
+// Form-P scratch after the standard layout: G and U [T*min(k,m), r], then
+// Z [T*k, r], all fp32.
+static bool formp_layout(int T, int n, int k, int g, int r, moe_ws_layout* L, size_t* og, size_t* ou,
+                         size_t* oz, size_t* total) {
+    if (g < 2 || r < 16 || r % 16 != 0 || !layout_of(T, n, k, g, L)) return false;
+    const int m = n / g;
+    const size_t mk = (size_t)T * (k < m ? k : m);
+    *og = align_up(L->total, 256);
+    *ou = align_up(*og + mk * r * sizeof(float), 256);
+    *oz = align_up(*ou + mk * r * sizeof(float), 256);
+    *total = align_up(*oz + (size_t)T * k * r * sizeof(float), 256);
+    return true;
+}
+
+size_t moe_formp_workspace_bytes(int T, int n, int k, int experts_per_dept, int r) {
+    moe_ws_layout L;
+    size_t og, ou, oz, total;
+    return formp_layout(T, n, k, experts_per_dept, r, &L, &og, &ou, &oz, &total) ? total : 0;
+}
+
+int deamoe_p_layer_forward(const float* x, int T, int d, int n, int k, float scale, const float* w_router,
+                           const float* bias, int experts_per_dept, int k_dept, int r, int dtype,
+                           const void* dept_gate, const void* dept_up, const void* dept_down,
+                           const void* a_gate, const void* a_up, const void* a_down, void* ws,
+                           size_t ws_bytes, int32_t* topk_idx, float* topk_w, float* y, void* stream) {
+    const char* who = "deamoe_p_layer_forward";
+    const int g = experts_per_dept;
+    moe_ws_layout L;
+    size_t og, ou, oz, total;
+    if (!formp_layout(T, n, k, g, r, &L, &og, &ou, &oz, &total))
+        return fail(MOE_ERR_INVALID_ARG,
+                    "%s: need 1<=T<=%d, 1<=n<=%d, 1<=k<=min(n,%d), experts_per_dept>=2 dividing n, "
+                    "r a positive multiple of 16 (T=%d n=%d k=%d g=%d r=%d)",
+                    who, moe::kMaxT, moe::kMaxN, moe::kMaxK, T, n, k, g, r);
+    const int m = n / g;
+    if (k_dept < 0 || k_dept > m || (k_dept > 0 && (long long)k > (long long)k_dept * g))
+        return fail(MOE_ERR_INVALID_ARG, "%s: k_dept=%d must be 0 (plain top-k) or in [1, %d] with k <= k_dept*g",
+                    who, k_dept, m);
+    if (!ws || !aligned16(ws)) return fail(MOE_ERR_INVALID_ARG, "%s: workspace null or unaligned", who);
+    if (ws_bytes < total)
+        return fail(MOE_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu required (moe_formp_workspace_bytes)",
+                    who, ws_bytes, total);
+    int rc = check_hidden(x, d, who);
+    if (rc) return rc;
+    if (dtype != MOE_DTYPE_BF16) return fail(MOE_ERR_UNSUPPORTED, "%s: form P takes bf16 weights only", who);
+    if (d > moe::formp_max_hidden() || d > kMaxRouterHidden)
+        return fail(MOE_ERR_UNSUPPORTED, "%s: d=%d exceeds %d", who, d, moe::formp_max_hidden());
+    if (r > moe::formp_max_width()) return fail(MOE_ERR_UNSUPPORTED, "%s: r=%d exceeds %d", who, r, moe::formp_max_width());
+    const void* wts[6] = {dept_gate, dept_up, dept_down, a_gate, a_up, a_down};
+    for (const void* p : wts)
+        if (!p || !aligned16(p)) return fail(MOE_ERR_INVALID_ARG, "%s: weights null or unaligned", who);
+    if (!y || !aligned16(y)) return fail(MOE_ERR_INVALID_ARG, "%s: y null or unaligned", who);
+    if (!w_router || !aligned16(w_router)) return fail(MOE_ERR_INVALID_ARG, "%s: w_router null or unaligned", who);
+    if (!topk_idx || !topk_w) return fail(MOE_ERR_INVALID_ARG, "%s: routing outputs are null", who);
+    moe::RouteArgs ra = {};
+    ra.x = x;
+    ra.w_router = w_router;
+    ra.bias = bias;
+    ra.T = T; ra.d = d; ra.n = n; ra.k = k;
+    ra.scale = scale;
+    ra.topk_idx = topk_idx;
+    ra.topk_w = topk_w;
+    ra.ws = resolve(ws, L);
+    ra.g = g;
+    ra.y_zero = y;
+    ra.y_elems = (long long)T * d;
+    ra.fuse_dispatch = 1;
+    ra.route_g = g;
+    ra.k_dept = k_dept;
+    cudaStream_t s = as_stream(stream);
+    cudaError_t e = moe::launch_route(ra, s);
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    char* b = static_cast<char*>(ws);
+    moe::FormPArgs a = {};
+    a.x = x;
+    a.T = T; a.d = d; a.n = n; a.k = k; a.g = g; a.m = m;
+    a.mk = k < m ? k : m;
+    a.r = r;
+    a.dgate = dept_gate; a.dup = dept_up; a.ddown = dept_down;
+    a.agate = a_gate; a.aup = a_up; a.adown = a_down;
+    a.topk_idx = topk_idx;
+    a.gbuf = reinterpret_cast<float*>(b + og);
+    a.ubuf = reinterpret_cast<float*>(b + ou);
+    a.zbuf = reinterpret_cast<float*>(b + oz);
+    a.y = y;
+    a.ws = ra.ws;
+    e = moe::launch_formp(a, moe::device_sm_count(), s);
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    return MOE_OK;
+}
+
+int64_t moe_unique_weight_bytes_formp(int d, int n, int r, int A_d, int A_e) {
+    if (d <= 0 || n <= 0 || r <= 0 || A_d < 0 || A_e < 0 || A_e > n) return -1;
+    return 4LL * d * n + 2LL * ((int64_t)A_d * 3 * d * r + (int64_t)A_e * 3 * r * r);
+}
+
 int64_t moe_unique_weight_bytes_vanilla(int d, int n, int I, int I_s, int dtype, int A_e) {
     const int bw = weight_bytes(dtype);
     if (d <= 0 || n <= 0 || I < 0 || I_s < 0 || bw == 0 || A_e < 0 || A_e > n) return -1;

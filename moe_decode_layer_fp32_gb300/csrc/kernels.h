@@ -152,6 +152,30 @@ __device__ __forceinline__ bool prefer_tc(const FfnArgs& a) {
     return tiles > 0 && tc_rows * S * 3 < rows_cc * cc_weight;
 }
 
+// DeaMoE form P ([DeaMoE] §3.1 eq. (4)): three passes over one layer.
+enum FormPStage { kFormPUp = 0, kFormPPriv = 1, kFormPDown = 2 };
+struct FormPArgs {
+    const float* x;          // [T, d]
+    int T, d, n, k, g, m;    // m = n / g departments
+    int mk;                  // min(k, m): department entries per token at most
+    int r;                   // department / expert width (hffn)
+    const void* dgate;       // [m, r, d] bf16
+    const void* dup;
+    const void* ddown;
+    const void* agate;       // [n, r, r] bf16
+    const void* aup;
+    const void* adown;
+    const int32_t* topk_idx; // [T, k] routing of the step
+    float* gbuf;             // [T*mk, r] SiLU(W_g x) per department entry
+    float* ubuf;             // [T*mk, r] SiLU(W_u x)
+    float* zbuf;             // [T*k, r] A_d^T Y per assignment (before SiLU)
+    float* y;                // [T, d], zeroed by the routing kernel
+    WsPtrs ws;
+};
+cudaError_t launch_formp(const FormPArgs& a, int sms, cudaStream_t s);
+int formp_max_hidden();   // widest h the up / down passes take
+int formp_max_width();    // widest r the private pass takes
+
 struct CombineArgs {
     const float* rows;
     int T, d, k, m;        // m = departments (0 for vanilla)

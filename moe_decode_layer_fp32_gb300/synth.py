@@ -54,6 +54,10 @@ class LayerShape:
     batches: tuple = field(default_factory=tuple)
     zipf: float = 0.0      # >0: router bias makes popularity Zipf(s)
     zipf_g: int = 0        # department size used to build that bias
+    # DeaMoE in the paper's parameterisation (eq. 4): departments of width
+    # r = I_sh and per-expert r x r matrices A_g, A_u, A_d
+    form_p: bool = False
+    k_dept: int = 0        # group-limited routing: departments per token (0 = plain top-k)
 
     @property
     def m(self) -> int:
@@ -90,8 +94,24 @@ ZIPF_VANILLA = LayerShape("vanilla-7b-zipf1.1", d=2048, n=64, k=8, dtype="bf16",
                           I=1152, zipf=1.1, zipf_g=8,
                           batches=(1, 2, 4, 8, 16, 32, 64, 128))
 
+# DeaMoE form P at the budget-matched Table 1 shapes (h, r, m departments, n
+# experts, k_dept, k): the 7B-class model (1024, 384, 8, 672, 4, 10) and the
+# DeepSeek-V3 match (7168, 2048, 8, 864, 5, 10), plus a tiny correctness case.
+TINY_FORMP = LayerShape("tiny-deamoe-p-h256-r64-dept4x4-top4-kdept2-bf16", d=256, n=16, k=4,
+                        dtype="bf16", g=4, I_sh=64, form_p=True, k_dept=2, batches=(1, 5, 33))
+FORMP_7B = LayerShape("deamoe-p-h1024-r384-dept8x84-top10-kdept4-bf16", d=1024, n=672, k=10,
+                      dtype="bf16", g=84, I_sh=384, form_p=True, k_dept=4,
+                      batches=(1, 4, 16, 64))
+FORMP_DSV3 = LayerShape("deamoe-p-h7168-r2048-dept8x108-top10-kdept5-bf16", d=7168, n=864,
+                        k=10, dtype="bf16", g=108, I_sh=2048, form_p=True, k_dept=5,
+                        batches=(1, 4, 16, 64))
+# The DeepSeek-V3 routed experts alone (the baseline of Figure 2).
+DSV3_ROUTED = LayerShape("vanilla-d7168-e256-i2048-top8-bf16", d=7168, n=256, k=8,
+                         dtype="bf16", I=2048, batches=(1, 4, 16, 64))
+
 ALL_SHAPES = (TINY_DEAMOE, TINY_VANILLA, VANILLA_128E, DEAMOE_7B, VANILLA_7B,
-              DSV3_VANILLA, DSV3_DEAMOE, ZIPF_DEAMOE, ZIPF_VANILLA)
+              DSV3_VANILLA, DSV3_DEAMOE, ZIPF_DEAMOE, ZIPF_VANILLA, TINY_FORMP, FORMP_7B,
+              FORMP_DSV3, DSV3_ROUTED)
 
 WEIGHT_STD = 0.02
 
@@ -103,6 +123,7 @@ TID_GATE, TID_UP, TID_DOWN = 10, 11, 12            # vanilla experts
 TID_DGATE, TID_DUP, TID_DDOWN = 20, 21, 22         # department backbone
 TID_PGATE, TID_PUP, TID_PDOWN = 30, 31, 32         # private columns
 TID_SGATE, TID_SUP, TID_SDOWN = 40, 41, 42         # shared expert
+TID_AGATE, TID_AUP, TID_ADOWN = 50, 51, 52         # form-P expert matrices
 
 
 def stream_seed(seed: int, tensor_id: int, salt: int = 0) -> int:
@@ -184,13 +205,27 @@ def proj(units: int, rows: int, d: int, seed: int, tensor_id: int, dtype: str,
     return out
 
 
+def near_identity(units: int, r: int, seed: int, tensor_id: int, dtype: str,
+                  device="cpu") -> torch.Tensor:
+    """``[units, r, r]`` matrices ``I + N(0, 0.02)`` in the storage dtype: the
+    identity start of the form-P expert matrices (DeaMoE §3.4) with a
+    perturbation standing in for training.  Drawn in fp32, rounded once."""
+    out = torch.empty((units, r, r), dtype=storage_dtype(dtype), device=device)
+    eye = torch.eye(r, dtype=torch.float32, device=device)
+    for u in range(units):
+        a = normal((r, r), seed, tensor_id, WEIGHT_STD, device, salt=u + 1)
+        out[u].copy_((a + eye).to(storage_dtype(dtype)))
+    return out
+
+
 def make_layer(shape: LayerShape, seed: int, device="cpu", with_router: bool = True) -> dict:
     """All weights of one layer as a dict of tensors on ``device``.
 
     Keys: ``router`` [n,d] f32, ``bias`` [n] f32 or None; vanilla: ``gate``,
     ``up``, ``down`` [n,I,d]; DeaMoE: ``dgate``, ``dup``, ``ddown`` [m,I_sh,d]
     and ``pgate``, ``pup``, ``pdown`` [n,I_pr,d]; shared expert: ``sgate``,
-    ``sup``, ``sdown`` [I_s,d] (or None).
+    ``sup``, ``sdown`` [I_s,d] (or None); form P: the department tensors
+    with r = I_sh and ``agate``, ``aup``, ``adown`` [n,r,r].
     """
     s = shape
     L: dict = {"shape": s}
@@ -206,6 +241,10 @@ def make_layer(shape: LayerShape, seed: int, device="cpu", with_router: bool = T
         L["dgate"] = proj(s.m, s.I_sh, s.d, seed, TID_DGATE, s.dtype, device)
         L["dup"] = proj(s.m, s.I_sh, s.d, seed, TID_DUP, s.dtype, device)
         L["ddown"] = proj(s.m, s.I_sh, s.d, seed, TID_DDOWN, s.dtype, device)
+    if s.form_p:
+        L["agate"] = near_identity(s.n, s.I_sh, seed, TID_AGATE, s.dtype, device)
+        L["aup"] = near_identity(s.n, s.I_sh, seed, TID_AUP, s.dtype, device)
+        L["adown"] = near_identity(s.n, s.I_sh, seed, TID_ADOWN, s.dtype, device)
     if s.I_pr > 0:
         L["pgate"] = proj(s.n, s.I_pr, s.d, seed, TID_PGATE, s.dtype, device)
         L["pup"] = proj(s.n, s.I_pr, s.d, seed, TID_PUP, s.dtype, device)
