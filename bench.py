@@ -44,6 +44,9 @@ WORKLOADS = {
     "dsv3-deamoe": synth.DSV3_DEAMOE,
     "zipf-deamoe": synth.ZIPF_DEAMOE,
     "zipf-vanilla": synth.ZIPF_VANILLA,
+    "formp-7b": synth.FORMP_7B,
+    "formp-dsv3": synth.FORMP_DSV3,
+    "dsv3-routed": synth.DSV3_ROUTED,
 }
 METRIC = "MoE-layer decode µs and achieved HBM GB/s (unique weight bytes) at batch 1–64"
 L2_BYTES = 129 * 2 ** 20
@@ -197,14 +200,15 @@ class Workload:
             for T in batches:
                 key = (r, T)
                 self.x[key] = synth.hidden(T, s.d, seed * 1000 + r * 131 + T, device)
-                self.ws[key] = B.new_workspace(T, s.n, s.k, self.g, device)
+                self.ws[key] = (B.new_formp_workspace(T, s.n, s.k, s.g, s.I_sh, device) if s.form_p
+                                else B.new_workspace(T, s.n, s.k, self.g, device))
                 self.idx[key] = torch.empty((T, s.k), dtype=torch.int32, device=device)
                 self.w[key] = torch.empty((T, s.k), dtype=torch.float32, device=device)
                 self.y[key] = torch.empty((T, s.d), dtype=torch.float32, device=device)
         # group-limited routing: the departments, or n/8 groups of a vanilla
         # layer; half of them kept per token
         self.rg = s.g if s.I_sh > 0 and s.g > 1 else max(1, s.n // 8)
-        self.k_dept = max(1, (s.n // self.rg) // 2)
+        self.k_dept = s.k_dept or max(1, (s.n // self.rg) // 2)
         self.gidx = {T: torch.empty((T, s.k), dtype=torch.int32, device=device) for T in batches}
         self.gw = {T: torch.empty((T, s.k), dtype=torch.float32, device=device) for T in batches}
         self.bias_copy = [torch.zeros(s.n, device=device) for _ in range(replicas)]
@@ -221,7 +225,11 @@ class Workload:
         s, B, L, key = self.shape, self.B, self.layers[r], (r, T)
         x = self.x[key] if x is None else x
         y = self.y[key] if y is None else y
-        if s.I_sh > 0:
+        if s.form_p:
+            B.deamoe_p_layer_forward(x, s.k, 1.0, L["router"], L["bias"], s.g, s.k_dept,
+                                     (L["dgate"], L["dup"], L["ddown"]), (L["agate"], L["aup"], L["adown"]),
+                                     self.ws[key], self.idx[key], self.w[key], y)
+        elif s.I_sh > 0:
             priv = (L["pgate"], L["pup"], L["pdown"]) if s.I_pr > 0 else None
             B.deamoe_layer_forward(x, s.k, 1.0, L["router"], L["bias"], s.g,
                                    (L["dgate"], L["dup"], L["ddown"]), priv, self.shared(L),
@@ -231,9 +239,13 @@ class Workload:
                                 self.shared(L), self.ws[key], self.idx[key], self.w[key], y)
 
     def route_only(self, r, T):
-        L, key = self.layers[r], (r, T)
-        self.B.moe_route_topk(self.x[key], L["router"], L["bias"], self.shape.k, 1.0,
-                              self.idx[key], self.w[key], self.ws[key])
+        s, L, key = self.shape, self.layers[r], (r, T)
+        if s.k_dept:
+            self.B.moe_route_topk_grouped(self.x[key], L["router"], L["bias"], s.k, s.g, s.k_dept, False, 1.0,
+                                          self.idx[key], self.w[key], self.ws[key])
+        else:
+            self.B.moe_route_topk(self.x[key], L["router"], L["bias"], s.k, 1.0,
+                                  self.idx[key], self.w[key], self.ws[key])
 
     def grouped_only(self, r, T, strict: bool):
         """Group-limited routing of the same inputs (k_dept of the departments,
@@ -255,7 +267,10 @@ class Workload:
 
     def ffn_only(self, r, T, out):
         s, B, L, key = self.shape, self.B, self.layers[r], (r, T)
-        if s.I_sh > 0:
+        if s.form_p:
+            B.deamoe_p_ffn(self.x[key], s.k, s.g, (L["dgate"], L["dup"], L["ddown"]),
+                           (L["agate"], L["aup"], L["adown"]), self.idx[key], self.ws[key], out)
+        elif s.I_sh > 0:
             priv = (L["pgate"], L["pup"], L["pdown"]) if s.I_pr > 0 else None
             B.deamoe_ffn(self.x[key], s.k, s.g, (L["dgate"], L["dup"], L["ddown"]), priv,
                          self.shared(L), self.ws[key], B.MOE_OUT_ACCUM, out)
@@ -271,7 +286,9 @@ class Workload:
             st, A_e, A_d = B.moe_read_status(ws)
             if st != 0:
                 raise RuntimeError(f"device status {st} for {key}")
-            if s.I_sh > 0:
+            if s.form_p:
+                U = B.moe_unique_weight_bytes_formp(s.d, s.n, s.I_sh, A_d, A_e)
+            elif s.I_sh > 0:
                 U = B.moe_unique_weight_bytes_deamoe(s.d, s.n, s.I_sh, s.I_pr, s.I_s, code, A_d, A_e)
             else:
                 U = B.moe_unique_weight_bytes_vanilla(s.d, s.n, s.I, s.I_s, code, A_e)
@@ -286,6 +303,8 @@ class Workload:
         automatic mode exactly when the kernels recorded a choice; with a fixed
         threshold when the weights qualify and T >= thr."""
         s, T = self.shape, key[1]
+        if s.form_p:
+            return False
         rows = [r for r in (s.I, s.I_sh, s.I_pr, s.I_s) if r > 0]
         ok = s.dtype == "bf16" and s.d % 128 == 0 and all(r % 128 == 0 for r in rows)
         if not ok:
@@ -329,7 +348,8 @@ def run_ours(args, rank, world, local):
     # Replicas: enough that the bytes between two uses of a replica exceed 4x L2.
     # (smallest pass: one token, k experts, one department)
     bw = 2 if shape.dtype == "bf16" else 4
-    per_layer_min = bw * 3 * shape.d * (shape.I_pr * shape.k + shape.I_sh + shape.I * shape.k + shape.I_s)
+    per_layer_min = (bw * 3 * (shape.d * shape.I_sh + shape.I_sh * shape.I_sh * shape.k) if shape.form_p else
+                     bw * 3 * shape.d * (shape.I_pr * shape.k + shape.I_sh + shape.I * shape.k + shape.I_s))
     R = args.replicas or max(2, min(16, -(-4 * L2_BYTES // max(1, per_layer_min))))
     W = Workload(B, shape, batches, R, args.seed + 17 * rank, device)
 
@@ -395,7 +415,8 @@ def run_ours(args, rank, world, local):
     ffn_bytes = reps_f * sum(W.ffn_bytes.values())
     peaks = load_peaks()
     achieved = ffn_bytes / t_ffn / 1e9
-    ffn_kernels = sorted({"ffn_tc_kernel" if W.choice[key] == 2 else "ffn_stream_kernel" for key in W.ws})
+    ffn_kernels = (["formp_kernel up / private / down passes"] if shape.form_p else
+                   sorted({"ffn_tc_kernel" if W.choice[key] == 2 else "ffn_stream_kernel" for key in W.ws}))
     roofline = {"bound": "hbm", "kernel": "expert FFN step (" + ", ".join(ffn_kernels) + ")",
                 "achieved": round(achieved, 1),
                 "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
@@ -453,8 +474,9 @@ def run_ours(args, rank, world, local):
         "per_batch": per_batch,
         "roofline": roofline,
         "e2e": e2e,
-        # per layer pass: routing (+ fused dispatch), CUDA-core FFN, tensor-core FFN when launched
-        "gpu_launches": sum(2 + int(W.tc_launched((i % R, T), args.tc_min_tokens))
+        # per layer pass: routing (+ fused dispatch), CUDA-core FFN, tensor-core FFN when
+        # launched; form P: routing and its three passes
+        "gpu_launches": sum((4 if shape.form_p else 2 + int(W.tc_launched((i % R, T), args.tc_min_tokens)))
                             for i in range(args.steps) for T in batches),
         "clocks": clock_info,
         "cpu_baseline": cpu,
@@ -468,7 +490,9 @@ def workload_config(shape, batches):
     return {"workload": f"{shape.name} T={'/'.join(map(str, batches))}", "d": shape.d,
             "n_experts": shape.n, "top_k": shape.k, "I": shape.I, "I_sh": shape.I_sh,
             "I_pr": shape.I_pr, "experts_per_dept": shape.g, "I_shared": shape.I_s,
-            "weights_dtype": shape.dtype, "zipf": shape.zipf, "batches": list(batches)}
+            "weights_dtype": shape.dtype, "zipf": shape.zipf, "batches": list(batches),
+            "form": "P (eq. 4, r = I_sh)" if shape.form_p else "C" if shape.I_sh > 0 else "vanilla",
+            "k_dept": shape.k_dept}
 
 
 def load_traffic(workload: str):
@@ -512,13 +536,31 @@ def cpu_baseline(W, shape, batches, budget_s):
     host = {}
     while t_total <= budget_s and passes < 100 * len(keys):
         r, T = keys[passes % len(keys)]
-        if r not in host:
+        if shape.form_p:
+            # form P: host copies of the units this pass touches only (a
+            # whole layer can be tens of GB)
             L = W.layers[r]
-            host[r] = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in L.items()}
+            Wl = host.setdefault(r, {"router": L["router"].cpu(), "bias": None if L["bias"] is None else L["bias"].cpu()})
+            sel, _, _ = O.route_grouped(W.x[(r, T)].cpu(), Wl["router"], shape.k, shape.g, shape.k_dept or
+                                        shape.n // shape.g, bias=Wl["bias"])          # untimed: units to copy
+            for e in set(sel.ravel().tolist()):
+                for key_, src, u in (("dgate", "dgate", e // shape.g), ("dup", "dup", e // shape.g),
+                                     ("ddown", "ddown", e // shape.g), ("agate", "agate", e),
+                                     ("aup", "aup", e), ("adown", "adown", e)):
+                    Wl.setdefault(key_, {})
+                    if u not in Wl[key_]:
+                        Wl[key_][u] = L[src][u].cpu()
+        else:
+            if r not in host:
+                L = W.layers[r]
+                host[r] = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in L.items()}
         L = host[r]
         x = W.x[(r, T)].cpu()
         t0 = time.perf_counter()
-        idx, p, _ = O.route(x, L["router"], shape.k, bias=L["bias"])
+        if shape.k_dept:
+            idx, p, _ = O.route_grouped(x, L["router"], shape.k, shape.g, shape.k_dept, bias=L["bias"])
+        else:
+            idx, p, _ = O.route(x, L["router"], shape.k, bias=L["bias"])
         oracle_forward(O, shape, L, x, idx, p)
         t_total += time.perf_counter() - t0
         done_bytes += W.unique[(r, T)]
@@ -531,6 +573,9 @@ def cpu_baseline(W, shape, batches, budget_s):
 
 
 def oracle_forward(O, shape, L, x, idx, p):
+    if shape.form_p:
+        return O.deamoe_layer_p(x, idx, p, shape.g, L["dgate"], L["dup"], L["ddown"], L["agate"], L["aup"],
+                                L["adown"])
     sh = None if L["sgate"] is None else (L["sgate"], L["sup"], L["sdown"])
     if shape.I_sh > 0:
         priv = (L["pgate"], L["pup"], L["pdown"]) if shape.I_pr > 0 else (None, None, None)
@@ -554,7 +599,13 @@ def run_reference(args, rank, world):
     bias = synth.zipf_bias(s.n, s.zipf_g, s.zipf, seed) if s.zipf > 0 else None
     ntok = -(-(args.steps + args.warmup) // s.k)
     xs = synth.hidden(ntok, s.d, seed + 7)
-    idx_all, _, _ = O.route(xs, router, s.k, bias=bias)       # untimed: which units to make
+
+    def route(x):
+        if s.k_dept:
+            return O.route_grouped(x, router, s.k, s.g, s.k_dept, bias=bias)
+        return O.route(x, router, s.k, bias=bias)
+
+    idx_all, _, _ = route(xs)       # untimed: which units to make
     units = {}
 
     def unit(tid, u, rows):
@@ -563,7 +614,16 @@ def run_reference(args, rank, world):
                                            synth.storage_dtype(s.dtype), salt=u + 1)
         return units[(tid, u)]
 
+    def amat(tid, e):
+        if (tid, e) not in units:
+            units[(tid, e)] = synth.near_identity_unit(e, s.I_sh, seed, tid, s.dtype)
+        return units[(tid, e)]
+
     def weights(e):
+        if s.form_p:
+            j = e // s.g
+            return ([unit(t, j, s.I_sh) for t in (synth.TID_DGATE, synth.TID_DUP, synth.TID_DDOWN)] +
+                    [amat(t, e) for t in (synth.TID_AGATE, synth.TID_AUP, synth.TID_ADOWN)])
         if s.I_sh > 0:
             j = e // s.g
             return [torch.cat([unit(t1, j, s.I_sh)] + ([unit(t2, e, s.I_pr)] if s.I_pr else []))
@@ -581,7 +641,7 @@ def run_reference(args, rank, world):
         nbytes = 0
         if q == 0:
             x = xs[tok:tok + 1]
-            idx, p, _ = O.route(x, router, s.k, bias=bias)
+            idx, p, _ = route(x)
             state.update(x=x, idx=idx, p=p, depts=set())
             nbytes += 4 * s.d * s.n
             if SH is not None:
@@ -589,12 +649,18 @@ def run_reference(args, rank, world):
                 nbytes += bw * 3 * s.d * s.I_s
         x, idx, p = state["x"], state["idx"], state["p"]
         e = int(idx[0, q])
-        p[0, q] * O.swiglu_expert(x[0], *W[e])
-        if s.I_sh > 0:
+        if s.form_p:
+            p[0, q] * O.deamoe_expert_p(x[0], *W[e])
+            j = e // s.g
+            nbytes += 2 * (3 * s.d * s.I_sh * (j not in state["depts"]) + 3 * s.I_sh * s.I_sh)
+            state["depts"].add(j)
+        elif s.I_sh > 0:
+            p[0, q] * O.swiglu_expert(x[0], *W[e])
             j = e // s.g
             nbytes += bw * 3 * s.d * (s.I_pr + (s.I_sh if j not in state["depts"] else 0))
             state["depts"].add(j)
         else:
+            p[0, q] * O.swiglu_expert(x[0], *W[e])
             nbytes += bw * 3 * s.d * s.I
         return nbytes
 

@@ -403,6 +403,17 @@ int deamoe_p_layer_forward(const float* x, int T, int d, int n, int k, float sca
                            void* ws, size_t ws_bytes, int32_t* topk_idx, float* topk_w,
                            float* y, void* stream);
 
+/*
+ * The three weight passes of deamoe_p_layer_forward alone, on a routing the
+ * caller already made: topk_idx [T, k] and the workspace's dispatch lists
+ * (moe_dispatch with experts_per_dept, or an earlier layer call on the same
+ * inputs).  y is overwritten.  Arguments and limits as above.
+ */
+int deamoe_p_ffn(const float* x, int T, int d, int n, int k, int experts_per_dept, int r,
+                 int dtype, const void* dept_gate, const void* dept_up, const void* dept_down,
+                 const void* a_gate, const void* a_up, const void* a_down,
+                 const int32_t* topk_idx, void* ws, size_t ws_bytes, float* y, void* stream);
+
 /* ------------------------------------------------------------------------- */
 /* Router-bias load balancing                                                */
 /* ------------------------------------------------------------------------- */

@@ -59,6 +59,7 @@ _SIGS = {
     "deamoe_p_layer_forward": (_I, [_P, _I, _I, _I, _I, _F, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P,
                                     _P, _P, _P, _SZ, _P, _P, _P, _P]),
     "moe_unique_weight_bytes_formp": (C.c_int64, [_I, _I, _I, _I, _I]),
+    "deamoe_p_ffn": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "moe_route_topk_grouped": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _SZ, _P]),
     "moe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _P, _SZ, _P]),
     "moe_rows_count": (_I64, [_I, _I, _I, _I, _I]),
@@ -310,6 +311,16 @@ def deamoe_p_layer_forward(x, k: int, scale: float, w_router, bias, experts_per_
         _ptr(x), T, d, n, k, scale, _ptr(w_router), _ptr(bias), experts_per_dept, k_dept, r,
         _dtype_code(dept[0]), _ptr(dept[0]), _ptr(dept[1]), _ptr(dept[2]), _ptr(amat[0]), _ptr(amat[1]),
         _ptr(amat[2]), _ptr(ws), ws.numel(), _ptr(topk_idx), _ptr(topk_w), _ptr(y), _stream()))
+
+
+def deamoe_p_ffn(x, k: int, experts_per_dept: int, dept, amat, topk_idx, ws, y):
+    T, d = x.shape
+    n = amat[0].shape[0]
+    r = dept[0].shape[1]
+    _check("deamoe_p_ffn", lib().deamoe_p_ffn(
+        _ptr(x), T, d, n, k, experts_per_dept, r, _dtype_code(dept[0]), _ptr(dept[0]), _ptr(dept[1]),
+        _ptr(dept[2]), _ptr(amat[0]), _ptr(amat[1]), _ptr(amat[2]), _ptr(topk_idx), _ptr(ws), ws.numel(),
+        _ptr(y), _stream()))
 
 
 def moe_unique_weight_bytes_formp(d, n, r, A_d, A_e) -> int:

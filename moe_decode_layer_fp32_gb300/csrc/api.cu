@@ -802,24 +802,17 @@ size_t moe_formp_workspace_bytes(int T, int n, int k, int experts_per_dept, int 
     return formp_layout(T, n, k, experts_per_dept, r, &L, &og, &ou, &oz, &total) ? total : 0;
 }
 
-int deamoe_p_layer_forward(const float* x, int T, int d, int n, int k, float scale, const float* w_router,
-                           const float* bias, int experts_per_dept, int k_dept, int r, int dtype,
-                           const void* dept_gate, const void* dept_up, const void* dept_down,
-                           const void* a_gate, const void* a_up, const void* a_down, void* ws,
-                           size_t ws_bytes, int32_t* topk_idx, float* topk_w, float* y, void* stream) {
-    const char* who = "deamoe_p_layer_forward";
-    const int g = experts_per_dept;
-    moe_ws_layout L;
-    size_t og, ou, oz, total;
-    if (!formp_layout(T, n, k, g, r, &L, &og, &ou, &oz, &total))
+// Checks shared by the form-P layer and its FFN step; fills the layout and
+// the scratch offsets.
+static int formp_checks(const float* x, int T, int d, int n, int k, int g, int r, int dtype,
+                        const void* const (&wts)[6], const void* ws, size_t ws_bytes, const float* y,
+                        moe_ws_layout* L, size_t* og, size_t* ou, size_t* oz, const char* who) {
+    size_t total;
+    if (!formp_layout(T, n, k, g, r, L, og, ou, oz, &total))
         return fail(MOE_ERR_INVALID_ARG,
                     "%s: need 1<=T<=%d, 1<=n<=%d, 1<=k<=min(n,%d), experts_per_dept>=2 dividing n, "
                     "r a positive multiple of 16 (T=%d n=%d k=%d g=%d r=%d)",
                     who, moe::kMaxT, moe::kMaxN, moe::kMaxK, T, n, k, g, r);
-    const int m = n / g;
-    if (k_dept < 0 || k_dept > m || (k_dept > 0 && (long long)k > (long long)k_dept * g))
-        return fail(MOE_ERR_INVALID_ARG, "%s: k_dept=%d must be 0 (plain top-k) or in [1, %d] with k <= k_dept*g",
-                    who, k_dept, m);
     if (!ws || !aligned16(ws)) return fail(MOE_ERR_INVALID_ARG, "%s: workspace null or unaligned", who);
     if (ws_bytes < total)
         return fail(MOE_ERR_WORKSPACE, "%s: workspace %zu bytes < %zu required (moe_formp_workspace_bytes)",
@@ -830,10 +823,52 @@ int deamoe_p_layer_forward(const float* x, int T, int d, int n, int k, float sca
     if (d > moe::formp_max_hidden() || d > kMaxRouterHidden)
         return fail(MOE_ERR_UNSUPPORTED, "%s: d=%d exceeds %d", who, d, moe::formp_max_hidden());
     if (r > moe::formp_max_width()) return fail(MOE_ERR_UNSUPPORTED, "%s: r=%d exceeds %d", who, r, moe::formp_max_width());
-    const void* wts[6] = {dept_gate, dept_up, dept_down, a_gate, a_up, a_down};
     for (const void* p : wts)
         if (!p || !aligned16(p)) return fail(MOE_ERR_INVALID_ARG, "%s: weights null or unaligned", who);
     if (!y || !aligned16(y)) return fail(MOE_ERR_INVALID_ARG, "%s: y null or unaligned", who);
+    return MOE_OK;
+}
+
+static int formp_launch(const float* x, int T, int d, int n, int k, int g, int r, const void* const (&wts)[6],
+                        const int32_t* topk_idx, void* ws, const moe_ws_layout& L, size_t og, size_t ou,
+                        size_t oz, float* y, bool zero_y, cudaStream_t s, const char* who) {
+    char* b = static_cast<char*>(ws);
+    const int m = n / g;
+    moe::FormPArgs a = {};
+    a.x = x;
+    a.T = T; a.d = d; a.n = n; a.k = k; a.g = g; a.m = m;
+    a.mk = k < m ? k : m;
+    a.r = r;
+    a.dgate = wts[0]; a.dup = wts[1]; a.ddown = wts[2];
+    a.agate = wts[3]; a.aup = wts[4]; a.adown = wts[5];
+    a.topk_idx = topk_idx;
+    a.gbuf = reinterpret_cast<float*>(b + og);
+    a.ubuf = reinterpret_cast<float*>(b + ou);
+    a.zbuf = reinterpret_cast<float*>(b + oz);
+    a.y = y;
+    a.zero_y = zero_y ? 1 : 0;
+    a.ws = resolve(ws, L);
+    cudaError_t e = moe::launch_formp(a, moe::device_sm_count(), s);
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    return MOE_OK;
+}
+
+int deamoe_p_layer_forward(const float* x, int T, int d, int n, int k, float scale, const float* w_router,
+                           const float* bias, int experts_per_dept, int k_dept, int r, int dtype,
+                           const void* dept_gate, const void* dept_up, const void* dept_down,
+                           const void* a_gate, const void* a_up, const void* a_down, void* ws,
+                           size_t ws_bytes, int32_t* topk_idx, float* topk_w, float* y, void* stream) {
+    const char* who = "deamoe_p_layer_forward";
+    const int g = experts_per_dept;
+    const void* const wts[6] = {dept_gate, dept_up, dept_down, a_gate, a_up, a_down};
+    moe_ws_layout L;
+    size_t og, ou, oz;
+    int rc = formp_checks(x, T, d, n, k, g, r, dtype, wts, ws, ws_bytes, y, &L, &og, &ou, &oz, who);
+    if (rc) return rc;
+    const int m = n / g;
+    if (k_dept < 0 || k_dept > m || (k_dept > 0 && (long long)k > (long long)k_dept * g))
+        return fail(MOE_ERR_INVALID_ARG, "%s: k_dept=%d must be 0 (plain top-k) or in [1, %d] with k <= k_dept*g",
+                    who, k_dept, m);
     if (!w_router || !aligned16(w_router)) return fail(MOE_ERR_INVALID_ARG, "%s: w_router null or unaligned", who);
     if (!topk_idx || !topk_w) return fail(MOE_ERR_INVALID_ARG, "%s: routing outputs are null", who);
     moe::RouteArgs ra = {};
@@ -854,23 +889,22 @@ int deamoe_p_layer_forward(const float* x, int T, int d, int n, int k, float sca
     cudaStream_t s = as_stream(stream);
     cudaError_t e = moe::launch_route(ra, s);
     if (e != cudaSuccess) return cuda_fail(e, who);
-    char* b = static_cast<char*>(ws);
-    moe::FormPArgs a = {};
-    a.x = x;
-    a.T = T; a.d = d; a.n = n; a.k = k; a.g = g; a.m = m;
-    a.mk = k < m ? k : m;
-    a.r = r;
-    a.dgate = dept_gate; a.dup = dept_up; a.ddown = dept_down;
-    a.agate = a_gate; a.aup = a_up; a.adown = a_down;
-    a.topk_idx = topk_idx;
-    a.gbuf = reinterpret_cast<float*>(b + og);
-    a.ubuf = reinterpret_cast<float*>(b + ou);
-    a.zbuf = reinterpret_cast<float*>(b + oz);
-    a.y = y;
-    a.ws = ra.ws;
-    e = moe::launch_formp(a, moe::device_sm_count(), s);
-    if (e != cudaSuccess) return cuda_fail(e, who);
-    return MOE_OK;
+    return formp_launch(x, T, d, n, k, g, r, wts, topk_idx, ws, L, og, ou, oz, y, false, s, who);
+}
+
+int deamoe_p_ffn(const float* x, int T, int d, int n, int k, int experts_per_dept, int r, int dtype,
+                 const void* dept_gate, const void* dept_up, const void* dept_down, const void* a_gate,
+                 const void* a_up, const void* a_down, const int32_t* topk_idx, void* ws, size_t ws_bytes,
+                 float* y, void* stream) {
+    const char* who = "deamoe_p_ffn";
+    const int g = experts_per_dept;
+    const void* const wts[6] = {dept_gate, dept_up, dept_down, a_gate, a_up, a_down};
+    moe_ws_layout L;
+    size_t og, ou, oz;
+    int rc = formp_checks(x, T, d, n, k, g, r, dtype, wts, ws, ws_bytes, y, &L, &og, &ou, &oz, who);
+    if (rc) return rc;
+    if (!topk_idx) return fail(MOE_ERR_INVALID_ARG, "%s: topk_idx is null", who);
+    return formp_launch(x, T, d, n, k, g, r, wts, topk_idx, ws, L, og, ou, oz, y, true, as_stream(stream), who);
 }
 
 int64_t moe_unique_weight_bytes_formp(int d, int n, int r, int A_d, int A_e) {

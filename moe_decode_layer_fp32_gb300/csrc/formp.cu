@@ -82,6 +82,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) formp_kernel(FormPArgs a)
     constexpr int kNT = (NCW + 1) * 32;
     constexpr bool DOT = STAGE != kFormPDown;     // gate / up rows
     constexpr bool DOWN = STAGE != kFormPUp;      // down rows
+    // Narrow rows (the 4-warp layout): a stage carries as many whole rows as
+    // fit and the consumers take them RMAX at a time, so that each copy still
+    // moves 16 KB.  Wider rows fill a stage with RMAX rows or fewer (measured
+    // faster there: the sub-block loop costs more than it saves).
+    constexpr bool SUB = NCW <= 4;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char* ring = smem_raw;
     PSmem<NS>& sm = *reinterpret_cast<PSmem<NS>*>(smem_raw + (size_t)NS * kPStageBytes);
@@ -100,11 +105,18 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) formp_kernel(FormPArgs a)
     pdl_wait_primary();
 
     if (STAGE == kFormPUp) {
-        // the private pass adds into the assignment buffer: clear it here
+        // the private pass adds into the assignment buffer, the down pass
+        // into y (when no routing kernel cleared it): clear them here
         float4* z4 = reinterpret_cast<float4*>(a.zbuf);
         const long long n4 = (long long)a.T * a.k * a.r / 4;
         for (long long i = blockIdx.x * (long long)kNT + tid; i < n4; i += (long long)gridDim.x * kNT)
             z4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (a.zero_y) {
+            float4* y4 = reinterpret_cast<float4*>(a.y);
+            const long long m4 = (long long)a.T * a.d / 4;
+            for (long long i = blockIdx.x * (long long)kNT + tid; i < m4; i += (long long)gridDim.x * kNT)
+                y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
     const bool dept_units = STAGE != kFormPPriv;
     const int A = dept_units ? a.ws.counts[1] : a.ws.counts[0];
@@ -118,7 +130,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) formp_kernel(FormPArgs a)
 
     const int width = STAGE == kFormPPriv ? a.r : a.d;   // row length (elements)
     const int row_bytes = width * 2;
-    const int rps = min(RMAX, kPStageBytes / row_bytes);
+    const int rps = min(SUB ? kPSegMax : RMAX, kPStageBytes / row_bytes);   // rows per stage
     const int nchunks = width / 8;
 
     if (warp == NCW) {
@@ -257,17 +269,20 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) formp_kernel(FormPArgs a)
                 for (int mat = 0; mat < 2; ++mat) {
                     const int slot = it % NS;
                     if (wait_full(slot, it)) {
-                        const char* st = reinterpret_cast<const char*>(ring + (size_t)slot * kPStageBytes);
-                        float* gr = &sm.gu[mat][rb * kMT];
-                        if (mat == 0 || NX == 1) {
-                            if (mg == 1) K::template gu_any<1>(st, nr, row_bytes, coff, cval, xin[0], gr, mg, lane);
-                            else if (mg == 2) K::template gu_any<2>(st, nr, row_bytes, coff, cval, xin[0], gr, mg, lane);
-                            else K::template gu_any<4>(st, nr, row_bytes, coff, cval, xin[0], gr, mg, lane);
-                        } else {
-                            if (mg == 1) K::template gu_any<1>(st, nr, row_bytes, coff, cval, xin[NX - 1], gr, mg, lane);
-                            else if (mg == 2) K::template gu_any<2>(st, nr, row_bytes, coff, cval, xin[NX - 1], gr, mg, lane);
-                            else K::template gu_any<4>(st, nr, row_bytes, coff, cval, xin[NX - 1], gr, mg, lane);
-                        }
+                        const char* st0 = reinterpret_cast<const char*>(ring + (size_t)slot * kPStageBytes);
+                        // the stage's rows RMAX at a time against one input set
+                        auto dots = [&](const float2 (&xv)[CH][kMT][4]) {
+                            for (int sb = 0; sb < (SUB ? nr : 1); sb += RMAX) {
+                                const int ns = SUB ? min(RMAX, nr - sb) : nr;
+                                const char* st = st0 + (size_t)sb * row_bytes;
+                                float* gr = &sm.gu[mat][(rb + sb) * kMT];
+                                if (mg == 1) K::template gu_any<1>(st, ns, row_bytes, coff, cval, xv, gr, mg, lane);
+                                else if (mg == 2) K::template gu_any<2>(st, ns, row_bytes, coff, cval, xv, gr, mg, lane);
+                                else K::template gu_any<4>(st, ns, row_bytes, coff, cval, xv, gr, mg, lane);
+                            }
+                        };
+                        if (mat == 0) dots(xin[0]);
+                        else dots(xin[NX - 1]);
                         release(slot);
                     }
                     ++it;
@@ -344,11 +359,15 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) formp_kernel(FormPArgs a)
             const int nr = min(rps, s.nrows - rb);
             const int slot = it % NS;
             if (wait_full(slot, it)) {
-                const char* st = reinterpret_cast<const char*>(ring + (size_t)slot * kPStageBytes);
-                const float* hr = &sm.h[rb * kMT];
-                if (mg == 1) K::template down_any<1>(st, nr, row_bytes, coff, cval, hr, yacc);
-                else if (mg == 2) K::template down_any<2>(st, nr, row_bytes, coff, cval, hr, yacc);
-                else K::template down_any<4>(st, nr, row_bytes, coff, cval, hr, yacc);
+                const char* st0 = reinterpret_cast<const char*>(ring + (size_t)slot * kPStageBytes);
+                for (int sb = 0; sb < (SUB ? nr : 1); sb += RMAX) {
+                    const int ns = SUB ? min(RMAX, nr - sb) : nr;
+                    const char* st = st0 + (size_t)sb * row_bytes;
+                    const float* hr = &sm.h[(rb + sb) * kMT];
+                    if (mg == 1) K::template down_any<1>(st, ns, row_bytes, coff, cval, hr, yacc);
+                    else if (mg == 2) K::template down_any<2>(st, ns, row_bytes, coff, cval, hr, yacc);
+                    else K::template down_any<4>(st, ns, row_bytes, coff, cval, hr, yacc);
+                }
                 release(slot);
             }
             ++it;

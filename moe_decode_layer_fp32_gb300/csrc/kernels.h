@@ -169,7 +169,8 @@ struct FormPArgs {
     float* gbuf;             // [T*mk, r] SiLU(W_g x) per department entry
     float* ubuf;             // [T*mk, r] SiLU(W_u x)
     float* zbuf;             // [T*k, r] A_d^T Y per assignment (before SiLU)
-    float* y;                // [T, d], zeroed by the routing kernel
+    float* y;                // [T, d], zeroed by the routing kernel or, with
+    int zero_y;              //   zero_y, by the up pass
     WsPtrs ws;
 };
 cudaError_t launch_formp(const FormPArgs& a, int sms, cudaStream_t s);

@@ -380,8 +380,10 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
     const int rch = (a.d / 4 + kRouteThreads - 1) / kRouteThreads;
     const int tblocks = (a.T + 7) / 8;
     // from four token blocks on, 4 experts per block so that each activation
-    // chunk serves 4; below, one expert per block for parallelism
-    const int eb = a.n % 4 == 0 && tblocks >= 4 ? 4 : 1;
+    // chunk serves 4; below, one expert per block for parallelism, unless
+    // that would take more than one wave of blocks (a 512-thread block holds
+    // its SM's registers alone): from 256 experts on, 4 per block
+    const int eb = a.n % 4 == 0 && (tblocks >= 4 || a.n >= 256) ? 4 : 1;
     const bool grouped = a.k_dept > 0 && !a.logits_only;
     if (eb == 4) {
         if (grouped) launch_route_eb<4, true>(a, rch, a.n / 4 * tblocks, s);

@@ -211,11 +211,16 @@ def near_identity(units: int, r: int, seed: int, tensor_id: int, dtype: str,
     identity start of the form-P expert matrices (DeaMoE §3.4) with a
     perturbation standing in for training.  Drawn in fp32, rounded once."""
     out = torch.empty((units, r, r), dtype=storage_dtype(dtype), device=device)
-    eye = torch.eye(r, dtype=torch.float32, device=device)
     for u in range(units):
-        a = normal((r, r), seed, tensor_id, WEIGHT_STD, device, salt=u + 1)
-        out[u].copy_((a + eye).to(storage_dtype(dtype)))
+        out[u].copy_(near_identity_unit(u, r, seed, tensor_id, dtype, device))
     return out
+
+
+def near_identity_unit(u: int, r: int, seed: int, tensor_id: int, dtype: str, device="cpu") -> torch.Tensor:
+    """Unit ``u`` of ``near_identity`` alone (its own stream, salt = u + 1)."""
+    a = normal((r, r), seed, tensor_id, WEIGHT_STD, device, salt=u + 1)
+    a += torch.eye(r, dtype=torch.float32, device=device)
+    return a.to(storage_dtype(dtype))
 
 
 def make_layer(shape: LayerShape, seed: int, device="cpu", with_router: bool = True) -> dict:

@@ -134,3 +134,28 @@ def test_formp_rejects_bad_arguments(B):
         B.deamoe_p_layer_forward(x, s.k, 1.0, L["router"], None, s.g, 0, f32, amat, ws, idx, w, y)
     assert B.moe_formp_workspace_bytes(2, 16, 4, 1, 64) == 0
     assert B.moe_formp_workspace_bytes(2, 16, 4, 4, 40) == 0
+
+
+def test_formp_ffn_step_on_a_separate_routing(B):
+    """Routing (group-limited) and dispatch as separate calls, then the three
+    passes alone: the same output as the oracle, y overwritten."""
+    s = synth.FORMP_7B
+    T = 9
+    L = synth.make_layer(s, 11, DEV)
+    x = synth.hidden(T, s.d, 11, DEV)
+    ws = B.new_formp_workspace(T, s.n, s.k, s.g, s.I_sh)
+    idx = torch.empty((T, s.k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, s.k), device=DEV)
+    B.moe_route_topk_grouped(x, L["router"], L["bias"], s.k, s.g, s.k_dept, False, 1.0, idx, w, ws)
+    B.moe_dispatch(idx, w, s.n, s.g, ws)
+    y = torch.full((T, s.d), float("nan"), device=DEV)
+    B.deamoe_p_ffn(x, s.k, s.g, (L["dgate"], L["dup"], L["ddown"]), (L["agate"], L["aup"], L["adown"]),
+                   idx, ws, y)
+    torch.cuda.synchronize()
+    assert B.moe_read_status(ws)[0] == 0
+    oi, op, info = O.route_grouped(x, L["router"], s.k, s.g, s.k_dept, bias=L["bias"])
+    ties = H.compare_grouped_routing(idx.cpu().numpy(), w.cpu().numpy(), oi, op, info, x, L["router"], s.g,
+                                     s.k_dept, False)
+    tokens = [t for t in range(T) if t not in ties]
+    ref = oracle_formp(s, L, x, oi, op, tokens)
+    assert H.rel_err(y.cpu().numpy()[tokens], ref) <= 1e-4
