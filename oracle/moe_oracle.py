@@ -51,6 +51,9 @@ Readings where the pages are silent (each also listed in the design doc):
   (sum of the expert token counts) / n; the bias is fp32 state, updated once
   per call from fp64 arithmetic rounded to fp32 once.  With no routed token
   the imbalance ratio (0 / 0) is reported as 0 and no bias moves.
+* R10 FP8 weights: E4M3 codes with one fp32 scale per weight row (a row of a
+  gate, up or down matrix, i.e. one intermediate index of a unit); the pages
+  give the format's size only.
 """
 
 from __future__ import annotations
@@ -68,6 +71,34 @@ def bf16_bits_to_f64(u16: np.ndarray) -> np.ndarray:
     """Exact value of bf16 bit patterns: the top half of an fp32 word."""
     u32 = u16.astype(np.uint32) << np.uint32(16)
     return u32.view(np.float32).astype(np.float64)
+
+
+def e4m3_bits_to_f64(u8: np.ndarray) -> np.ndarray:
+    """Exact value of FP8 E4M3 codes (the "fn" layout: 1 sign bit, 4 exponent
+    bits with bias 7, 3 mantissa bits; no infinities; S.1111.111 is NaN).
+    Normal: (-1)^s 2^(e-7) (1 + m/8); subnormal (e = 0): (-1)^s 2^-6 (m/8)."""
+    b = np.asarray(u8, dtype=np.uint8).astype(np.int64)
+    sgn = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = (b & 0x7).astype(np.float64)
+    mag = np.where(e == 0, np.ldexp(m / 8.0, -6), np.ldexp(1.0 + m / 8.0, (e - 7).astype(np.int64)))
+    out = sgn * mag
+    return np.where((b & 0x7F) == 0x7F, np.nan, out)
+
+
+def dequant_rows_e4m3(codes, row_scale) -> np.ndarray:
+    """FP8 weights with one fp32 scale per row (R10): ``w[..., r, c] =
+    row_scale[..., r] * e4m3(codes[..., r, c])``, exactly, in fp64."""
+    try:
+        import torch
+        if isinstance(codes, torch.Tensor):
+            codes = codes.detach().cpu().contiguous().view(torch.uint8).numpy()
+        if isinstance(row_scale, torch.Tensor):
+            row_scale = row_scale.detach().cpu().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    vals = e4m3_bits_to_f64(codes)
+    return vals * np.asarray(row_scale, np.float64)[..., None]
 
 
 def to_f64(w) -> np.ndarray:

@@ -683,3 +683,35 @@ def test_unique_bytes_matches_touched_tensors():
     # vanilla with a shared expert, bf16
     Uv = O.unique_bytes_vanilla(2048, 128, 768, 256, 10, 2)
     assert Uv == 4 * 2048 * 128 + 2 * 3 * 2048 * (10 * 768 + 256)
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) weights with per-row scales
+# ---------------------------------------------------------------------------
+
+
+def test_e4m3_decode_hand_values():
+    # worked from the layout: sign | 4 exponent bits (bias 7) | 3 mantissa bits
+    codes = np.array([0x00, 0x80, 0x38, 0xB8, 0x7E, 0xFE, 0x01, 0x07, 0x08, 0x3C, 0x40, 0x30],
+                     np.uint8)
+    want = [0.0, -0.0, 1.0, -1.0, 448.0, -448.0, 2.0 ** -9, 7 * 2.0 ** -9, 2.0 ** -6, 1.5, 2.0, 0.5]
+    got = O.e4m3_bits_to_f64(codes)
+    np.testing.assert_array_equal(got, want)
+    assert np.signbit(got[1]) and not np.signbit(got[0])
+    assert np.isnan(O.e4m3_bits_to_f64(np.array([0x7F, 0xFF], np.uint8))).all()
+
+
+def test_e4m3_decode_matches_library_for_every_code():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    lib = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    mine = O.e4m3_bits_to_f64(codes.numpy())
+    np.testing.assert_array_equal(np.isnan(mine), np.isnan(lib))
+    ok = ~np.isnan(lib)
+    np.testing.assert_array_equal(mine[ok], lib[ok])
+
+
+def test_dequant_rows_scales_each_row():
+    codes = np.array([[[0x38, 0x40], [0xB8, 0x30]]], np.uint8)      # 1, 2 / -1, 0.5
+    scale = np.array([[0.25, 3.0]], np.float32)
+    np.testing.assert_array_equal(O.dequant_rows_e4m3(codes, scale),
+                                  [[[0.25, 0.5], [-3.0, 1.5]]])
