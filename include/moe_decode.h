@@ -55,6 +55,7 @@ extern "C" {
 
 #define MOE_DTYPE_F32  0
 #define MOE_DTYPE_BF16 1
+#define MOE_DTYPE_FP8_E4M3 2  /* E4M3 codes + one fp32 scale per row: the *_fp8 calls */
 
 /* Output modes of the FFN steps. */
 #define MOE_OUT_ROWS  0  /* one unweighted row per (unit, token); moe_combine sums them */
@@ -359,6 +360,59 @@ int deamoe_layer_forward(const float* x, int T, int d, int n, int k, float scale
                          float* y, void* stream);
 
 /* ------------------------------------------------------------------------- */
+/* FP8 (E4M3) expert weights                                                 */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * The FFN steps and layer calls above with FP8 E4M3 weights and one fp32
+ * scale per weight row.  The pages count expert weights in FP8 ([DeaMoE] §1:
+ * a DeepSeek-V3 expert is about 44 MB of FP8 weights) and note that
+ * quantised weights change the model's numbers ([MoE-inf], quantisation);
+ * the scale granularity (one per row of each gate / up / down matrix, i.e.
+ * per intermediate index of a unit) is this library's choice.
+ *   Weight tensors: E4M3 codes (1 byte) in the layouts of the bf16 calls.
+ *   row_scales: a host array of device pointers to float scales, three per
+ *     class -- gate, up, down -- each [units * rows] (row r of unit u at
+ *     u * rows + r): the value of a weight is scale[row] * e4m3(code).
+ *     moe_*_vanilla_fp8 / moe_layer_forward_fp8: [0..2] the experts,
+ *     [3..5] the shared expert (ignored when I_s == 0);
+ *     deamoe_*_fp8: [0..2] the departments, [3..5] the private rows
+ *     (ignored when I_pr == 0), [6..8] the shared expert (ignored when
+ *     I_s == 0).
+ * Other arguments, limits and results as for the bf16 calls, except that
+ * the CUDA-core kernel always runs (no tensor-core path for FP8).  The
+ * bf16 / fp32 calls reject dtype MOE_DTYPE_FP8_E4M3.
+ */
+int moe_ffn_vanilla_fp8(const float* x, int T, int d, int n, int k, int I,
+                        const void* w_gate, const void* w_up, const void* w_down, int I_s,
+                        const void* s_gate, const void* s_up, const void* s_down,
+                        const float* const row_scales[6], const void* ws, size_t ws_bytes,
+                        int out_mode, float* out, void* stream);
+
+int deamoe_ffn_fp8(const float* x, int T, int d, int n, int k, int experts_per_dept, int I_sh,
+                   int I_pr, const void* dept_gate, const void* dept_up, const void* dept_down,
+                   const void* priv_gate, const void* priv_up, const void* priv_down, int I_s,
+                   const void* s_gate, const void* s_up, const void* s_down,
+                   const float* const row_scales[9], const void* ws, size_t ws_bytes,
+                   int out_mode, float* out, void* stream);
+
+int moe_layer_forward_fp8(const float* x, int T, int d, int n, int k, float scale,
+                          const float* w_router, const float* bias, int I,
+                          const void* w_gate, const void* w_up, const void* w_down, int I_s,
+                          const void* s_gate, const void* s_up, const void* s_down,
+                          const float* const row_scales[6], void* ws, size_t ws_bytes,
+                          int32_t* topk_idx, float* topk_w, float* y, void* stream);
+
+int deamoe_layer_forward_fp8(const float* x, int T, int d, int n, int k, float scale,
+                             const float* w_router, const float* bias, int experts_per_dept,
+                             int I_sh, int I_pr, const void* dept_gate, const void* dept_up,
+                             const void* dept_down, const void* priv_gate, const void* priv_up,
+                             const void* priv_down, int I_s, const void* s_gate, const void* s_up,
+                             const void* s_down, const float* const row_scales[9], void* ws,
+                             size_t ws_bytes, int32_t* topk_idx, float* topk_w, float* y,
+                             void* stream);
+
+/* ------------------------------------------------------------------------- */
 /* DeaMoE layer in the paper's parameterisation ("form P")                   */
 /* ------------------------------------------------------------------------- */
 
@@ -449,9 +503,11 @@ int moe_bias_update(const int32_t* counts, int n, float gamma, int rule,
 /*
  * Weight bytes one step must read at least once ("unique weight bytes"): the
  * fp32 router, the shared expert, and each active unit's three matrices once.
- *   vanilla: 4*d*n + bw*3*d*(A_e*I + I_s)
- *   DeaMoE:  4*d*n + bw*3*d*(A_d*I_sh + A_e*I_pr + I_s)
- * where bw = 2 (bf16) or 4 (fp32).  Returns -1 on invalid arguments.
+ *   vanilla: 4*d*n + R*(A_e*I + I_s)
+ *   DeaMoE:  4*d*n + R*(A_d*I_sh + A_e*I_pr + I_s)
+ * where R, the bytes of one intermediate row of a unit, is 3*d*bw with
+ * bw = 2 (bf16) or 4 (fp32), and 3*(d + 4) for FP8 (codes and the three
+ * fp32 row scales).  Returns -1 on invalid arguments.
  */
 int64_t moe_unique_weight_bytes_vanilla(int d, int n, int I, int I_s, int dtype, int A_e);
 int64_t moe_unique_weight_bytes_deamoe(int d, int n, int I_sh, int I_pr, int I_s,

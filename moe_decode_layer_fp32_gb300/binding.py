@@ -19,6 +19,7 @@ LIB_PATH = os.environ.get("MOE_GB300_LIB") or os.path.join(
 MOE_OK = 0
 MOE_DTYPE_F32 = 0
 MOE_DTYPE_BF16 = 1
+MOE_DTYPE_FP8_E4M3 = 2
 MOE_OUT_ROWS = 0
 MOE_OUT_ACCUM = 1
 
@@ -55,6 +56,13 @@ _SIGS = {
     "moe_route_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _SZ, _P]),
     "moe_route_topk_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
     "moe_bias_update": (_I, [_P, _I, _F, _I, _P, _P, _P]),
+    "moe_ffn_vanilla_fp8": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P, _SZ, _I, _P, _P]),
+    "deamoe_ffn_fp8": (_I, [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P,
+                            _SZ, _I, _P, _P]),
+    "moe_layer_forward_fp8": (_I, [_P, _I, _I, _I, _I, _F, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P,
+                                   _SZ, _P, _P, _P, _P]),
+    "deamoe_layer_forward_fp8": (_I, [_P, _I, _I, _I, _I, _F, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P,
+                                      _I, _P, _P, _P, _P, _P, _SZ, _P, _P, _P, _P]),
     "moe_formp_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "deamoe_p_layer_forward": (_I, [_P, _I, _I, _I, _I, _F, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P,
                                     _P, _P, _P, _SZ, _P, _P, _P, _P]),
@@ -121,7 +129,17 @@ def _dtype_code(t) -> int:
         return MOE_DTYPE_BF16
     if t.dtype == torch.float32:
         return MOE_DTYPE_F32
+    if t.dtype == torch.float8_e4m3fn:
+        return MOE_DTYPE_FP8_E4M3
     raise ValueError(f"unsupported weight dtype {t.dtype}")
+
+
+def _scales(scales, count: int):
+    """Host array of device pointers to the FP8 row scales (None entries for
+    absent classes)."""
+    if scales is None or len(scales) != count:
+        raise ValueError(f"FP8 weights need {count} row-scale tensors (None where a class is absent)")
+    return (C.c_void_p * count)(*[_ptr(t) for t in scales])
 
 
 def moe_set_tc_min_tokens(min_tokens: int) -> int:
@@ -225,20 +243,27 @@ def moe_rows_count(T: int, n: int, k: int, experts_per_dept: int, has_shared: bo
     return r
 
 
-def moe_ffn_vanilla(x, k: int, w_gate, w_up, w_down, shared, ws, out_mode: int, out):
-    """``shared`` = (s_gate, s_up, s_down) or None."""
+def moe_ffn_vanilla(x, k: int, w_gate, w_up, w_down, shared, ws, out_mode: int, out, scales=None):
+    """``shared`` = (s_gate, s_up, s_down) or None; FP8 weights: ``scales`` =
+    the row scales (gate, up, down of the experts, then of the shared expert)."""
     T, d = x.shape
     n, I, _ = w_gate.shape
     sg, su, sd = shared if shared is not None else (None, None, None)
     I_s = sg.shape[0] if sg is not None else 0
+    if _dtype_code(w_gate) == MOE_DTYPE_FP8_E4M3:
+        _check("moe_ffn_vanilla_fp8", lib().moe_ffn_vanilla_fp8(
+            _ptr(x), T, d, n, k, I, _ptr(w_gate), _ptr(w_up), _ptr(w_down), I_s, _ptr(sg), _ptr(su),
+            _ptr(sd), _scales(scales, 6), _ptr(ws), ws.numel(), out_mode, _ptr(out), _stream()))
+        return
     _check("moe_ffn_vanilla", lib().moe_ffn_vanilla(
         _ptr(x), T, d, n, k, I, _dtype_code(w_gate), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
         I_s, _ptr(sg), _ptr(su), _ptr(sd), _ptr(ws), ws.numel(), out_mode, _ptr(out), _stream()))
 
 
-def deamoe_ffn(x, k: int, experts_per_dept: int, dept, priv, shared, ws, out_mode: int, out):
+def deamoe_ffn(x, k: int, experts_per_dept: int, dept, priv, shared, ws, out_mode: int, out, scales=None):
     """``dept`` = (gate, up, down) [m, I_sh, d]; ``priv`` = (gate, up, down)
-    [n, I_pr, d] or None; ``shared`` = (gate, up, down) [I_s, d] or None."""
+    [n, I_pr, d] or None; ``shared`` = (gate, up, down) [I_s, d] or None; FP8
+    weights: ``scales`` = 9 row-scale tensors (departments, private, shared)."""
     T, d = x.shape
     m, I_sh, _ = dept[0].shape
     n = m * experts_per_dept
@@ -246,6 +271,12 @@ def deamoe_ffn(x, k: int, experts_per_dept: int, dept, priv, shared, ws, out_mod
     I_pr = pg.shape[1] if pg is not None else 0
     sg, su, sd = shared if shared is not None else (None, None, None)
     I_s = sg.shape[0] if sg is not None else 0
+    if _dtype_code(dept[0]) == MOE_DTYPE_FP8_E4M3:
+        _check("deamoe_ffn_fp8", lib().deamoe_ffn_fp8(
+            _ptr(x), T, d, n, k, experts_per_dept, I_sh, I_pr, _ptr(dept[0]), _ptr(dept[1]), _ptr(dept[2]),
+            _ptr(pg), _ptr(pu), _ptr(pd), I_s, _ptr(sg), _ptr(su), _ptr(sd), _scales(scales, 9), _ptr(ws),
+            ws.numel(), out_mode, _ptr(out), _stream()))
+        return
     _check("deamoe_ffn", lib().deamoe_ffn(
         _ptr(x), T, d, n, k, experts_per_dept, I_sh, I_pr, _dtype_code(dept[0]),
         _ptr(dept[0]), _ptr(dept[1]), _ptr(dept[2]), _ptr(pg), _ptr(pu), _ptr(pd),
@@ -260,11 +291,17 @@ def moe_combine(rows, T: int, n: int, k: int, experts_per_dept: int, has_shared:
 
 
 def moe_layer_forward(x, k: int, scale: float, w_router, bias, w_gate, w_up, w_down, shared,
-                      ws, topk_idx, topk_w, y):
+                      ws, topk_idx, topk_w, y, scales=None):
     T, d = x.shape
     n, I, _ = w_gate.shape
     sg, su, sd = shared if shared is not None else (None, None, None)
     I_s = sg.shape[0] if sg is not None else 0
+    if _dtype_code(w_gate) == MOE_DTYPE_FP8_E4M3:
+        _check("moe_layer_forward_fp8", lib().moe_layer_forward_fp8(
+            _ptr(x), T, d, n, k, scale, _ptr(w_router), _ptr(bias), I, _ptr(w_gate), _ptr(w_up),
+            _ptr(w_down), I_s, _ptr(sg), _ptr(su), _ptr(sd), _scales(scales, 6), _ptr(ws), ws.numel(),
+            _ptr(topk_idx), _ptr(topk_w), _ptr(y), _stream()))
+        return
     _check("moe_layer_forward", lib().moe_layer_forward(
         _ptr(x), T, d, n, k, scale, _ptr(w_router), _ptr(bias), I, _dtype_code(w_gate),
         _ptr(w_gate), _ptr(w_up), _ptr(w_down), I_s, _ptr(sg), _ptr(su), _ptr(sd),
@@ -272,7 +309,7 @@ def moe_layer_forward(x, k: int, scale: float, w_router, bias, w_gate, w_up, w_d
 
 
 def deamoe_layer_forward(x, k: int, scale: float, w_router, bias, experts_per_dept: int, dept,
-                         priv, shared, ws, topk_idx, topk_w, y):
+                         priv, shared, ws, topk_idx, topk_w, y, scales=None):
     T, d = x.shape
     n = w_router.shape[0]
     I_sh = dept[0].shape[1]
@@ -280,6 +317,13 @@ def deamoe_layer_forward(x, k: int, scale: float, w_router, bias, experts_per_de
     I_pr = pg.shape[1] if pg is not None else 0
     sg, su, sd = shared if shared is not None else (None, None, None)
     I_s = sg.shape[0] if sg is not None else 0
+    if _dtype_code(dept[0]) == MOE_DTYPE_FP8_E4M3:
+        _check("deamoe_layer_forward_fp8", lib().deamoe_layer_forward_fp8(
+            _ptr(x), T, d, n, k, scale, _ptr(w_router), _ptr(bias), experts_per_dept, I_sh, I_pr,
+            _ptr(dept[0]), _ptr(dept[1]), _ptr(dept[2]), _ptr(pg), _ptr(pu), _ptr(pd), I_s, _ptr(sg),
+            _ptr(su), _ptr(sd), _scales(scales, 9), _ptr(ws), ws.numel(), _ptr(topk_idx), _ptr(topk_w),
+            _ptr(y), _stream()))
+        return
     _check("deamoe_layer_forward", lib().deamoe_layer_forward(
         _ptr(x), T, d, n, k, scale, _ptr(w_router), _ptr(bias), experts_per_dept, I_sh, I_pr,
         _dtype_code(dept[0]), _ptr(dept[0]), _ptr(dept[1]), _ptr(dept[2]), _ptr(pg), _ptr(pu),

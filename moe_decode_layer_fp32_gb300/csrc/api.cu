@@ -122,7 +122,14 @@ int check_ws(const void* ws, size_t ws_bytes, int T, int n, int k, int g, moe_ws
     return MOE_OK;
 }
 
-int weight_bytes(int dtype) { return dtype == MOE_DTYPE_BF16 ? 2 : dtype == MOE_DTYPE_F32 ? 4 : 0; }
+int weight_bytes(int dtype) {
+    return dtype == MOE_DTYPE_BF16 ? 2 : dtype == MOE_DTYPE_F32 ? 4 : dtype == MOE_DTYPE_FP8_E4M3 ? 1 : 0;
+}
+// Bytes of one intermediate row of a unit (gate, up and down rows), FP8 row
+// scales included.
+long long unit_row_bytes(int d, int dtype) {
+    return 3LL * d * weight_bytes(dtype) + (dtype == MOE_DTYPE_FP8_E4M3 ? 3 * 4 : 0);
+}
 
 int check_hidden(const float* x, int d, const char* who) {
     if (!x || !aligned16(x)) return fail(MOE_ERR_INVALID_ARG, "%s: x null or unaligned", who);
@@ -548,6 +555,33 @@ int64_t moe_rows_count(int T, int n, int k, int experts_per_dept, int has_shared
     return rows_count(T, n, k, experts_per_dept, has_shared);
 }
 
+// FP8 weights: the row scales of every class, in the order the *_fp8 calls
+// take them (the main class -- experts or departments --, the private rows,
+// then the shared expert); nsets is the number of triples.  Other dtypes
+// take none.
+static int attach_row_scales(moe::FfnArgs& a, const float* const* sc, int nsets, const char* who) {
+    if (a.dtype != MOE_DTYPE_FP8_E4M3) {
+        if (sc) return fail(MOE_ERR_INVALID_ARG, "%s: row scales are for FP8 weights only", who);
+        return MOE_OK;
+    }
+    if (!sc) return fail(MOE_ERR_INVALID_ARG, "%s: FP8 weights need the *_fp8 call and its row scales", who);
+    int next = 0;
+    for (int c = 0; c < a.ncls; ++c) {
+        moe::UnitClass& uc = a.cls[c];
+        const int set = uc.kind == moe::kUnitShared ? nsets - 1 : next++;
+        const float* g = sc[3 * set];
+        const float* u = sc[3 * set + 1];
+        const float* dn = sc[3 * set + 2];
+        if (!g || !u || !dn || (reinterpret_cast<uintptr_t>(g) | reinterpret_cast<uintptr_t>(u) |
+                                reinterpret_cast<uintptr_t>(dn)) & 3u)
+            return fail(MOE_ERR_INVALID_ARG, "%s: row scales of set %d null or unaligned", who, set);
+        uc.sc_gate = g;
+        uc.sc_up = u;
+        uc.sc_down = dn;
+    }
+    return MOE_OK;
+}
+
 static int setup_vanilla(moe::FfnArgs& a, const float* x, int T, int d, int n, int k, int I,
                          int dtype, const void* w_gate, const void* w_up, const void* w_down,
                          int I_s, const void* s_gate, const void* s_up, const void* s_down,
@@ -574,15 +608,15 @@ static int setup_vanilla(moe::FfnArgs& a, const float* x, int T, int d, int n, i
     return MOE_OK;
 }
 
-int moe_ffn_vanilla(const float* x, int T, int d, int n, int k, int I, int dtype,
+static int ffn_vanilla_impl(const float* const* sc, const char* who, const float* x, int T, int d, int n, int k, int I, int dtype,
                     const void* w_gate, const void* w_up, const void* w_down, int I_s,
                     const void* s_gate, const void* s_up, const void* s_down, const void* ws,
                     size_t ws_bytes, int out_mode, float* out, void* stream) {
-    const char* who = "moe_ffn_vanilla";
     moe::FfnArgs a;
     int rc = setup_vanilla(a, x, T, d, n, k, I, dtype, w_gate, w_up, w_down, I_s, s_gate, s_up,
                            s_down, ws, ws_bytes, out_mode, out, who);
     if (rc) return rc;
+    if ((rc = attach_row_scales(a, sc, 2, who))) return rc;
     moe::TcArgs t;
     const bool tc = prepare_tc(a, T, &t);
     return run_ffn(a, T, n, k, 1, I_s > 0, tc, t, false, stream, who);
@@ -619,18 +653,18 @@ static int setup_deamoe(moe::FfnArgs& a, const float* x, int T, int d, int n, in
     return MOE_OK;
 }
 
-int deamoe_ffn(const float* x, int T, int d, int n, int k, int experts_per_dept, int I_sh,
+static int deamoe_ffn_impl(const float* const* sc, const char* who, const float* x, int T, int d, int n, int k, int experts_per_dept, int I_sh,
                int I_pr, int dtype, const void* dept_gate, const void* dept_up,
                const void* dept_down, const void* priv_gate, const void* priv_up,
                const void* priv_down, int I_s, const void* s_gate, const void* s_up,
                const void* s_down, const void* ws, size_t ws_bytes, int out_mode, float* out,
                void* stream) {
-    const char* who = "deamoe_ffn";
     moe::FfnArgs a;
     int rc = setup_deamoe(a, x, T, d, n, k, experts_per_dept, I_sh, I_pr, dtype, dept_gate, dept_up,
                           dept_down, priv_gate, priv_up, priv_down, I_s, s_gate, s_up, s_down, ws,
                           ws_bytes, out_mode, out, who);
     if (rc) return rc;
+    if ((rc = attach_row_scales(a, sc, 3, who))) return rc;
     moe::TcArgs t;
     const bool tc = prepare_tc(a, T, &t);
     return run_ffn(a, T, n, k, experts_per_dept, I_s > 0, tc, t, false, stream, who);
@@ -737,16 +771,16 @@ static int layer_route(const float* x, int T, int d, int n, int k, float scale, 
     return MOE_OK;
 }
 
-int moe_layer_forward(const float* x, int T, int d, int n, int k, float scale,
+static int layer_forward_impl(const float* const* sc, const char* who, const float* x, int T, int d, int n, int k, float scale,
                       const float* w_router, const float* bias, int I, int dtype,
                       const void* w_gate, const void* w_up, const void* w_down, int I_s,
                       const void* s_gate, const void* s_up, const void* s_down, void* ws,
                       size_t ws_bytes, int32_t* topk_idx, float* topk_w, float* y, void* stream) {
-    const char* who = "moe_layer_forward";
     moe::FfnArgs a;
     int rc = setup_vanilla(a, x, T, d, n, k, I, dtype, w_gate, w_up, w_down, I_s, s_gate, s_up,
                            s_down, ws, ws_bytes, MOE_OUT_ACCUM, y, who);
     if (rc) return rc;
+    if ((rc = attach_row_scales(a, sc, 2, who))) return rc;
     moe_ws_layout L;
     layout_of(T, n, k, 1, &L);
     moe::TcArgs t;
@@ -758,19 +792,19 @@ int moe_layer_forward(const float* x, int T, int d, int n, int k, float scale,
     return layer_ffn(a, T, n, k, 1, I_s > 0, tc, t, path, stream, who);
 }
 
-int deamoe_layer_forward(const float* x, int T, int d, int n, int k, float scale,
+static int deamoe_layer_forward_impl(const float* const* sc, const char* who, const float* x, int T, int d, int n, int k, float scale,
                          const float* w_router, const float* bias, int experts_per_dept, int I_sh,
                          int I_pr, int dtype, const void* dept_gate, const void* dept_up,
                          const void* dept_down, const void* priv_gate, const void* priv_up,
                          const void* priv_down, int I_s, const void* s_gate, const void* s_up,
                          const void* s_down, void* ws, size_t ws_bytes, int32_t* topk_idx,
                          float* topk_w, float* y, void* stream) {
-    const char* who = "deamoe_layer_forward";
     moe::FfnArgs a;
     int rc = setup_deamoe(a, x, T, d, n, k, experts_per_dept, I_sh, I_pr, dtype, dept_gate, dept_up,
                           dept_down, priv_gate, priv_up, priv_down, I_s, s_gate, s_up, s_down, ws,
                           ws_bytes, MOE_OUT_ACCUM, y, who);
     if (rc) return rc;
+    if ((rc = attach_row_scales(a, sc, 3, who))) return rc;
     moe_ws_layout L;
     layout_of(T, n, k, experts_per_dept, &L);
     moe::TcArgs t;
@@ -780,6 +814,99 @@ int deamoe_layer_forward(const float* x, int T, int d, int n, int k, float scale
                           topk_w, y, tc, path != kLayerGlobal, a, stream, who)))
         return rc;
     return layer_ffn(a, T, n, k, experts_per_dept, I_s > 0, tc, t, path, stream, who);
+}
+
+int moe_ffn_vanilla(const float* x, int T, int d, int n, int k, int I, int dtype,
+                    const void* w_gate, const void* w_up, const void* w_down, int I_s,
+                    const void* s_gate, const void* s_up, const void* s_down, const void* ws,
+                    size_t ws_bytes, int out_mode, float* out, void* stream) {
+    return ffn_vanilla_impl(nullptr, "moe_ffn_vanilla", x, T, d, n, k, I, dtype, w_gate, w_up, w_down, I_s,
+                            s_gate, s_up, s_down, ws, ws_bytes, out_mode, out, stream);
+}
+
+int moe_ffn_vanilla_fp8(const float* x, int T, int d, int n, int k, int I, const void* w_gate,
+                        const void* w_up, const void* w_down, int I_s, const void* s_gate,
+                        const void* s_up, const void* s_down, const float* const row_scales[6],
+                        const void* ws, size_t ws_bytes, int out_mode, float* out, void* stream) {
+    const char* who = "moe_ffn_vanilla_fp8";
+    if (!row_scales) return fail(MOE_ERR_INVALID_ARG, "%s: row_scales is null", who);
+    return ffn_vanilla_impl(row_scales, who, x, T, d, n, k, I, MOE_DTYPE_FP8_E4M3, w_gate, w_up, w_down, I_s,
+                            s_gate, s_up, s_down, ws, ws_bytes, out_mode, out, stream);
+}
+
+int deamoe_ffn(const float* x, int T, int d, int n, int k, int experts_per_dept, int I_sh,
+               int I_pr, int dtype, const void* dept_gate, const void* dept_up,
+               const void* dept_down, const void* priv_gate, const void* priv_up,
+               const void* priv_down, int I_s, const void* s_gate, const void* s_up,
+               const void* s_down, const void* ws, size_t ws_bytes, int out_mode, float* out,
+               void* stream) {
+    return deamoe_ffn_impl(nullptr, "deamoe_ffn", x, T, d, n, k, experts_per_dept, I_sh, I_pr, dtype, dept_gate,
+                           dept_up, dept_down, priv_gate, priv_up, priv_down, I_s, s_gate, s_up, s_down, ws,
+                           ws_bytes, out_mode, out, stream);
+}
+
+int deamoe_ffn_fp8(const float* x, int T, int d, int n, int k, int experts_per_dept, int I_sh,
+                   int I_pr, const void* dept_gate, const void* dept_up, const void* dept_down,
+                   const void* priv_gate, const void* priv_up, const void* priv_down, int I_s,
+                   const void* s_gate, const void* s_up, const void* s_down,
+                   const float* const row_scales[9], const void* ws, size_t ws_bytes, int out_mode,
+                   float* out, void* stream) {
+    const char* who = "deamoe_ffn_fp8";
+    if (!row_scales) return fail(MOE_ERR_INVALID_ARG, "%s: row_scales is null", who);
+    return deamoe_ffn_impl(row_scales, who, x, T, d, n, k, experts_per_dept, I_sh, I_pr, MOE_DTYPE_FP8_E4M3,
+                           dept_gate, dept_up, dept_down, priv_gate, priv_up, priv_down, I_s, s_gate, s_up,
+                           s_down, ws, ws_bytes, out_mode, out, stream);
+}
+
+int moe_layer_forward(const float* x, int T, int d, int n, int k, float scale,
+                      const float* w_router, const float* bias, int I, int dtype,
+                      const void* w_gate, const void* w_up, const void* w_down, int I_s,
+                      const void* s_gate, const void* s_up, const void* s_down, void* ws,
+                      size_t ws_bytes, int32_t* topk_idx, float* topk_w, float* y, void* stream) {
+    return layer_forward_impl(nullptr, "moe_layer_forward", x, T, d, n, k, scale, w_router, bias, I, dtype,
+                              w_gate, w_up, w_down, I_s, s_gate, s_up, s_down, ws, ws_bytes, topk_idx, topk_w,
+                              y, stream);
+}
+
+int moe_layer_forward_fp8(const float* x, int T, int d, int n, int k, float scale,
+                          const float* w_router, const float* bias, int I, const void* w_gate,
+                          const void* w_up, const void* w_down, int I_s, const void* s_gate,
+                          const void* s_up, const void* s_down, const float* const row_scales[6],
+                          void* ws, size_t ws_bytes, int32_t* topk_idx, float* topk_w, float* y,
+                          void* stream) {
+    const char* who = "moe_layer_forward_fp8";
+    if (!row_scales) return fail(MOE_ERR_INVALID_ARG, "%s: row_scales is null", who);
+    return layer_forward_impl(row_scales, who, x, T, d, n, k, scale, w_router, bias, I, MOE_DTYPE_FP8_E4M3,
+                              w_gate, w_up, w_down, I_s, s_gate, s_up, s_down, ws, ws_bytes, topk_idx, topk_w,
+                              y, stream);
+}
+
+int deamoe_layer_forward(const float* x, int T, int d, int n, int k, float scale,
+                         const float* w_router, const float* bias, int experts_per_dept, int I_sh,
+                         int I_pr, int dtype, const void* dept_gate, const void* dept_up,
+                         const void* dept_down, const void* priv_gate, const void* priv_up,
+                         const void* priv_down, int I_s, const void* s_gate, const void* s_up,
+                         const void* s_down, void* ws, size_t ws_bytes, int32_t* topk_idx,
+                         float* topk_w, float* y, void* stream) {
+    return deamoe_layer_forward_impl(nullptr, "deamoe_layer_forward", x, T, d, n, k, scale, w_router, bias,
+                                     experts_per_dept, I_sh, I_pr, dtype, dept_gate, dept_up, dept_down,
+                                     priv_gate, priv_up, priv_down, I_s, s_gate, s_up, s_down, ws, ws_bytes,
+                                     topk_idx, topk_w, y, stream);
+}
+
+int deamoe_layer_forward_fp8(const float* x, int T, int d, int n, int k, float scale,
+                             const float* w_router, const float* bias, int experts_per_dept, int I_sh,
+                             int I_pr, const void* dept_gate, const void* dept_up, const void* dept_down,
+                             const void* priv_gate, const void* priv_up, const void* priv_down, int I_s,
+                             const void* s_gate, const void* s_up, const void* s_down,
+                             const float* const row_scales[9], void* ws, size_t ws_bytes,
+                             int32_t* topk_idx, float* topk_w, float* y, void* stream) {
+    const char* who = "deamoe_layer_forward_fp8";
+    if (!row_scales) return fail(MOE_ERR_INVALID_ARG, "%s: row_scales is null", who);
+    return deamoe_layer_forward_impl(row_scales, who, x, T, d, n, k, scale, w_router, bias, experts_per_dept,
+                                     I_sh, I_pr, MOE_DTYPE_FP8_E4M3, dept_gate, dept_up, dept_down, priv_gate,
+                                     priv_up, priv_down, I_s, s_gate, s_up, s_down, ws, ws_bytes, topk_idx,
+                                     topk_w, y, stream);
 }
 
 // Form-P scratch after the standard layout: G and U [T*min(k,m), r], then
@@ -915,7 +1042,7 @@ int64_t moe_unique_weight_bytes_formp(int d, int n, int r, int A_d, int A_e) {
 int64_t moe_unique_weight_bytes_vanilla(int d, int n, int I, int I_s, int dtype, int A_e) {
     const int bw = weight_bytes(dtype);
     if (d <= 0 || n <= 0 || I < 0 || I_s < 0 || bw == 0 || A_e < 0 || A_e > n) return -1;
-    return 4LL * d * n + (int64_t)bw * 3 * d * ((int64_t)A_e * I + I_s);
+    return 4LL * d * n + unit_row_bytes(d, dtype) * ((int64_t)A_e * I + I_s);
 }
 
 int64_t moe_unique_weight_bytes_deamoe(int d, int n, int I_sh, int I_pr, int I_s, int dtype,
@@ -924,7 +1051,7 @@ int64_t moe_unique_weight_bytes_deamoe(int d, int n, int I_sh, int I_pr, int I_s
     if (d <= 0 || n <= 0 || I_sh < 0 || I_pr < 0 || I_s < 0 || bw == 0 || A_d < 0 || A_e < 0 ||
         A_e > n)
         return -1;
-    return 4LL * d * n + (int64_t)bw * 3 * d * ((int64_t)A_d * I_sh + (int64_t)A_e * I_pr + I_s);
+    return 4LL * d * n + unit_row_bytes(d, dtype) * ((int64_t)A_d * I_sh + (int64_t)A_e * I_pr + I_s);
 }
 
 }  // extern "C"

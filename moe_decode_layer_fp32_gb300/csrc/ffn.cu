@@ -477,7 +477,16 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
             const int m = i & (kMT - 1);
             float hv = 0.0f;
             if (m < mg) {
-                hv = silu_f(sm.gu[0][i]) * sm.gu[1][i];
+                if constexpr (K::kBw == 1) {
+                    // FP8 rows: the gate and up dot products and the down row
+                    // carry the rows' scales
+                    const UnitClass& uc = a.cls[s.cls];
+                    const size_t ri = (size_t)rec.x * uc.rows + s.row0 + i / kMT;
+                    hv = silu_f(__ldg(uc.sc_gate + ri) * sm.gu[0][i]) * (__ldg(uc.sc_up + ri) * sm.gu[1][i]) *
+                         __ldg(uc.sc_down + ri);
+                } else {
+                    hv = silu_f(sm.gu[0][i]) * sm.gu[1][i];
+                }
                 if (a.out_mode == MOE_OUT_ACCUM)
                     hv *= m == 0 ? wt[0] : m == 1 ? wt[1] : m == 2 ? wt[2] : wt[3];
             }
@@ -656,6 +665,10 @@ auto with_ffn_cfg(const FfnArgs& a, F f) {
     if (a.dtype == MOE_DTYPE_BF16) {
         if (a.d <= 2048) return f(FfnCfg<__nv_bfloat16, MOE_CC_NCW, MOE_CC_CH, MOE_CC_RMAX, MOE_CC_CPS>{});
         return f(FfnCfg<__nv_bfloat16, 15, 2, 1, 1>{});
+    }
+    if (a.dtype == MOE_DTYPE_FP8_E4M3) {
+        if (a.d <= 2048) return f(FfnCfg<__nv_fp8_e4m3, 8, 1, 4, 2>{});
+        return f(FfnCfg<__nv_fp8_e4m3, 15, 2, 2, 1>{});
     }
     if (a.d <= 1024) return f(FfnCfg<float, 4, 1, 8, 1>{});
     return f(FfnCfg<float, 15, 2, 1, 1>{});

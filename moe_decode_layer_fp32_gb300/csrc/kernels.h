@@ -52,6 +52,11 @@ struct UnitClass {
     const void* w_down;
     int rows;       // intermediate rows of one unit
     int kind;       // UnitKind
+    // FP8 weights: one fp32 scale per row, [units * rows] per matrix (null
+    // for bf16 / fp32 weights)
+    const float* sc_gate;
+    const float* sc_up;
+    const float* sc_down;
 };
 
 struct FfnArgs {

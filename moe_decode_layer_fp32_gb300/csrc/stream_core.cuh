@@ -11,6 +11,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "kernels.h"
 
@@ -27,6 +28,23 @@ struct WLoad<__nv_bfloat16> {
     static constexpr int kBytes = 2;
     __device__ static __forceinline__ void load8(const char* p, float2 (&f)[4]) {
         unpack_bf16x8_f2(*reinterpret_cast<const uint4*>(p), f);
+    }
+};
+// FP8 E4M3 codes: 8 per 8 bytes, decoded pairwise (exactly) through half2;
+// the row scale is applied by the caller.
+template <>
+struct WLoad<__nv_fp8_e4m3> {
+    static constexpr int kBytes = 1;
+    __device__ static __forceinline__ void load8(const char* p, float2 (&f)[4]) {
+        const uint2 v = *reinterpret_cast<const uint2*>(p);
+        const uint32_t w[2] = {v.x, v.y};
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] & 0xffffu), __NV_E4M3);
+            const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] >> 16), __NV_E4M3);
+            f[2 * i] = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+            f[2 * i + 1] = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+        }
     }
 };
 template <>

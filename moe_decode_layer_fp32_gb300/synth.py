@@ -42,7 +42,7 @@ class LayerShape:
     d: int                 # hidden size (h in the DeaMoE paper)
     n: int                 # routed experts
     k: int                 # experts per token
-    dtype: str             # weight storage: "bf16" or "f32"
+    dtype: str             # weight storage: "bf16", "f32" or "fp8" (E4M3 + fp32 row scales)
     # vanilla
     I: int = 0             # vanilla expert intermediate
     # DeaMoE form C
@@ -105,13 +105,19 @@ FORMP_7B = LayerShape("deamoe-p-h1024-r384-dept8x84-top10-kdept4-bf16", d=1024, 
 FORMP_DSV3 = LayerShape("deamoe-p-h7168-r2048-dept8x108-top10-kdept5-bf16", d=7168, n=864,
                         k=10, dtype="bf16", g=108, I_sh=2048, form_p=True, k_dept=5,
                         batches=(1, 4, 16, 64))
+# FP8 (E4M3, one fp32 scale per row) storage of the two 2048-wide layers.
+VANILLA_128E_FP8 = LayerShape("vanilla-d2048-e128-i768-top8-fp8", d=2048, n=128, k=8,
+                              dtype="fp8", I=768, batches=(1, 4, 16))
+DEAMOE_7B_FP8 = LayerShape("deamoe-d2048-e64-dept8x8-ish1024-ipr128-top8-fp8", d=2048,
+                           n=64, k=8, dtype="fp8", g=8, I_sh=1024, I_pr=128,
+                           batches=(1, 4, 8, 16))
 # The DeepSeek-V3 routed experts alone (the baseline of Figure 2).
 DSV3_ROUTED = LayerShape("vanilla-d7168-e256-i2048-top8-bf16", d=7168, n=256, k=8,
                          dtype="bf16", I=2048, batches=(1, 4, 16, 64))
 
 ALL_SHAPES = (TINY_DEAMOE, TINY_VANILLA, VANILLA_128E, DEAMOE_7B, VANILLA_7B,
               DSV3_VANILLA, DSV3_DEAMOE, ZIPF_DEAMOE, ZIPF_VANILLA, TINY_FORMP, FORMP_7B,
-              FORMP_DSV3, DSV3_ROUTED)
+              FORMP_DSV3, DSV3_ROUTED, VANILLA_128E_FP8, DEAMOE_7B_FP8)
 
 WEIGHT_STD = 0.02
 
@@ -152,7 +158,21 @@ def normal(shape, seed: int, tensor_id: int, std: float = 1.0, device="cpu",
 
 
 def storage_dtype(name: str) -> torch.dtype:
-    return {"bf16": torch.bfloat16, "f32": torch.float32}[name]
+    return {"bf16": torch.bfloat16, "f32": torch.float32, "fp8": torch.float8_e4m3fn}[name]
+
+
+E4M3_MAX = 448.0
+
+
+def quantize_rows_e4m3(w: torch.Tensor):
+    """Storage of fp32 weights ``[..., rows, d]`` as FP8 E4M3 codes with one
+    fp32 scale per row: ``scale = max|row| / 448`` (1 for an all-zero row),
+    codes = the row divided by its scale, rounded to nearest even E4M3.
+    Returns ``(codes, scales)``."""
+    amax = w.abs().amax(dim=-1)
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    q = (w / scale.unsqueeze(-1)).clamp(-E4M3_MAX, E4M3_MAX)
+    return q.to(torch.float8_e4m3fn), scale.to(torch.float32)
 
 
 def hidden(T: int, d: int, seed: int, device="cpu") -> torch.Tensor:
@@ -223,6 +243,17 @@ def near_identity_unit(u: int, r: int, seed: int, tensor_id: int, dtype: str, de
     return a.to(storage_dtype(dtype))
 
 
+def proj_fp8(units: int, rows: int, d: int, seed: int, tensor_id: int, device="cpu"):
+    """``proj`` in FP8 storage: the same fp32 draws, quantised per row.
+    Returns ``(codes [units, rows, d], scales [units, rows])``."""
+    codes = torch.empty((units, rows, d), dtype=torch.float8_e4m3fn, device=device)
+    scales = torch.empty((units, rows), dtype=torch.float32, device=device)
+    for u in range(units):
+        w = normal((rows, d), seed, tensor_id, WEIGHT_STD, device, salt=u + 1)
+        codes[u], scales[u] = quantize_rows_e4m3(w)
+    return codes, scales
+
+
 def make_layer(shape: LayerShape, seed: int, device="cpu", with_router: bool = True) -> dict:
     """All weights of one layer as a dict of tensors on ``device``.
 
@@ -230,34 +261,44 @@ def make_layer(shape: LayerShape, seed: int, device="cpu", with_router: bool = T
     ``up``, ``down`` [n,I,d]; DeaMoE: ``dgate``, ``dup``, ``ddown`` [m,I_sh,d]
     and ``pgate``, ``pup``, ``pdown`` [n,I_pr,d]; shared expert: ``sgate``,
     ``sup``, ``sdown`` [I_s,d] (or None); form P: the department tensors
-    with r = I_sh and ``agate``, ``aup``, ``adown`` [n,r,r].
+    with r = I_sh and ``agate``, ``aup``, ``adown`` [n,r,r].  FP8 layers hold
+    E4M3 codes under those keys and the row scales under ``<key>_sc``.
     """
     s = shape
     L: dict = {"shape": s}
+
+    def put(key, units, rows, tid, squeeze=False):
+        if s.dtype == "fp8":
+            codes, scales = proj_fp8(units, rows, s.d, seed, tid, device)
+            L[key], L[key + "_sc"] = (codes[0], scales[0]) if squeeze else (codes, scales)
+        else:
+            w = proj(units, rows, s.d, seed, tid, s.dtype, device)
+            L[key] = w[0] if squeeze else w
+
     if with_router:
         L["router"] = router(s.d, s.n, seed, device)
         L["bias"] = (zipf_bias(s.n, s.zipf_g, s.zipf, seed).to(device)
                      if s.zipf > 0 else None)
     if s.I > 0:
-        L["gate"] = proj(s.n, s.I, s.d, seed, TID_GATE, s.dtype, device)
-        L["up"] = proj(s.n, s.I, s.d, seed, TID_UP, s.dtype, device)
-        L["down"] = proj(s.n, s.I, s.d, seed, TID_DOWN, s.dtype, device)
+        put("gate", s.n, s.I, TID_GATE)
+        put("up", s.n, s.I, TID_UP)
+        put("down", s.n, s.I, TID_DOWN)
     if s.I_sh > 0:
-        L["dgate"] = proj(s.m, s.I_sh, s.d, seed, TID_DGATE, s.dtype, device)
-        L["dup"] = proj(s.m, s.I_sh, s.d, seed, TID_DUP, s.dtype, device)
-        L["ddown"] = proj(s.m, s.I_sh, s.d, seed, TID_DDOWN, s.dtype, device)
+        put("dgate", s.m, s.I_sh, TID_DGATE)
+        put("dup", s.m, s.I_sh, TID_DUP)
+        put("ddown", s.m, s.I_sh, TID_DDOWN)
     if s.form_p:
         L["agate"] = near_identity(s.n, s.I_sh, seed, TID_AGATE, s.dtype, device)
         L["aup"] = near_identity(s.n, s.I_sh, seed, TID_AUP, s.dtype, device)
         L["adown"] = near_identity(s.n, s.I_sh, seed, TID_ADOWN, s.dtype, device)
     if s.I_pr > 0:
-        L["pgate"] = proj(s.n, s.I_pr, s.d, seed, TID_PGATE, s.dtype, device)
-        L["pup"] = proj(s.n, s.I_pr, s.d, seed, TID_PUP, s.dtype, device)
-        L["pdown"] = proj(s.n, s.I_pr, s.d, seed, TID_PDOWN, s.dtype, device)
+        put("pgate", s.n, s.I_pr, TID_PGATE)
+        put("pup", s.n, s.I_pr, TID_PUP)
+        put("pdown", s.n, s.I_pr, TID_PDOWN)
     if s.I_s > 0:
-        L["sgate"] = proj(1, s.I_s, s.d, seed, TID_SGATE, s.dtype, device)[0]
-        L["sup"] = proj(1, s.I_s, s.d, seed, TID_SUP, s.dtype, device)[0]
-        L["sdown"] = proj(1, s.I_s, s.d, seed, TID_SDOWN, s.dtype, device)[0]
+        put("sgate", 1, s.I_s, TID_SGATE, squeeze=True)
+        put("sup", 1, s.I_s, TID_SUP, squeeze=True)
+        put("sdown", 1, s.I_s, TID_SDOWN, squeeze=True)
     else:
         L["sgate"] = L["sup"] = L["sdown"] = None
     return L
