@@ -47,6 +47,8 @@ WORKLOADS = {
     "formp-7b": synth.FORMP_7B,
     "formp-dsv3": synth.FORMP_DSV3,
     "dsv3-routed": synth.DSV3_ROUTED,
+    "vanilla-128e-fp8": synth.VANILLA_128E_FP8,
+    "deamoe-7b-fp8": synth.DEAMOE_7B_FP8,
 }
 METRIC = "MoE-layer decode µs and achieved HBM GB/s (unique weight bytes) at batch 1–64"
 L2_BYTES = 129 * 2 ** 20
@@ -221,6 +223,14 @@ class Workload:
     def shared(self, L):
         return None if L["sgate"] is None else (L["sgate"], L["sup"], L["sdown"])
 
+    def scales(self, L):
+        """FP8 row scales in the order of the *_fp8 calls (None otherwise)."""
+        if self.shape.dtype != "fp8":
+            return None
+        keys = (("dgate", "dup", "ddown", "pgate", "pup", "pdown") if self.shape.I_sh > 0 else
+                ("gate", "up", "down"))
+        return [L.get(k_ + "_sc") for k_ in keys + ("sgate", "sup", "sdown")]
+
     def layer(self, r, T, x=None, y=None):
         s, B, L, key = self.shape, self.B, self.layers[r], (r, T)
         x = self.x[key] if x is None else x
@@ -233,10 +243,11 @@ class Workload:
             priv = (L["pgate"], L["pup"], L["pdown"]) if s.I_pr > 0 else None
             B.deamoe_layer_forward(x, s.k, 1.0, L["router"], L["bias"], s.g,
                                    (L["dgate"], L["dup"], L["ddown"]), priv, self.shared(L),
-                                   self.ws[key], self.idx[key], self.w[key], y)
+                                   self.ws[key], self.idx[key], self.w[key], y, scales=self.scales(L))
         else:
             B.moe_layer_forward(x, s.k, 1.0, L["router"], L["bias"], L["gate"], L["up"], L["down"],
-                                self.shared(L), self.ws[key], self.idx[key], self.w[key], y)
+                                self.shared(L), self.ws[key], self.idx[key], self.w[key], y,
+                                scales=self.scales(L))
 
     def route_only(self, r, T):
         s, L, key = self.shape, self.layers[r], (r, T)
@@ -273,15 +284,15 @@ class Workload:
         elif s.I_sh > 0:
             priv = (L["pgate"], L["pup"], L["pdown"]) if s.I_pr > 0 else None
             B.deamoe_ffn(self.x[key], s.k, s.g, (L["dgate"], L["dup"], L["ddown"]), priv,
-                         self.shared(L), self.ws[key], B.MOE_OUT_ACCUM, out)
+                         self.shared(L), self.ws[key], B.MOE_OUT_ACCUM, out, scales=self.scales(L))
         else:
             B.moe_ffn_vanilla(self.x[key], s.k, L["gate"], L["up"], L["down"], self.shared(L),
-                              self.ws[key], B.MOE_OUT_ACCUM, out)
+                              self.ws[key], B.MOE_OUT_ACCUM, out, scales=self.scales(L))
 
     def account(self):
         """Unique weight bytes of every (replica, batch) pass from device counts."""
         s, B = self.shape, self.B
-        code = B.MOE_DTYPE_BF16 if s.dtype == "bf16" else B.MOE_DTYPE_F32
+        code = {"bf16": B.MOE_DTYPE_BF16, "f32": B.MOE_DTYPE_F32, "fp8": B.MOE_DTYPE_FP8_E4M3}[s.dtype]
         for key, ws in self.ws.items():
             st, A_e, A_d = B.moe_read_status(ws)
             if st != 0:
@@ -347,7 +358,7 @@ def run_ours(args, rank, world, local):
 
     # Replicas: enough that the bytes between two uses of a replica exceed 4x L2.
     # (smallest pass: one token, k experts, one department)
-    bw = 2 if shape.dtype == "bf16" else 4
+    bw = {"bf16": 2, "f32": 4, "fp8": 1}[shape.dtype]
     per_layer_min = (bw * 3 * (shape.d * shape.I_sh + shape.I_sh * shape.I_sh * shape.k) if shape.form_p else
                      bw * 3 * shape.d * (shape.I_pr * shape.k + shape.I_sh + shape.I * shape.k + shape.I_s))
     R = args.replicas or max(2, min(16, -(-4 * L2_BYTES // max(1, per_layer_min))))
@@ -554,6 +565,10 @@ def cpu_baseline(W, shape, batches, budget_s):
             if r not in host:
                 L = W.layers[r]
                 host[r] = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in L.items()}
+                if shape.dtype == "fp8":
+                    # the oracle decodes each unit it reads (codes and row scales)
+                    for k_ in [k_ for k_ in host[r] if k_ + "_sc" in host[r]]:
+                        host[r][k_] = _Fp8Units(O, host[r][k_], host[r][k_ + "_sc"])
         L = host[r]
         x = W.x[(r, T)].cpu()
         t0 = time.perf_counter()
@@ -570,6 +585,16 @@ def cpu_baseline(W, shape, batches, budget_s):
             "sample": f"{passes} full layer passes cycling over (replica, T) for T in "
                       f"{sorted(batches)}, {min(passes, len(keys))} distinct, in {t_total:.1f} s "
                       "(host copies of the weights made outside the timed sections)"}
+
+
+class _Fp8Units:
+    """FP8 unit tensor for the oracle: indexing a unit decodes it exactly."""
+
+    def __init__(self, O, codes, scales):
+        self.O, self.codes, self.scales = O, codes, scales
+
+    def __getitem__(self, u):
+        return self.O.dequant_rows_e4m3(self.codes[u], self.scales[u])
 
 
 def oracle_forward(O, shape, L, x, idx, p):
@@ -593,7 +618,8 @@ def run_reference(args, rank, world):
     from oracle import moe_oracle as O
     s = WORKLOADS[args.workload]
     batches = tuple(int(b) for b in args.batches.split(",")) if args.batches else s.batches
-    bw = 2 if s.dtype == "bf16" else 4
+    bw = {"bf16": 2, "f32": 4, "fp8": 1}[s.dtype]
+    row_b = 3 * s.d * bw + (12 if s.dtype == "fp8" else 0)    # one intermediate row: weights (+ FP8 scales)
     seed = args.seed * 1000
     router = synth.router(s.d, s.n, seed)
     bias = synth.zipf_bias(s.n, s.zipf_g, s.zipf, seed) if s.zipf > 0 else None
@@ -610,8 +636,12 @@ def run_reference(args, rank, world):
 
     def unit(tid, u, rows):
         if (tid, u) not in units:
-            units[(tid, u)] = synth.normal((rows, s.d), seed, tid, synth.WEIGHT_STD, "cpu",
-                                           synth.storage_dtype(s.dtype), salt=u + 1)
+            if s.dtype == "fp8":
+                w = synth.normal((rows, s.d), seed, tid, synth.WEIGHT_STD, "cpu", salt=u + 1)
+                units[(tid, u)] = torch.from_numpy(O.dequant_rows_e4m3(*synth.quantize_rows_e4m3(w)))
+            else:
+                units[(tid, u)] = synth.normal((rows, s.d), seed, tid, synth.WEIGHT_STD, "cpu",
+                                               synth.storage_dtype(s.dtype), salt=u + 1)
         return units[(tid, u)]
 
     def amat(tid, e):
@@ -646,7 +676,7 @@ def run_reference(args, rank, world):
             nbytes += 4 * s.d * s.n
             if SH is not None:
                 O.swiglu_expert(x[0], *SH)
-                nbytes += bw * 3 * s.d * s.I_s
+                nbytes += row_b * s.I_s
         x, idx, p = state["x"], state["idx"], state["p"]
         e = int(idx[0, q])
         if s.form_p:
@@ -657,11 +687,11 @@ def run_reference(args, rank, world):
         elif s.I_sh > 0:
             p[0, q] * O.swiglu_expert(x[0], *W[e])
             j = e // s.g
-            nbytes += bw * 3 * s.d * (s.I_pr + (s.I_sh if j not in state["depts"] else 0))
+            nbytes += row_b * (s.I_pr + (s.I_sh if j not in state["depts"] else 0))
             state["depts"].add(j)
         else:
             p[0, q] * O.swiglu_expert(x[0], *W[e])
-            nbytes += bw * 3 * s.d * s.I
+            nbytes += row_b * s.I
         return nbytes
 
     for i in range(args.warmup):

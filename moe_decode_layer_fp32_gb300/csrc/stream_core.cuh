@@ -30,8 +30,9 @@ struct WLoad<__nv_bfloat16> {
         unpack_bf16x8_f2(*reinterpret_cast<const uint4*>(p), f);
     }
 };
-// FP8 E4M3 codes: 8 per 8 bytes, decoded pairwise (exactly) through half2;
-// the row scale is applied by the caller.
+// FP8 E4M3 codes: 8 per 8 bytes, decoded pairwise (exactly) through half2 by
+// the conversion unit; the row scale is applied by the caller.  (Decoding
+// with integer bit operations instead measured 1.5x slower on the stream.)
 template <>
 struct WLoad<__nv_fp8_e4m3> {
     static constexpr int kBytes = 1;
