@@ -31,6 +31,9 @@ namespace moe {
 namespace {
 
 constexpr int kStageBytes = 16384;   // one ring slot
+#ifndef MOE_ROUTE_PDL
+#define MOE_ROUTE_PDL 1
+#endif
 constexpr int kRingBytesPerSM = 10 * kStageBytes;  // weights in flight per SM
 constexpr int kSegMax = 256;         // rows per segment (gate/up/h buffers)
 
@@ -242,6 +245,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
         __syncthreads();
     }
 
+    // The next layer's routing grid (a programmatic dependent) may take SMs
+    // as this grid's CTAs finish; it waits for this grid's completion.
+    if (MOE_ROUTE_PDL) pdl_allow_dependents();
     // Everything below reads what the routing / dispatch kernel wrote.
     pdl_wait_primary();
     // The tensor-core kernel ran first and took the step: nothing to do.

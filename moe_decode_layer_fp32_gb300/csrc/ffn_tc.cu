@@ -36,6 +36,9 @@
 
 #include "../../include/moe_decode.h"
 #include "kernels.h"
+#ifndef MOE_ROUTE_PDL
+#define MOE_ROUTE_PDL 1
+#endif
 #include "local_route.cuh"
 #include "tc_ptx.cuh"
 
@@ -214,6 +217,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
     tc_fence_after_sync();
     const uint32_t tmem = sm.tmem_base;
 
+    // The next layer's routing grid (a programmatic dependent) may take SMs
+    // as this grid's CTAs finish; it waits for this grid's completion.
+    if (MOE_ROUTE_PDL) pdl_allow_dependents();
     // Everything below reads what the routing / dispatch kernel wrote.
     pdl_wait_primary();
 

@@ -18,6 +18,9 @@ namespace moe {
 namespace {
 
 constexpr int kRouteThreads = 512;
+#ifndef MOE_ROUTE_PDL
+#define MOE_ROUTE_PDL 1
+#endif
 constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kDispatchThreads = 512;
 constexpr int kMaskWords = (kMaxT + 31) / 32;
@@ -238,6 +241,11 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
     __shared__ int s_last;
     // Let the FFN grid (launched as a programmatic dependent) start its prologue.
     pdl_allow_dependents();
+    // This grid is itself a programmatic dependent of the kernel before it
+    // in the stream (an FFN step of the previous layer, say): its blocks may
+    // be resident early, and everything they read or write waits for that
+    // kernel's completion here.
+    pdl_wait_primary();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     if (a.split_x)
@@ -369,10 +377,19 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
 // The group-limited selection is its own instantiation, which leaves the
 // plain kernel's registers as they are.
 template <int EB, bool GROUPED>
-void launch_route_eb(const RouteArgs& a, int rch, int blocks, cudaStream_t s) {
-    if (rch <= 1) route_kernel<1, EB, GROUPED><<<blocks, kRouteThreads, 0, s>>>(a);
-    else if (rch <= 2) route_kernel<2, EB, GROUPED><<<blocks, kRouteThreads, 0, s>>>(a);
-    else route_kernel<4, EB, GROUPED><<<blocks, kRouteThreads, 0, s>>>(a);
+cudaError_t launch_route_eb(const RouteArgs& a, int rch, int blocks, cudaStream_t s) {
+    auto kern = rch <= 1 ? route_kernel<1, EB, GROUPED> : rch <= 2 ? route_kernel<2, EB, GROUPED>
+                                                                   : route_kernel<4, EB, GROUPED>;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kRouteThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = MOE_ROUTE_PDL;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
@@ -385,14 +402,10 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
     // its SM's registers alone): from 256 experts on, 4 per block
     const int eb = a.n % 4 == 0 && (tblocks >= 4 || a.n >= 256) ? 4 : 1;
     const bool grouped = a.k_dept > 0 && !a.logits_only;
-    if (eb == 4) {
-        if (grouped) launch_route_eb<4, true>(a, rch, a.n / 4 * tblocks, s);
-        else launch_route_eb<4, false>(a, rch, a.n / 4 * tblocks, s);
-    } else {
-        if (grouped) launch_route_eb<1, true>(a, rch, a.n * tblocks, s);
-        else launch_route_eb<1, false>(a, rch, a.n * tblocks, s);
-    }
-    return cudaGetLastError();
+    if (eb == 4) return grouped ? launch_route_eb<4, true>(a, rch, a.n / 4 * tblocks, s)
+                                : launch_route_eb<4, false>(a, rch, a.n / 4 * tblocks, s);
+    return grouped ? launch_route_eb<1, true>(a, rch, a.n * tblocks, s)
+                   : launch_route_eb<1, false>(a, rch, a.n * tblocks, s);
 }
 
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t s) {
