@@ -151,3 +151,75 @@ def test_unique_bytes_match_oracle_formula(B):
         assert B.moe_unique_weight_bytes_deamoe(d, n, I_sh, I_pr, I_s, 1, A_d, A_e) == \
             O.unique_bytes_deamoe_c(d, n, I_sh, I_pr, I_s, A_d, A_e, 2)
     assert B.moe_unique_weight_bytes_vanilla(2048, 128, 768, 0, 9, 8) == -1
+
+
+# ---------------------------------------------------------------------------
+# Host checks of the NEXT-row entry points (nothing is launched)
+# ---------------------------------------------------------------------------
+
+FAKE = 1 << 20          # an aligned address that is never dereferenced
+
+
+def test_grouped_routing_rejects_bad_group_arguments(B):
+    lib = B.lib()
+    need = lib.moe_workspace_bytes(4, 16, 4, 1)
+    args = lambda g, kd, strict, k=4: (FAKE, FAKE, None, 4, 256, 16, k, g, kd, strict, 1.0, FAKE, FAKE,  # noqa: E731
+                                       FAKE, need, None)
+    for g, kd, strict, k in ((3, 1, 0, 4), (4, 0, 0, 4), (4, 5, 0, 4), (4, 1, 0, 5), (1, 5, 1, 4)):
+        assert lib.moe_route_topk_grouped(*args(g, kd, strict, k)) == -1
+
+
+def test_bias_update_rejects_bad_arguments_on_the_host(B):
+    lib = B.lib()
+    assert lib.moe_bias_update(FAKE, 0, 0.1, 0, FAKE, None, None) == -1
+    assert lib.moe_bias_update(FAKE, 1025, 0.1, 0, FAKE, None, None) == -1
+    assert lib.moe_bias_update(None, 8, 0.1, 0, FAKE, None, None) == -1
+    assert lib.moe_bias_update(FAKE, 8, 0.1, 0, None, None, None) == -1
+    assert lib.moe_bias_update(FAKE, 8, 0.1, 7, FAKE, None, None) == -1
+    assert lib.moe_bias_update(FAKE, 8, -0.5, 0, FAKE, None, None) == -1
+    assert lib.moe_bias_update(FAKE, 8, float("nan"), 1, FAKE, None, None) == -1
+    assert lib.moe_bias_update(FAKE, 8, float("inf"), 1, FAKE, None, None) == -1
+
+
+def test_formp_workspace_and_argument_checks(B):
+    lib = B.lib()
+    T, n, k, g, r = 4, 16, 4, 4, 64
+    base = lib.moe_workspace_bytes(T, n, k, g)
+    total = lib.moe_formp_workspace_bytes(T, n, k, g, r)
+    # G and U per department entry (T * min(k, m)), A_d^T Y per assignment, fp32
+    assert total >= base + 4 * r * (2 * T * min(k, n // g) + T * k)
+    assert lib.moe_formp_workspace_bytes(T, n, k, 1, r) == 0        # no departments
+    assert lib.moe_formp_workspace_bytes(T, n, k, g, 40) == 0       # r % 16
+    w = (FAKE,) * 6
+
+    def call(k_dept=0, dtype=1, rr=r, ws_bytes=total, weights=w, d=256):
+        return lib.deamoe_p_layer_forward(FAKE, T, d, n, k, 1.0, FAKE, None, g, k_dept, rr, dtype, *weights,
+                                          FAKE, ws_bytes, FAKE, FAKE, FAKE, None)
+    assert call(k_dept=-1) == -1
+    assert call(k_dept=5) == -1                      # more departments than m = 4
+    assert call(dtype=0) == -2                       # fp32 weights
+    assert call(ws_bytes=total - 256) == -3
+    assert call(weights=(FAKE, None, FAKE, FAKE, FAKE, FAKE)) == -1
+    assert call(d=8192) == -2                        # wider than the passes take
+    big = lib.moe_formp_workspace_bytes(T, n, k, g, 4096)
+    assert call(rr=4096, ws_bytes=big) == -2         # r above 2048
+
+
+def test_fp8_calls_need_their_row_scales(B):
+    lib = B.lib()
+    T, d, n, k, I = 2, 256, 16, 2, 64
+    need = lib.moe_workspace_bytes(T, n, k, 1)
+    # the bf16 / fp32 call with the FP8 code: refused before any launch
+    rc = lib.moe_layer_forward(FAKE, T, d, n, k, 1.0, FAKE, None, I, B.MOE_DTYPE_FP8_E4M3, FAKE, FAKE, FAKE, 0,
+                               None, None, None, FAKE, need, FAKE, FAKE, FAKE, None)
+    assert rc == -1 and b"row scales" in lib.moe_last_error()
+    # the FP8 call without scales, or with a missing one
+    rc = lib.moe_layer_forward_fp8(FAKE, T, d, n, k, 1.0, FAKE, None, I, FAKE, FAKE, FAKE, 0, None, None, None,
+                                   None, FAKE, need, FAKE, FAKE, FAKE, None)
+    assert rc == -1
+    sc = (C.c_void_p * 6)(FAKE, None, FAKE, None, None, None)
+    rc = lib.moe_layer_forward_fp8(FAKE, T, d, n, k, 1.0, FAKE, None, I, FAKE, FAKE, FAKE, 0, None, None, None,
+                                   sc, FAKE, need, FAKE, FAKE, FAKE, None)
+    assert rc == -1 and b"set 0" in lib.moe_last_error()
+    # FP8 bytes: codes plus three fp32 scales per row
+    assert lib.moe_unique_weight_bytes_vanilla(d, n, I, 0, B.MOE_DTYPE_FP8_E4M3, 3) == 4 * d * n + 3 * I * 3 * (d + 4)
