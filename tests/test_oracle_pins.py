@@ -715,3 +715,18 @@ def test_dequant_rows_scales_each_row():
     scale = np.array([[0.25, 3.0]], np.float32)
     np.testing.assert_array_equal(O.dequant_rows_e4m3(codes, scale),
                                   [[[0.25, 0.5], [-3.0, 1.5]]])
+
+
+def test_e4m3_row_quantisation_error_bound():
+    """Round to nearest even with 3 mantissa bits: a weight stored as row scale
+    times an E4M3 code is within 2^-4 of itself (relative) in the normal range,
+    and within half the smallest subnormal step (2^-10 times the scale) below."""
+    g = torch.Generator().manual_seed(5)
+    w = torch.randn((64, 512), generator=g) * 0.02
+    codes, scale = synth.quantize_rows_e4m3(w)
+    back = O.dequant_rows_e4m3(codes, scale)
+    wd = w.double().numpy()
+    bound = np.maximum(2.0 ** -4 * np.abs(wd), 2.0 ** -10 * scale.double().numpy()[:, None])
+    assert (np.abs(back - wd) <= bound * (1 + 1e-12)).all()
+    # the row maximum is represented exactly (it maps to 448)
+    np.testing.assert_allclose(np.abs(back).max(axis=1), np.abs(wd).max(axis=1), rtol=1e-7)
