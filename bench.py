@@ -309,6 +309,21 @@ class Workload:
             lay = B.moe_workspace_layout(key[1], s.n, s.k, self.g)
             self.choice[key] = int(ws[lay["sync"] + 4: lay["sync"] + 8].cpu().view(torch.int32)[0])
 
+    def launches(self, key, thr: int) -> int:
+        """Kernels one layer pass launches: form P, the routing kernel and its
+        three passes; otherwise the routing kernel and the FFN kernels -- the
+        tensor-core kernel alone on its in-CTA routing path (automatic choice,
+        rows at most 4096 wide, T <= 32, at most 256 experts), both FFN kernels
+        when the tensor-core kernel is launched beside the CUDA-core one, else
+        the CUDA-core kernel alone."""
+        s, T = self.shape, key[1]
+        if s.form_p:
+            return 4
+        if not self.tc_launched(key, thr):
+            return 2
+        tc_alone = thr == 0 and s.d <= 4096 and T <= 32 and s.n <= 256 and self.choice[key] == 2
+        return 2 if tc_alone else 3
+
     def tc_launched(self, key, thr: int) -> bool:
         """Whether the layer pass launches the tensor-core FFN kernel: in
         automatic mode exactly when the kernels recorded a choice; with a fixed
@@ -485,10 +500,7 @@ def run_ours(args, rank, world, local):
         "per_batch": per_batch,
         "roofline": roofline,
         "e2e": e2e,
-        # per layer pass: routing (+ fused dispatch), CUDA-core FFN, tensor-core FFN when
-        # launched; form P: routing and its three passes
-        "gpu_launches": sum((4 if shape.form_p else 2 + int(W.tc_launched((i % R, T), args.tc_min_tokens)))
-                            for i in range(args.steps) for T in batches),
+        "gpu_launches": sum(W.launches((i % R, T), args.tc_min_tokens) for i in range(args.steps) for T in batches),
         "clocks": clock_info,
         "cpu_baseline": cpu,
     }
