@@ -44,7 +44,7 @@ struct PSmem {
     int dn_cnt[kMT];                  // down pass: the group's tokens' assignments
     int dn_pos[kMT][kMaxK];           //   in the department: position and
     float dn_w[kMT][kMaxK];           //   routing weight
-    int4 units[kMaxN];                // active unit records (from the dispatch)
+    int4 units[1];                    // active unit records (from the dispatch), sized at launch
 };
 
 struct PSeg {
@@ -396,7 +396,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) formp_kernel(FormPArgs a)
 template <int STAGE, int NCW, int CH, int RMAX, int CPS>
 cudaError_t launch_formp_cfg(const FormPArgs& a, int sms, cudaStream_t s) {
     constexpr int NS = kPRingBytesPerSM / kPStageBytes / CPS;
-    const size_t smem = (size_t)NS * kPStageBytes + sizeof(PSmem<NS>);
+    const int cap = STAGE == kFormPPriv ? a.n : a.m;   // unit records the dispatch may hold
+    const size_t smem = (size_t)NS * kPStageBytes + sizeof(PSmem<NS>) + (size_t)cap * sizeof(int4);
     auto kern = formp_kernel<STAGE, NCW, CH, RMAX, CPS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -419,6 +420,11 @@ cudaError_t launch_formp_cfg(const FormPArgs& a, int sms, cudaStream_t s) {
 // private pass takes rows of at most 2048.
 template <int STAGE>
 cudaError_t launch_formp_stage(const FormPArgs& a, int width, int sms, cudaStream_t s) {
+#ifndef MOE_FP_NARROW_PRIV
+#define MOE_FP_NARROW_PRIV 1
+#endif
+    // rows of at most 512 (64 chunks): two consumer warps, four CTAs per SM
+    if (MOE_FP_NARROW_PRIV && width <= 512) return launch_formp_cfg<STAGE, 2, 1, 4, 4>(a, sms, s);
     if (width <= 1024) return launch_formp_cfg<STAGE, 4, 1, 4, 2>(a, sms, s);
     if (width <= 2048) return launch_formp_cfg<STAGE, 8, 1, 4, 1>(a, sms, s);
     if constexpr (STAGE != kFormPPriv) return launch_formp_cfg<STAGE, 15, 2, 1, 1>(a, sms, s);
