@@ -29,7 +29,7 @@ Sources (cited by title and section):
   batch becomes expert-specific matrices" (dispatch / combine) and "Local MoE
   execution pipeline" (permutation with an inverse map).
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
 
 * R1 routing decision: keys are fp32 (the router is fp32); the oracle rounds
   its fp64 logit to fp32, adds the fp32 bias in fp32, and orders by key

@@ -9,7 +9,7 @@ import torch
 from moe_decode_layer_fp32_gb300 import synth
 from oracle import moe_oracle as O
 
-# Spec tolerances: max|y - y_ref| / max|y_ref| per output tensor.
+# Output tolerances: max|y - y_ref| / max|y_ref| per output tensor.
 TOL = {"bf16": 2e-2, "f32": 1e-4}
 
 

@@ -2,7 +2,7 @@
 the C ABI, against the CPU oracle's per-token, per-expert evaluation.
 
 Routing must match bit-exactly up to certified fp32 near-ties (group-limited
-when the shape gives k_dept); outputs within the benchmark spec's bound for bf16
+when the shape gives k_dept); outputs within the stated bound for bf16
 weights, max|y - y_ref| / max|y_ref| <= 2e-2, and in practice far inside it
 (fp32 arithmetic on exactly decoded weights), which the tests also check at
 1e-4.

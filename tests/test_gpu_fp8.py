@@ -2,7 +2,7 @@
 C ABI, against the oracle on the exactly decoded weights.
 
 The device decodes each code exactly and applies the row scale in fp32, so
-outputs stay within 1e-4 of the fp64 oracle (the benchmark spec's 2e-2 bound for
+outputs stay within 1e-4 of the fp64 oracle (the 2e-2 output bound for
 reduced-precision weights is checked as well); routing is unchanged (fp32
 router) and compared as everywhere else.
 """

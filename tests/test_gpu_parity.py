@@ -2,7 +2,7 @@
 
 Routing indices and dispatch lists must match bit-exactly (certified fp32
 near-ties excepted, see helpers.compare_routing); outputs must match within
-the benchmark spec's tolerance: max|y - y_ref| / max|y_ref| <= 2e-2 for bf16
+the output tolerance: max|y - y_ref| / max|y_ref| <= 2e-2 for bf16
 weights and 1e-4 for fp32 weights.
 """
 
