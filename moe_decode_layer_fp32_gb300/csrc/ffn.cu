@@ -208,7 +208,13 @@ __device__ __forceinline__ int group_tokens(const FfnArgs& a, const int4 rec, in
 }
 
 
-template <typename WT, int NCW, int CH, int RMAX, int CPS>
+// ONE: a one-token step on the in-CTA routing path
+// (the host launches it only then).  CTA 0 builds the workspace lists as
+// usual; the other CTAs take the unit records straight from the selection
+// (local_tables_one_token), every CTA streams an equal share of the rows, and
+// the consumers run the one-token register tile only.  A separate
+// instantiation, so that the general kernel's code is not touched by it.
+template <typename WT, int NCW, int CH, int RMAX, int CPS, bool ONE>
 __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs a) {
     using K = Ffn<WT, NCW, CH, RMAX>;
     constexpr int NS = kRingBytesPerSM / kStageBytes / CPS;   // ring slots per CTA
@@ -261,7 +267,12 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
         const bool writer = blockIdx.x == 0;
         local_topk<kNT>(a, lr, writer);
         const UnitTableView view = {sm.units, sm.cls_off, sm.cls_units, sm.cls_groups, sm.cls_cost, cpre};
-        local_tables<kNT, kMT, true>(a, view, lr, writer);
+        if constexpr (ONE) {
+            if (!writer) local_tables_one_token<kNT>(a, view, lr);
+            else local_tables<kNT, kMT, true>(a, view, lr, writer);
+        } else {
+            local_tables<kNT, kMT, true>(a, view, lr, writer);
+        }
     } else if (a.max_tokens >= a.T) {
         int off = 0;
         for (int c = 0; c < a.ncls; ++c) {
@@ -339,7 +350,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
     // when the cost total would not fit the 32-bit split search
     long long r_begin = grid_share(R, blockIdx.x, gridDim.x, a.grid_magic);
     long long r_end = grid_share(R, blockIdx.x + 1, gridDim.x, a.grid_magic);
-    if (R > 0) {
+    if constexpr (ONE) {
+        // one token: every row costs the same, so the equal split above stands
+    } else if (R > 0) {
         __shared__ long long s_split[2];
         const long long tot = split_total_cost(a, sm);
         if (tot > 0 && tot < (1ll << 31)) {
@@ -463,7 +476,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
                     if (wait_full(slot, it)) {
                         const char* st = reinterpret_cast<const char*>(ring + (size_t)slot * kStageBytes);
                         float* gr = &sm.gu[mat][rb * kMT];
-                        if (mg == 1)
+                        if (ONE || mg == 1)
                             K::template gu_any<1>(st, nr, row_bytes, coff, cval, xr, gr, mg, lane);
                         else if (mg == 2)
                             K::template gu_any<2>(st, nr, row_bytes, coff, cval, xr, gr, mg, lane);
@@ -516,7 +529,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
             if (wait_full(slot, it)) {
                 const char* st = reinterpret_cast<const char*>(ring + (size_t)slot * kStageBytes);
                 const float* hr = &sm.h[rb * kMT];
-                if (mg == 1)
+                if (ONE || mg == 1)
                     K::template down_any<1>(st, nr, row_bytes, coff, cval, hr, yacc);
                 else if (mg == 2)
                     K::template down_any<2>(st, nr, row_bytes, coff, cval, hr, yacc);
@@ -585,11 +598,12 @@ size_t smem_per_cta_limit(int cps) {
 
 template <typename WT, int NCW, int CH, int RMAX, int CPS>
 cudaError_t launch_ffn_t(const FfnArgs& a, cudaStream_t s, FfnCfg<WT, NCW, CH, RMAX, CPS> cfg_tag) {
-    auto kern = ffn_stream_kernel<WT, NCW, CH, RMAX, CPS>;
+    const unsigned grid = (unsigned)(device_sm_count() * CPS);
+    auto kern = a.local_route && a.T == 1 ? ffn_stream_kernel<WT, NCW, CH, RMAX, CPS, true>
+                                          : ffn_stream_kernel<WT, NCW, CH, RMAX, CPS, false>;
     const size_t smem = ffn_smem(a, cfg_tag);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)(device_sm_count() * CPS);
     FfnArgs args = a;
     args.grid_magic = grid_magic_of(grid);
     cudaLaunchConfig_t cfg = {};

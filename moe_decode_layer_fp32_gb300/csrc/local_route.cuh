@@ -337,6 +337,75 @@ __device__ void local_tables(const FfnArgs& a, const UnitTableView& sm, const Lo
     __syncthreads();
 }
 
+// One token (after the top-k; every thread of the CTA; ends with a barrier):
+// every unit then holds exactly that token, so the unit records follow from
+// the selection itself, with no masks, counts or scans.  The order is the
+// general tables' (ascending expert id, then ascending department id: a
+// unit's place is the number of selected ids below its own), so that a CTA
+// built either way splits the same row sequence; one group per unit; a
+// department's omega is the token's weights on its experts summed in slot
+// order.  No cost prefixes: the caller splits the rows evenly.
+template <int NT>
+__device__ void local_tables_one_token(const FfnArgs& a, const UnitTableView& sm, const LocalRoute& lr) {
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x, k = a.k;
+        const bool act = lane < k;
+        const int e = act ? lr.idx[lane] : 0;
+        const int dj = act ? lr.didx[lane] : 0;
+        const float w = act ? lr.w[lane] : 0.0f;
+        const bool dept = lr.m > 0;
+        int p = 0;              // experts selected below e
+        uint32_t same = 0u;     // slots on department dj
+        float om = 0.0f;
+        for (int r = 0; r < k; ++r) {
+            const int er = __shfl_sync(0xffffffffu, e, r);
+            const int dr = __shfl_sync(0xffffffffu, dj, r);
+            const float wr = __shfl_sync(0xffffffffu, w, r);
+            p += er < e ? 1 : 0;
+            if (dr == dj) {
+                same |= 1u << r;
+                om += wr;
+            }
+        }
+        // one lane per selected department: its first slot
+        const bool first = dept && act && (same & ((1u << lane) - 1u)) == 0u;
+        const uint32_t fm = __ballot_sync(0xffffffffu, first);
+        int q = 0;              // departments selected below dj
+        for (int r = 0; r < k; ++r) {
+            const int dr = __shfl_sync(0xffffffffu, dj, r);
+            q += ((fm >> r) & 1u) && dr < dj ? 1 : 0;
+        }
+        if (act) {
+            lr.etok[p] = 0;
+            lr.ew[p] = w;
+        }
+        if (first) {
+            lr.dtok[q] = 0;
+            lr.dw[q] = om;
+        }
+        for (int c = 0; c < a.ncls; ++c) {
+            const int kind = a.cls[c].kind;
+            int4* u = sm.units + sm.cls_off[c];
+            int nu = 0;
+            if (kind == kUnitExpert) {
+                if (act) u[p] = make_int4(e, p, 1, p + 1);
+                nu = k;
+            } else if (kind == kUnitDept) {
+                if (first) u[q] = make_int4(dj, q, 1, q + 1);
+                nu = __popc(fm);
+            } else {
+                if (lane == 0) u[0] = make_int4(0, 0, 1, 1);
+                nu = 1;
+            }
+            if (lane == 0) {
+                sm.cls_units[c] = nu;
+                sm.cls_groups[c] = nu;
+            }
+        }
+    }
+    __syncthreads();
+}
+
 // Tokens of group `grp` of a unit from the shared-memory lists, with their
 // weights (ACCUM mode: the output row is the token).
 template <int MT>
