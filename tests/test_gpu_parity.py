@@ -411,6 +411,72 @@ def test_edge_shapes(B):
     check_layer(B, s4, 128, seed=8)
 
 
+# One token on the whole-layer path: its top-k ranks the candidates in one
+# pass instead of k warp rounds; the order and the bits must not change.
+ONE_TOKEN_SHAPES = [
+    synth.LayerShape("one-vanilla", d=256, n=64, k=6, dtype="bf16", I=64, batches=(1,)),
+    synth.LayerShape("one-deamoe", d=256, n=64, k=6, dtype="bf16", g=8, I_sh=64, I_pr=32,
+                     batches=(1,)),
+]
+
+
+def dyadic_router(d, n):
+    """Router whose logit for the all-ones token is exactly level(e) / 8 in
+    fp32 and fp64 alike (dyadic entries, power-of-two d): 16 levels of 4
+    experts each (37 is prime to 64), so the keys hold exact ties."""
+    c = torch.tensor([((e * 37) % n) // 4 / 8.0 for e in range(n)], dtype=torch.float32)
+    return (c[:, None] / d).expand(n, d).contiguous().to(DEV)
+
+
+@pytest.mark.parametrize("shape", ONE_TOKEN_SHAPES, ids=lambda s: s.name)
+@pytest.mark.parametrize("with_bias", [False, True], ids=["no-bias", "bias"])
+def test_one_token_layer_exact_ties(B, shape, with_bias):
+    L = synth.make_layer(shape, 11, DEV)
+    L["router"] = dyadic_router(shape.d, shape.n)
+    L["bias"] = (torch.tensor([((e * 13) % 5 - 2) / 4 for e in range(shape.n)], device=DEV)
+                 if with_bias else None)
+    x = torch.ones((1, shape.d), device=DEV)
+    ws, gi, gw, y = H.run_layer_forward(B, shape, L, x)
+    torch.cuda.synchronize()
+    assert B.moe_read_status(ws)[0] == 0
+    oi, op, info = O.route(x, L["router"], shape.k, bias=L["bias"])
+    gi, gw = gi.cpu().numpy(), gw.cpu().numpy()
+    # the oracle orders equal keys by expert index; so must the device
+    np.testing.assert_array_equal(gi, oi)
+    np.testing.assert_allclose(gw, op, rtol=1e-6)
+    # the last selected key is shared with experts left out: a tie was cut
+    key = info["key32"][0]
+    last = key[oi[0, -1]]
+    assert np.count_nonzero(key == last) > np.count_nonzero(key[oi[0]] == last)
+    y_ref = H.oracle_layer(shape, L, x, oi, op)
+    assert H.rel_err(y.cpu().numpy(), y_ref) <= H.TOL[shape.dtype]
+    # the routing kernel's warp top-k (the multi-token selection) gives the same bits
+    _, ri, rw = route_on_gpu(B, x, L["router"], L["bias"], shape.k)
+    np.testing.assert_array_equal(gi, ri)
+    assert np.array_equal(gw.view(np.uint32), rw.view(np.uint32))
+
+
+@pytest.mark.parametrize("T", [1, 3])
+def test_layer_flags_masked_experts_in_the_selection(B, T):
+    """Experts masked by a -inf selection bias rank after every finite key,
+    lowest index first; selecting one sets the routing status (no fault)."""
+    shape = ONE_TOKEN_SHAPES[0]
+    L = synth.make_layer(shape, 12, DEV)
+    bias = torch.full((shape.n,), float("-inf"), device=DEV)
+    bias[[5, 17, 40, 63]] = 0.0
+    L["bias"] = bias
+    x = synth.hidden(T, shape.d, 12, DEV)
+    ws, gi, gw, y = H.run_layer_forward(B, shape, L, x)
+    torch.cuda.synchronize()
+    assert B.moe_read_status(ws)[0] == -6
+    gi = gi.cpu().numpy()
+    for t in range(T):
+        assert sorted(gi[t, :4].tolist()) == [5, 17, 40, 63]
+        assert gi[t, 4:].tolist() == [0, 1]
+    _, ri, _ = route_on_gpu(B, x, L["router"], L["bias"], shape.k)
+    np.testing.assert_array_equal(gi, ri)
+
+
 def test_invariant_one_expert_per_dept_no_private_is_vanilla(B):
     """DeaMoE with one expert per department and no private rows is the
     vanilla layer: the two device paths agree."""
