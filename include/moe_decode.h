@@ -29,6 +29,12 @@
  *     ([DeaMoE] §2.1).  Stacked tensors are [units, rows, d].
  *   - Pointers must be 16-byte aligned; d must be a multiple of 8 and every
  *     intermediate size a multiple of 16.
+ *   - Routing kernels launch as programmatic dependents of the kernel before
+ *     them on the stream and may read the router weights before waiting for
+ *     that kernel to complete (everything else they read waits).  A kernel of
+ *     the caller's that writes router weights must therefore not trigger its
+ *     dependents early (griddepcontrol.launch_dependents) before those writes;
+ *     copies, memsets and kernels without that trigger need nothing.
  *   - Return value: MOE_OK or a negative MOE_ERR_* code; nothing is launched
  *     when the host-side checks fail.  moe_last_error() gives a message
  *     (thread-local).  Device-side checks (an expert index out of range, a

@@ -241,12 +241,27 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
     __shared__ int s_last;
     // Let the FFN grid (launched as a programmatic dependent) start its prologue.
     pdl_allow_dependents();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tblocks = (a.T + 7) >> 3;
+    const int eg = blockIdx.x / tblocks;
+    const int d4 = a.d >> 2;
+    // One expert per block: its router row is a layer constant, loaded before
+    // the wait below so that the round trip overlaps the previous kernel's
+    // last blocks (this grid's blocks take SMs as that kernel's blocks exit).
+    float4 w[EB == 1 ? RCH : 1];
+    if constexpr (EB == 1) {
+        const float4* wr = reinterpret_cast<const float4*>(a.w_router + (size_t)eg * a.d);
+#pragma unroll
+        for (int i = 0; i < RCH; ++i) {
+            const int c = tid + i * kRouteThreads;
+            w[i] = c < d4 ? __ldg(wr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
     // This grid is itself a programmatic dependent of the kernel before it
     // in the stream (an FFN step of the previous layer, say): its blocks may
-    // be resident early, and everything they read or write waits for that
-    // kernel's completion here.
+    // be resident early, and everything else they read or write waits for
+    // that kernel's completion here.
     pdl_wait_primary();
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     if (a.split_x)
         split_activations(a.x, (long long)a.T * a.d, a.ws.xb, blockIdx.x * (long long)kRouteThreads + tid,
@@ -259,26 +274,16 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
             y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 
-    const int tblocks = (a.T + 7) >> 3;
     const int groups = a.n / EB;
-    const int eg = blockIdx.x / tblocks;
     const int tb = blockIdx.x - eg * tblocks;
     const int t0 = tb * 8;
-    const int d4 = a.d >> 2;
     {
         float acc[8 * EB];
 #pragma unroll
         for (int q = 0; q < 8 * EB; ++q) acc[q] = 0.f;
         if constexpr (EB == 1) {
-            // one expert: its router chunks are loaded up front (one round
-            // trip), then the tokens' activations chunk by chunk
-            float4 w[RCH];
-            const float4* wr = reinterpret_cast<const float4*>(a.w_router + (size_t)eg * a.d);
-#pragma unroll
-            for (int i = 0; i < RCH; ++i) {
-                const int c = tid + i * kRouteThreads;
-                w[i] = c < d4 ? __ldg(wr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+            // one expert: its router chunks were loaded before the wait,
+            // then the tokens' activations chunk by chunk
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 if (t0 + q < a.T) {
