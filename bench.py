@@ -460,9 +460,9 @@ def run_ours(args, rank, world, local):
         ke = min(args.steps, 500)
         for i in range(min(args.warmup, 20)):
             for T in batches:
-                dx[T].copy_(hx[(i % R, T)], non_blocking=True)
+                B.moe_input_from_host(dx[T], hx[(i % R, T)])
                 W.layer(i % R, T, x=dx[T])
-                hy[(i % R, T)].copy_(W.y[(i % R, T)], non_blocking=True)
+                B.moe_output_to_host(hy[(i % R, T)], W.y[(i % R, T)])
         barrier(world)
         torch.cuda.synchronize()
         s0 = torch.cuda.Event(enable_timing=True)
@@ -471,9 +471,9 @@ def run_ours(args, rank, world, local):
         for i in range(ke):
             r = i % R
             for T in batches:
-                dx[T].copy_(hx[(r, T)], non_blocking=True)
+                B.moe_input_from_host(dx[T], hx[(r, T)])
                 W.layer(r, T, x=dx[T])
-                hy[(r, T)].copy_(W.y[(r, T)], non_blocking=True)
+                B.moe_output_to_host(hy[(r, T)], W.y[(r, T)])
         s1.record()
         torch.cuda.synchronize()
         barrier(world)

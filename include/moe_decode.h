@@ -331,6 +331,24 @@ int moe_combine(const float* rows, int T, int d, int n, int k, int experts_per_d
                 void* stream);
 
 /* ------------------------------------------------------------------------- */
+/* Host activations                                                          */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * A step whose activations live on the host: moe_input_from_host copies
+ * x_host (host, float[T, d]) into x (device, float[T, d]) before the layer
+ * call, and moe_output_to_host copies its output y (device, float[T, d]) into
+ * y_host (host) after it.  Each is one asynchronous copy on `stream`, ordered
+ * with the layer's launches.  Page-locked host memory keeps the copy
+ * asynchronous; pageable memory works, but the copy blocks the host.  Either
+ * buffer stays owned by the caller, and y_host is complete once the stream
+ * reaches the copy (synchronise before reading it).  MOE_ERR_INVALID_ARG for a
+ * null pointer or T, d < 1; MOE_ERR_CUDA if the copy cannot be enqueued.
+ */
+int moe_input_from_host(float* x, const float* x_host, int T, int d, void* stream);
+int moe_output_to_host(float* y_host, const float* y, int T, int d, void* stream);
+
+/* ------------------------------------------------------------------------- */
 /* Whole layer                                                               */
 /* ------------------------------------------------------------------------- */
 

@@ -53,6 +53,8 @@ _SIGS = {
     "moe_workspace_layout": (_I, [_I, _I, _I, _I, C.POINTER(WsLayout)]),
     "moe_workspace_init": (_I, [_P, _SZ, _P]),
     "moe_read_status": (_I, [_P, _SZ, C.POINTER(C.c_int32), C.POINTER(C.c_int32), _P]),
+    "moe_input_from_host": (_I, [_P, _P, _I, _I, _P]),
+    "moe_output_to_host": (_I, [_P, _P, _I, _I, _P]),
     "moe_route_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _SZ, _P]),
     "moe_route_topk_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
     "moe_bias_update": (_I, [_P, _I, _F, _I, _P, _P, _P]),
@@ -182,6 +184,30 @@ def moe_read_status(ws: torch.Tensor):
     cnt = (C.c_int32 * 2)()
     _check("moe_read_status", lib().moe_read_status(_ptr(ws), ws.numel(), st, cnt, _stream()))
     return int(st[0]), int(cnt[0]), int(cnt[1])
+
+
+def _host_ptr(t):
+    if t.is_cuda:
+        raise ValueError("expected a host (CPU) tensor")
+    if not t.is_contiguous() or t.dtype != torch.float32:
+        raise ValueError("expected a contiguous float32 host tensor")
+    return t.data_ptr()
+
+
+def moe_input_from_host(x, x_host):
+    """Enqueue the copy of host activations x_host [T, d] into device x [T, d]."""
+    if x.shape != x_host.shape or x.dim() != 2 or x.dtype != torch.float32:
+        raise ValueError("x and x_host must both be float32 [T, d]")
+    T, d = x.shape
+    _check("moe_input_from_host", lib().moe_input_from_host(_ptr(x), _host_ptr(x_host), T, d, _stream()))
+
+
+def moe_output_to_host(y_host, y):
+    """Enqueue the copy of the device output y [T, d] into host y_host [T, d]."""
+    if y.shape != y_host.shape or y.dim() != 2 or y.dtype != torch.float32:
+        raise ValueError("y and y_host must both be float32 [T, d]")
+    T, d = y.shape
+    _check("moe_output_to_host", lib().moe_output_to_host(_host_ptr(y_host), _ptr(y), T, d, _stream()))
 
 
 # ---------------------------------------------------------------- steps

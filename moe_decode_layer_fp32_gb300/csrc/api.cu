@@ -406,6 +406,33 @@ int moe_read_status(const void* ws, size_t ws_bytes, int32_t* host_status, int32
     return MOE_OK;
 }
 
+// Host <-> device activation copies of a step: one cudaMemcpyAsync each, on
+// the step's stream, so that a caller holding host buffers goes through the
+// library from input to output.
+static int host_copy_checks(const void* dev, const void* host, int T, int d, const char* who) {
+    if (!dev || !host) return fail(MOE_ERR_INVALID_ARG, "%s: null pointer", who);
+    if (T < 1 || d < 1) return fail(MOE_ERR_INVALID_ARG, "%s: T=%d, d=%d must be >= 1", who, T, d);
+    return MOE_OK;
+}
+
+int moe_input_from_host(float* x, const float* x_host, int T, int d, void* stream) {
+    const char* who = "moe_input_from_host";
+    int rc = host_copy_checks(x, x_host, T, d, who);
+    if (rc) return rc;
+    cudaError_t e = cudaMemcpyAsync(x, x_host, (size_t)T * d * sizeof(float), cudaMemcpyHostToDevice,
+                                    as_stream(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, who);
+}
+
+int moe_output_to_host(float* y_host, const float* y, int T, int d, void* stream) {
+    const char* who = "moe_output_to_host";
+    int rc = host_copy_checks(y, y_host, T, d, who);
+    if (rc) return rc;
+    cudaError_t e = cudaMemcpyAsync(y_host, y, (size_t)T * d * sizeof(float), cudaMemcpyDeviceToHost,
+                                    as_stream(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, who);
+}
+
 int moe_route_topk(const float* x, const float* w_router, const float* bias, int T, int d, int n,
                    int k, float scale, int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes,
                    void* stream) {

@@ -169,6 +169,19 @@ def test_grouped_routing_rejects_bad_group_arguments(B):
         assert lib.moe_route_topk_grouped(*args(g, kd, strict, k)) == -1
 
 
+def test_host_activation_copies_reject_bad_arguments(B):
+    lib = B.lib()
+    for fn in (lib.moe_input_from_host, lib.moe_output_to_host):
+        assert fn(None, FAKE, 4, 256, None) == -1
+        assert fn(FAKE, None, 4, 256, None) == -1
+        assert fn(FAKE, FAKE, 0, 256, None) == -1
+        assert fn(FAKE, FAKE, 4, 0, None) == -1
+        assert b"T=4, d=0" in lib.moe_last_error()
+    import torch
+    with pytest.raises(ValueError):   # shapes that differ
+        B.moe_output_to_host(torch.zeros(2, 8), torch.zeros(2, 4))
+
+
 def test_bias_update_rejects_bad_arguments_on_the_host(B):
     lib = B.lib()
     assert lib.moe_bias_update(FAKE, 0, 0.1, 0, FAKE, None, None) == -1

@@ -569,6 +569,29 @@ def test_one_workspace_for_routing_calls_and_smaller_steps(B):
         assert H.rel_err(yt.cpu().numpy(), ref) <= H.TOL[shape.dtype]
 
 
+def test_layer_with_host_activations_through_the_abi(B):
+    """moe_input_from_host -> layer -> moe_output_to_host: both copies are
+    exact, and the layer matches the same layer on device buffers (to the
+    rounding of its fp32 atomics), for each batch size of the default workload."""
+    shape = synth.VANILLA_128E
+    L = synth.make_layer(shape, 3, DEV)
+    for T in (1, 4, 16):
+        x = synth.hidden(T, shape.d, 3 + T, DEV)
+        _, _, _, y_dev = H.run_layer_forward(B, shape, L, x)
+        x_host = x.cpu().pin_memory()
+        y_host = torch.full((T, shape.d), float("nan")).pin_memory()
+        x_in = torch.full_like(x, float("nan"))
+        B.moe_input_from_host(x_in, x_host)
+        _, _, _, y = H.run_layer_forward(B, shape, L, x_in)
+        B.moe_output_to_host(y_host, y)
+        torch.cuda.synchronize()
+        assert torch.equal(x_in, x)
+        assert torch.equal(y_host, y.cpu())
+        assert H.rel_err(y_host.numpy(), y_dev.cpu().numpy()) <= 1e-6
+    with pytest.raises(ValueError):
+        B.moe_input_from_host(x_in, x_host[:, :8].contiguous())
+
+
 def test_repeated_calls_reuse_workspace(B):
     shape = synth.VANILLA_128E
     L = synth.make_layer(shape, 3, DEV)
