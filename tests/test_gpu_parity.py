@@ -167,6 +167,31 @@ def test_route_grouped_exact_ties(B, strict):
             np.testing.assert_allclose(gw, op, rtol=1e-6)
 
 
+@pytest.mark.parametrize("strict", [False, True], ids=["soft", "strict"])
+def test_route_grouped_wide_router_ties_and_bits(B, strict):
+    """More than 512 experts (20-21 keys per lane of the selecting warp), one or
+    two tokens: every tie is broken by index as in the oracle, and a token's
+    indices and weights do not depend on the other tokens of its step."""
+    d, n, g = 16, 640, 80
+    for T in (1, 2):
+        x = torch.ones((T, d), device=DEV)
+        wr = torch.zeros((n, d), device=DEV)
+        for bias in (None, torch.tensor([float((e // g) % 3) for e in range(n)], device=DEV)):
+            for k, k_dept in ((8, 2), (5, 5), (20, 3)):
+                gi, gw = grouped_on_gpu(B, x, wr, bias, k, g, k_dept, strict)
+                oi, op, _ = O.route_grouped(x, wr, k, g, k_dept, bias=bias, strict=strict)
+                np.testing.assert_array_equal(gi, oi)
+                np.testing.assert_allclose(gw, op, rtol=1e-6)
+    d, n, g, k, k_dept = 1024, 672, 84, 10, 4
+    wr = synth.router(d, n, 5, DEV)
+    bias = synth.zipf_bias(n, g, 1.1, 5).to(DEV)
+    x3 = synth.hidden(3, d, 5, DEV)
+    i1, w1 = grouped_on_gpu(B, x3[:1].contiguous(), wr, bias, k, g, k_dept, strict)
+    i3, w3 = grouped_on_gpu(B, x3, wr, bias, k, g, k_dept, strict)
+    np.testing.assert_array_equal(i1[0], i3[0])
+    assert np.array_equal(w1[0].view(np.uint32), w3[0].view(np.uint32))
+
+
 def test_route_grouped_hand_example(B):
     # the oracle pin's example: logits [5, 1 | 4.9, 0 | 4.8, 4.7 | 0, 0] and
     # [5, 4.9 | 4.8, 4.7 | 1, 0 | 0.5, 0.2] (x = e_0, d padded to 8)
