@@ -35,3 +35,16 @@ def test_reference_arm_prints_the_contract_line(workload):
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and isinstance(cb["sample"], str)
     assert cb["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_our_arm_fails_loudly_without_a_gpu():
+    """No GPU: the CUDA arm exits non-zero and prints no result line (there is
+    no CPU fallback to report instead)."""
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    out = subprocess.run([sys.executable, "bench.py", "--steps", "1", "--warmup", "1", "--no-cpu-baseline"],
+                         cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert out.returncode != 0
+    assert not [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
