@@ -257,7 +257,9 @@ __device__ __forceinline__ uint32_t ordered_key(float v) {
 // Lane holds experts lane + 32*j of logits_row[0..n) (J*32 >= n, k <= n).
 // On return lane r < k holds the r-th selected expert and its weight; the
 // result (same on every lane) says whether a non-finite key was selected.
-template <int J>
+// SMEM: logits_row points to shared memory (plain loads) instead of global
+// memory (L2 loads).
+template <int J, bool SMEM = false>
 __device__ __forceinline__ bool topk_select_warp(const float* logits_row, const float* bias, int n,
                                                  int k, float scale, int& out_idx, float& out_w) {
     const int lane = threadIdx.x & 31;
@@ -270,7 +272,7 @@ __device__ __forceinline__ bool topk_select_warp(const float* logits_row, const 
         lg[j] = 0.0f;
         key[j] = 0u;
         if (e < n) {
-            const float l = __ldcg(logits_row + e);
+            const float l = SMEM ? logits_row[e] : __ldcg(logits_row + e);
             const float kv = bias ? l + __ldg(bias + e) : l;
             lg[j] = l;
             // finite keys rank above kLowest; -inf and NaN take kLowest (still
@@ -337,7 +339,7 @@ __device__ __forceinline__ bool topk_select_warp(const float* logits_row, const 
 // expert is never a leader and a new leader is never replaced.  Either way the
 // selected experts come out by descending key.  Same lane layout and result as
 // topk_select_warp (k <= k_dept * g; strict needs k >= k_dept).
-template <int J>
+template <int J, bool SMEM = false>
 __device__ __forceinline__ bool topk_select_warp_grouped(const float* logits_row, const float* bias, int n,
                                                          int k, int g, int k_dept, bool strict, float scale,
                                                          int& out_idx, float& out_w) {
@@ -351,7 +353,7 @@ __device__ __forceinline__ bool topk_select_warp_grouped(const float* logits_row
         lg[j] = 0.0f;
         key[j] = 0u;
         if (e < n) {
-            const float l = __ldcg(logits_row + e);
+            const float l = SMEM ? logits_row[e] : __ldcg(logits_row + e);
             const float kv = bias ? l + __ldg(bias + e) : l;
             lg[j] = l;
             key[j] = (kv == kv && kv != -INFINITY) ? ordered_key(kv) : kLowest;

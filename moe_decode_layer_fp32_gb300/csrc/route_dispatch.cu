@@ -173,7 +173,7 @@ __device__ void dispatch_block(const int32_t* idx, const float* wts, int T, int 
 // the shared-memory copy the fused dispatch reads, when given).
 // GROUPED: the selection is group-limited (k_dept departments of g experts
 // at most; strict: exactly k_dept).
-template <int J, bool GROUPED>
+template <int J, bool GROUPED, bool SMEM = false>
 __device__ void topk_warp(const float* logits_row, const float* bias, int n, int k, float scale,
                           int g, int k_dept, bool strict, int32_t* idx_out, float* w_out,
                           int32_t* status, int32_t* idx_sm, float* w_sm) {
@@ -181,8 +181,8 @@ __device__ void topk_warp(const float* logits_row, const float* bias, int n, int
     int e;
     float wv;
     const bool bad = GROUPED
-                         ? topk_select_warp_grouped<J>(logits_row, bias, n, k, g, k_dept, strict, scale, e, wv)
-                         : topk_select_warp<J>(logits_row, bias, n, k, scale, e, wv);
+                         ? topk_select_warp_grouped<J, SMEM>(logits_row, bias, n, k, g, k_dept, strict, scale, e, wv)
+                         : topk_select_warp<J, SMEM>(logits_row, bias, n, k, scale, e, wv);
     if (lane < k) {
         idx_out[lane] = e;
         w_out[lane] = wv;
@@ -194,31 +194,40 @@ __device__ void topk_warp(const float* logits_row, const float* bias, int n, int
     if (bad && lane == 0) set_status(status, kDevErrRouting);
 }
 
-// Top-k of tokens [t0, t1), one warp per token.
+// Top-k of tokens [t0, t1), one warp per token.  For the group-limited
+// selection from 16 keys a lane on, `lsm` (when given) holds the tokens'
+// logits in shared memory, row t - t0: a warp's loads from L2 there come
+// one round trip after another.
 template <int J, bool GROUPED>
 __device__ __forceinline__ void topk_rows(const RouteArgs& a, int warp, int t0, int t1, int32_t* idx_sm,
-                                          float* w_sm) {
-    for (int t = t0 + warp; t < t1; t += kRouteWarps)
+                                          float* w_sm, const float* lsm) {
+    for (int t = t0 + warp; t < t1; t += kRouteWarps) {
+        int32_t* io = a.topk_idx + (size_t)t * a.k;
+        float* wo = a.topk_w + (size_t)t * a.k;
+        int32_t* is = idx_sm ? idx_sm + t * a.k : nullptr;
+        float* ws_ = idx_sm ? w_sm + t * a.k : nullptr;
+        if constexpr (GROUPED && J >= 16) {
+            if (lsm) {
+                topk_warp<J, GROUPED, true>(lsm + (size_t)(t - t0) * a.n, a.bias, a.n, a.k, a.scale, a.route_g,
+                                            a.k_dept, a.strict != 0, io, wo, a.ws.status, is, ws_);
+                continue;
+            }
+        }
         topk_warp<J, GROUPED>(a.ws.logits + (size_t)t * a.n, a.bias, a.n, a.k, a.scale, a.route_g, a.k_dept,
-                     a.strict != 0, a.topk_idx + (size_t)t * a.k, a.topk_w + (size_t)t * a.k, a.ws.status,
-                     idx_sm ? idx_sm + t * a.k : nullptr, idx_sm ? w_sm + t * a.k : nullptr);
+                              a.strict != 0, io, wo, a.ws.status, is, ws_);
+    }
 }
 
-template <int J, bool GROUPED>
-__device__ __forceinline__ void topk_range(const RouteArgs& a, int warp, int t0, int t1, int32_t* idx_sm,
-                                           float* w_sm) {
-    topk_rows<J, GROUPED>(a, warp, t0, t1, idx_sm, w_sm);
-}
 template <bool GROUPED>
 __device__ __forceinline__ void topk_any(const RouteArgs& a, int warp, int t0, int t1, int32_t* idx_sm,
-                                         float* w_sm) {
+                                         float* w_sm, const float* lsm) {
     const int J = (a.n + 31) / 32;
-    if (J <= 1) topk_range<1, GROUPED>(a, warp, t0, t1, idx_sm, w_sm);
-    else if (J <= 2) topk_range<2, GROUPED>(a, warp, t0, t1, idx_sm, w_sm);
-    else if (J <= 4) topk_range<4, GROUPED>(a, warp, t0, t1, idx_sm, w_sm);
-    else if (J <= 8) topk_range<8, GROUPED>(a, warp, t0, t1, idx_sm, w_sm);
-    else if (J <= 16) topk_range<16, GROUPED>(a, warp, t0, t1, idx_sm, w_sm);
-    else topk_range<32, GROUPED>(a, warp, t0, t1, idx_sm, w_sm);
+    if (J <= 1) topk_rows<1, GROUPED>(a, warp, t0, t1, idx_sm, w_sm, nullptr);
+    else if (J <= 2) topk_rows<2, GROUPED>(a, warp, t0, t1, idx_sm, w_sm, nullptr);
+    else if (J <= 4) topk_rows<4, GROUPED>(a, warp, t0, t1, idx_sm, w_sm, nullptr);
+    else if (J <= 8) topk_rows<8, GROUPED>(a, warp, t0, t1, idx_sm, w_sm, nullptr);
+    else if (J <= 16) topk_rows<16, GROUPED>(a, warp, t0, t1, idx_sm, w_sm, lsm);
+    else topk_rows<32, GROUPED>(a, warp, t0, t1, idx_sm, w_sm, lsm);
 }
 
 // Router logits: block (expert group, token block) computes the logits of EB
@@ -358,7 +367,19 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
     // the fused dispatch reads the top-k results from shared memory when one
     // block picked them all and they fit
     const bool staged = a.fuse_dispatch && !split && a.T * a.k <= kStagedAssignments;
-    topk_any<GROUPED>(a, warp, split ? t0 : 0, split ? min(t0 + 8, a.T) : a.T, staged ? s_idx : nullptr, s_w);
+    // Wide group-limited routers: the block first copies the tokens' logits into shared
+    // memory (the dispatch's, free until the dispatch starts) in one parallel
+    // round trip, so the selecting warps read them from there.
+    const int tt0 = split ? t0 : 0, tt1 = split ? min(t0 + 8, a.T) : a.T;
+    const float* lsm = nullptr;
+    if (GROUPED && a.n > 512 && (tt1 - tt0) * a.n <= kMaxN * kMaskWords) {
+        float* st = reinterpret_cast<float*>(sm.emask);
+        const float* src = a.ws.logits + (size_t)tt0 * a.n;
+        for (int i = tid; i < (tt1 - tt0) * a.n; i += kRouteThreads) st[i] = __ldcg(src + i);
+        __syncthreads();
+        lsm = st;
+    }
+    topk_any<GROUPED>(a, warp, tt0, tt1, staged ? s_idx : nullptr, s_w, lsm);
     if (tid == 0) a.ws.sync[ctr] = 0u;  // ready for the next call
     if (!a.fuse_dispatch) return;
     // With a split top-k the last token block to finish builds the dispatch;
