@@ -17,9 +17,12 @@
  * Conventions (all entry points):
  *   - Every pointer argument is a DEVICE pointer owned by the caller, unless a
  *     parameter says "host".  The library never allocates, frees or
- *     synchronises inside a step; all scratch lives in the caller's workspace.
+ *     synchronises inside a step; all scratch lives in the caller's workspace
+ *     (moe_route_topk_noalloc, which has none, uses the library's own fixed
+ *     array instead; its declaration states its own terms).
  *   - Every step is asynchronous on the given stream (a cudaStream_t passed as
- *     void*; NULL = legacy default stream) and may be captured in a CUDA graph.
+ *     void*; NULL = legacy default stream).  The workspace steps may be
+ *     captured in a CUDA graph.
  *   - Activations, router weights, routing weights and outputs are fp32.
  *     Expert weights are fp32 or bf16 (MOE_DTYPE_*), row-major.
  *   - Weight layout (per unit: an expert, a department backbone, a private
@@ -236,8 +239,11 @@ int moe_route_topk_grouped(const float* x, const float* w_router, const float* b
  * holds 65536 fp32 logits, 256 KB); larger steps return MOE_ERR_UNSUPPORTED
  * and launch nothing.
  * Set-up: the first call on each device looks up the scratch's device address
- * (cudaGetSymbolAddress) and remembers it; make that first call before any
- * stream capture.
+ * (cudaGetSymbolAddress) and remembers it for the life of the process; make
+ * that first call before any stream capture.  The address remembered is the
+ * one in the device's primary context (the runtime's context): calls from
+ * another context on the same device, or after cudaDeviceReset, are not
+ * supported.
  * Each call clears the scratch's status word and counter (stream-ordered)
  * before its kernel runs.  There is one scratch per device and process:
  * calls that overlap on the device (other streams, other host threads) race

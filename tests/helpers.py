@@ -11,6 +11,12 @@ from oracle import moe_oracle as O
 
 # Output tolerances: max|y - y_ref| / max|y_ref| per output tensor.
 TOL = {"bf16": 2e-2, "f32": 1e-4}
+# The kernels' own accuracy, checked beside TOL: they compute in fp32 on the
+# exactly decoded weights (the tensor-core kernel on bf16 hi + lo parts of the
+# activations and of H, exact to about 2^-17), so every output lands within
+# 1e-4 of the oracle whatever the weight storage.  A dropped intermediate row,
+# token or department term moves the output by about 1e-2 and fails it.
+KERNEL_TOL = 1e-4
 
 
 def ensure_built():

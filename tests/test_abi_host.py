@@ -153,6 +153,18 @@ def test_unique_bytes_match_oracle_formula(B):
     assert B.moe_unique_weight_bytes_vanilla(2048, 128, 768, 0, 9, 8) == -1
 
 
+def test_unique_bytes_formp_match_oracle_formula(B):
+    """The library's form-P count (bf16 weights) equals the oracle's, whose
+    closed form is pinned to the bytes of the tensors an evaluation touches."""
+    for (d, n, r, A_d, A_e) in [(256, 16, 64, 2, 4), (1024, 672, 384, 4, 10), (1024, 672, 384, 8, 383),
+                                (7168, 864, 2048, 5, 10), (7168, 864, 2048, 8, 416), (2048, 64, 1024, 0, 0)]:
+        assert B.moe_unique_weight_bytes_formp(d, n, r, A_d, A_e) == \
+            O.unique_bytes_deamoe_p(d, n, r, A_d, A_e, 2)
+    lib = B.lib()
+    for bad in ((0, 16, 64, 1, 1), (256, 16, 0, 1, 1), (256, 16, 64, -1, 1), (256, 16, 64, 1, 17)):
+        assert lib.moe_unique_weight_bytes_formp(*bad) == -1
+
+
 # ---------------------------------------------------------------------------
 # Host checks of the NEXT-row entry points (nothing is launched)
 # ---------------------------------------------------------------------------

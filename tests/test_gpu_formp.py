@@ -50,13 +50,25 @@ def check_formp(B, shape, T, seed, k_dept, sample=None):
     L = synth.make_layer(shape, seed, DEV)
     x = synth.hidden(T, shape.d, seed + 7 * T, DEV)
     ws, gi, gw, y = run_formp(B, shape, L, x, k_dept)
-    assert B.moe_read_status(ws)[0] == 0
+    st, A_e, A_d = B.moe_read_status(ws)
+    assert st == 0
     if k_dept:
         oi, op, info = O.route_grouped(x, L["router"], shape.k, shape.g, k_dept, bias=L["bias"])
         ties = H.compare_grouped_routing(gi, gw, oi, op, info, x, L["router"], shape.g, k_dept, False)
     else:
         oi, op, info = O.route(x, L["router"], shape.k, bias=L["bias"])
         ties = H.compare_routing(gi, gw, oi, op, info, x, L["router"])
+    # the device's active counts are those of the routing it took, and the
+    # library's byte count on them is the bytes of the tensors that routing
+    # touches (router, department matrices, A-matrices)
+    depts = sorted({int(e) // shape.g for e in gi.ravel()})
+    experts = sorted({int(e) for e in gi.ravel()})
+    assert (A_d, A_e) == (len(depts), len(experts))
+    touched = L["router"].numel() * 4 + sum(
+        L[key][u].numel() * L[key].element_size()
+        for keys, units in ((("dgate", "dup", "ddown"), depts), (("agate", "aup", "adown"), experts))
+        for key in keys for u in units)
+    assert B.moe_unique_weight_bytes_formp(shape.d, shape.n, shape.I_sh, A_d, A_e) == touched
     # a token whose selection differs at a certified fp32 near-tie (either
     # choice is correct) has no single expected output: it is left out
     tokens = [t for t in (range(T) if sample is None else sample) if t not in ties]

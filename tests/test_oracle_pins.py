@@ -685,6 +685,40 @@ def test_unique_bytes_matches_touched_tensors():
     assert Uv == 4 * 2048 * 128 + 2 * 3 * 2048 * (10 * 768 + 256)
 
 
+def test_unique_bytes_formp_matches_touched_tensors():
+    """Form P: the closed-form byte count equals the bytes of the tensors one
+    literal evaluation of eq. (4) touches -- the fp32 router, the three
+    [r, h] department matrices of every department a token reaches and the
+    three [r, r] A-matrices of every selected expert ([DeaMoE] §3.1, §3.3)."""
+    shape = synth.TINY_FORMP
+    L = synth.make_layer(shape, seed=2)
+    for T, k_dept in ((1, 2), (5, 2), (9, 0)):
+        x = synth.hidden(T, shape.d, seed=T)
+        if k_dept:
+            idx, p, _ = O.route_grouped(x, L["router"], shape.k, shape.g, k_dept)
+        else:
+            idx, p, _ = O.route(x, L["router"], shape.k)
+        depts = sorted({int(e) // shape.g for e in idx.ravel()})
+        experts = sorted({int(e) for e in idx.ravel()})
+        touched = L["router"].numel() * L["router"].element_size()
+        for j in depts:
+            touched += sum(L[key][j].numel() * L[key].element_size() for key in ("dgate", "dup", "ddown"))
+        for e in experts:
+            touched += sum(L[key][e].numel() * L[key].element_size() for key in ("agate", "aup", "adown"))
+        D = O.dispatch(idx, p, shape.n, shape.g)
+        assert list(D["active_depts"]) == depts and list(D["active_experts"]) == experts
+        U = O.unique_bytes_deamoe_p(shape.d, shape.n, shape.I_sh, len(D["active_depts"]),
+                                    len(D["active_experts"]), 2)
+        assert U == touched, (T, k_dept, U, touched)
+    # a department reached by several experts of one token is read once: one
+    # token, every selected expert in department 0 (k_dept = 1)
+    idx = np.arange(shape.k, dtype=np.int32)[None, :]
+    D = O.dispatch(idx, np.ones((1, shape.k)), shape.n, shape.g)
+    assert len(D["active_depts"]) == 1
+    assert O.unique_bytes_deamoe_p(shape.d, shape.n, shape.I_sh, 1, shape.k, 2) == (
+        4 * shape.d * shape.n + 2 * 3 * shape.I_sh * (shape.d + shape.k * shape.I_sh))
+
+
 # ---------------------------------------------------------------------------
 # FP8 (E4M3) weights with per-row scales
 # ---------------------------------------------------------------------------

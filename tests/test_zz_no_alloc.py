@@ -70,5 +70,5 @@ def test_noalloc_matches_workspace_entry_point(B, d, n, k, T, with_bias, scale):
         torch.cuda.synchronize()
         assert int(status.item()) == 0, f"call {call}: device status {int(status.item())}"
         assert torch.equal(idx.cpu(), idx_ref.cpu()), f"call {call}: expert indices differ"
-        err = H.rel_err(w.cpu().numpy(), w_ref.cpu().numpy())
-        assert err <= H.TOL["f32"], f"call {call}: weights rel err {err}"
+        # the same routing kernel on the same inputs: the weights agree bit for bit
+        assert torch.equal(w.cpu(), w_ref.cpu()), f"call {call}: routing weights differ"
