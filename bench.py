@@ -2,19 +2,29 @@
 """MoE decode-layer benchmark: µs per layer-step and achieved HBM GB/s over
 the unique weight bytes a step must read, on one GB300 (or N replicas).
 
-Default workload: the vanilla MoE decode layer d=2048, 128 routed experts,
-SwiGLU intermediate 768, top-8 softmax-renormalised routing, bf16 expert
-weights, fp32 router, no shared expert, at batches T in {1, 4, 16}.  A step is
-one decode-layer pass (route -> dispatch -> expert FFN -> combine) at each of
-the three batch sizes.  Consecutive steps use different layer replicas
-(distinct weights and inputs), so the bytes touched between two uses of the
-same replica exceed the 129 MB L2 many times over: weights are read cold.
+Default step (the suite): one decode-layer pass (route -> dispatch -> expert
+FFN -> combine, as the library's whole-layer calls run it) of every layer of
+the synthetic configurations, each at its batch sizes --
+  * vanilla MoE, d=2048, 128 experts, I=768, top-8, bf16: T = 1, 4, 16;
+  * DeaMoE ~7B (8 departments of 8, I_sh=1024, I_pr=128, top-8) and its
+    budget-matched vanilla twin (64 experts, I=1152): T = 1, 4, 8, 16;
+  * DeepSeek-V3-shaped vanilla (256 experts, I=2048, top-8, shared expert
+    2048) and DeaMoE (16 departments of 16, I_sh=1792, I_pr=256, same shared
+    expert): T = 1, 8, 32, 64;
+  * the 7B pair under Zipf(1.1)-skewed routing: T = 1, 2, 4, ..., 128.
+Expert weights bf16, router and activations fp32.  Consecutive steps use
+different layer replicas (distinct weights and inputs), so the bytes touched
+between two uses of a replica exceed the 129 MB L2 many times over: weights
+are read cold.
 
 value = unique weight bytes of all timed layer passes / device time (GB/s).
+per_batch gives, per layer and batch size, µs per layer, unique MB, GB/s, the
+fraction of the measured HBM bandwidth and each stage alone; next_rows the
+same for the matrix form P and FP8 weights (not part of the step).
 Inputs are synthetic (seeded), see moe_decode_layer_fp32_gb300.synth.
 
---impl reference times the CPU oracle (the reference arm of this build) on
-bounded samples of the same workload.
+--workload NAME times one layer alone.  --impl reference times the CPU oracle
+(the reference arm of this build) on bounded samples of the same workloads.
 """
 
 from __future__ import annotations
@@ -50,6 +60,14 @@ WORKLOADS = {
     "vanilla-128e-fp8": synth.VANILLA_128E_FP8,
     "deamoe-7b-fp8": synth.DEAMOE_7B_FP8,
 }
+# The default step: every layer of the five configurations that is not a
+# correctness case -- the vanilla 128-expert layer, the DeaMoE ~7B layer and its
+# budget-matched vanilla twin, the DeepSeek-V3-shaped vanilla and DeaMoE layers,
+# and the Zipf-skewed sweep of both 7B layers.
+SUITE = ("vanilla-128e", "deamoe-7b", "vanilla-7b", "dsv3-vanilla", "dsv3-deamoe", "zipf-deamoe", "zipf-vanilla")
+# Timed after the step, per batch size, outside `value`: the matrix form P at
+# its Table 1 shapes next to its baseline, and FP8 weights.
+NEXT = ("formp-7b", "formp-dsv3", "dsv3-routed", "vanilla-128e-fp8", "deamoe-7b-fp8")
 METRIC = "MoE-layer decode µs and achieved HBM GB/s (unique weight bytes) at batch 1–64"
 L2_BYTES = 129 * 2 ** 20
 
@@ -57,10 +75,12 @@ L2_BYTES = 129 * 2 ** 20
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=2000)
-    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    p.add_argument("--workload", choices=sorted(WORKLOADS), default="vanilla-128e")
+    p.add_argument("--workload", choices=["suite"] + sorted(WORKLOADS), default="suite",
+                   help="suite (default): one step runs every layer of " + ", ".join(SUITE))
+    p.add_argument("--no-next", action="store_true", help="skip the NEXT rows' per-batch timings")
     p.add_argument("--batches", type=str, default="", help="comma list overriding the workload's batches")
     p.add_argument("--replicas", type=int, default=0, help="layer replicas (0 = enough for cold L2)")
     p.add_argument("--seed", type=int, default=0)
@@ -362,150 +382,234 @@ def time_graphs(graphs, order, world, device):
     return max_over_ranks(start.elapsed_time(end) / 1e3, world, device)
 
 
+def replicas_for(shape, R_arg: int) -> int:
+    """Layer replicas so that the bytes between two uses of one replica exceed
+    4x L2 (from the smallest pass: one token, k experts, one department)."""
+    bw = {"bf16": 2, "f32": 4, "fp8": 1}[shape.dtype]
+    per_layer_min = (bw * 3 * (shape.d * shape.I_sh + shape.I_sh * shape.I_sh * shape.k) if shape.form_p else
+                     bw * 3 * shape.d * (shape.I_pr * shape.k + shape.I_sh + shape.I * shape.k + shape.I_s))
+    return R_arg or max(2, min(16, -(-4 * L2_BYTES // max(1, per_layer_min))))
+
+
+def stage_fns(W, T, scratch):
+    """Each stage alone over the replicas: routing with its top-k, dispatch,
+    the FFN step, and the NEXT rows on the same inputs (group-limited routing
+    soft and strict, router-bias update) for the layers that have them."""
+    R = W.R
+    fns = [("route_topk", lambda: [W.route_only(r, T) for r in range(R)]),
+           ("ffn", lambda: [W.ffn_only(r, T, scratch[r]) for r in range(R)])]
+    if not W.shape.form_p:
+        fns.insert(1, ("dispatch", lambda: [W.dispatch_only(r, T) for r in range(R)]))
+        fns += [("route_topk_grouped", lambda: [W.grouped_only(r, T, False) for r in range(R)]),
+                ("route_topk_grouped_strict", lambda: [W.grouped_only(r, T, True) for r in range(R)]),
+                ("bias_update", lambda: [W.bias_only(r, T) for r in range(R)])]
+    return fns
+
+
+def measure_batches(W, args, world, device, peak):
+    """Per batch size of one workload: µs per layer (graphs of its replicas),
+    unique bytes, GB/s, fraction of the HBM peak, and each stage alone."""
+    B, shape, R = W.B, W.shape, W.R
+    per_batch = {}
+    reps = max(3, min(200, args.steps // max(1, R)))
+    for T in W.batches:
+        gT = capture(lambda T=T: [W.layer(r, T) for r in range(R)])
+        time_graphs([gT], [0] * 3, world, device)
+        us = time_graphs([gT], [0] * reps, world, device) / (reps * R) * 1e6
+        U = sum(W.unique[(r, T)] for r in range(R)) / R
+        Uf = sum(W.ffn_bytes[(r, T)] for r in range(R)) / R
+        stage_us = {}
+        scratch_T = {r: torch.zeros_like(W.y[(r, T)]) for r in range(R)}
+        for name, fn in stage_fns(W, T, scratch_T):
+            gs = capture(fn)
+            time_graphs([gs], [0] * 3, world, device)
+            stage_us[name] = round(time_graphs([gs], [0] * reps, world, device) / (reps * R) * 1e6, 2)
+        if shape.form_p:
+            paths = ["formp passes"]
+        else:
+            paths = sorted({("tensor-core" if W.choice[(r, T)] == 2 else
+                             "cuda-core" if W.choice[(r, T)] == 1 or not W.tc_launched((r, T), args.tc_min_tokens)
+                             else "split") for r in range(R)})
+        e = {"us_per_layer": round(us, 2), "unique_MB": round(U / 1e6, 2), "GBps": round(U / us / 1e3, 1),
+             "frac": round(U / us / 1e3 / peak, 4),
+             "ffn_us": stage_us["ffn"], "ffn_frac": round(Uf / stage_us["ffn"] / 1e3 / peak, 4),
+             "stage_us": stage_us, "ffn_path": "/".join(paths),
+             "active_experts": round(sum(W.counts[(r, T)][0] for r in range(R)) / R, 2)}
+        if shape.I_sh > 0:
+            e["active_depts"] = round(sum(W.counts[(r, T)][1] for r in range(R)) / R, 2)
+        if not shape.form_p:
+            e["grouped_routing"] = f"{W.k_dept} of {shape.n // W.rg} groups of {W.rg}"
+            e["imbalance"] = round(sum(W.imbalance[(r, T)].item() for r in range(R)) / R, 3)
+        per_batch[str(T)] = e
+    return per_batch
+
+
 def run_ours(args, rank, world, local):
     from moe_decode_layer_fp32_gb300 import binding as B
     B.lib()  # fails loudly when the native library is missing
     B.moe_set_tc_min_tokens(args.tc_min_tokens)
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    shape = WORKLOADS[args.workload]
-    batches = tuple(int(b) for b in args.batches.split(",")) if args.batches else shape.batches
+    names = SUITE if args.workload == "suite" else (args.workload,)
+    override = tuple(int(b) for b in args.batches.split(",")) if args.batches else None
+    peaks = load_peaks()
+    peak = peaks["hbm_gbs"]
 
-    # Replicas: enough that the bytes between two uses of a replica exceed 4x L2.
-    # (smallest pass: one token, k experts, one department)
-    bw = {"bf16": 2, "f32": 4, "fp8": 1}[shape.dtype]
-    per_layer_min = (bw * 3 * (shape.d * shape.I_sh + shape.I_sh * shape.I_sh * shape.k) if shape.form_p else
-                     bw * 3 * shape.d * (shape.I_pr * shape.k + shape.I_sh + shape.I * shape.k + shape.I_s))
-    R = args.replicas or max(2, min(16, -(-4 * L2_BYTES // max(1, per_layer_min))))
-    W = Workload(B, shape, batches, R, args.seed + 17 * rank, device)
+    # one Workload per layer of the step: its replicas, inputs and workspaces
+    Ws = []
+    for name in names:
+        shape = WORKLOADS[name]
+        Ws.append(Workload(B, shape, override or shape.batches, replicas_for(shape, args.replicas),
+                           args.seed + 17 * rank, device))
+        Ws[-1].name = name
 
     # first pass (eager), then device counts -> unique bytes
-    for r in range(R):
-        for T in batches:
-            W.layer(r, T)
+    for W in Ws:
+        for r in range(W.R):
+            for T in W.batches:
+                W.layer(r, T)
     torch.cuda.synchronize()
-    W.account()
+    for W in Ws:
+        W.account()
 
-    # one graph per replica: a step = one layer pass at every batch size
-    graphs = [capture(lambda r=r: [W.layer(r, T) for T in batches]) for r in range(R)]
-    time_graphs(graphs, [i % R for i in range(args.warmup)], world, device)
+    # a step = one layer pass at every batch size of every workload; step i
+    # runs replica i % R of each workload (one graph per workload and replica)
+    graphs = [[capture(lambda W=W, r=r: [W.layer(r, T) for T in W.batches]) for r in range(W.R)] for W in Ws]
+    flat = [g for gs in graphs for g in gs]
+    index = {(w, r): sum(len(gs) for gs in graphs[:w]) + r for w, gs in enumerate(graphs) for r in range(len(gs))}
 
+    def order(steps):
+        return [index[(w, i % Ws[w].R)] for i in range(steps) for w in range(len(Ws))]
+
+    time_graphs(flat, order(args.warmup), world, device)
     clocks = ClockSampler(local)
     clocks.start()
-    t_step = time_graphs(graphs, [i % R for i in range(args.steps)], world, device)
+    t_step = time_graphs(flat, order(args.steps), world, device)
     clock_info = clocks.stop()
-    bytes_rank = sum(W.unique[(i % R, T)] for i in range(args.steps) for T in batches)
+    bytes_rank = sum(W.unique[(i % W.R, T)] for i in range(args.steps) for W in Ws for T in W.batches)
     bytes_all = sum_over_ranks(bytes_rank, world, device)
     value = bytes_all / t_step / 1e9
 
-    # per-batch µs per layer: graphs of the R replicas at one batch size
-    per_batch = {}
-    reps = max(3, min(200, args.steps // max(1, R)))
-    for T in batches:
-        gT = capture(lambda T=T: [W.layer(r, T) for r in range(R)])
-        time_graphs([gT], [0] * 3, world, device)
-        t = time_graphs([gT], [0] * reps, world, device)
-        us = t / (reps * R) * 1e6
-        U = sum(W.unique[(r, T)] for r in range(R)) / R
-        # each stage alone (route+top-k, dispatch, expert FFN), as graphs over the replicas
-        stage_us = {}
-        scratch_T = {r: torch.zeros_like(W.y[(r, T)]) for r in range(R)}
-        for name, fn in (("route_topk", lambda T=T: [W.route_only(r, T) for r in range(R)]),
-                         ("dispatch", lambda T=T: [W.dispatch_only(r, T) for r in range(R)]),
-                         ("ffn", lambda T=T: [W.ffn_only(r, T, scratch_T[r]) for r in range(R)]),
-                         ("route_topk_grouped", lambda T=T: [W.grouped_only(r, T, False) for r in range(R)]),
-                         ("route_topk_grouped_strict", lambda T=T: [W.grouped_only(r, T, True) for r in range(R)]),
-                         ("bias_update", lambda T=T: [W.bias_only(r, T) for r in range(R)])):
-            gs = capture(fn)
-            time_graphs([gs], [0] * 3, world, device)
-            stage_us[name] = round(time_graphs([gs], [0] * reps, world, device) / (reps * R) * 1e6, 2)
-        paths = sorted({("tensor-core" if W.choice[(r, T)] == 2 else
-                         "cuda-core" if W.choice[(r, T)] == 1 or not W.tc_launched((r, T), args.tc_min_tokens)
-                         else "split") for r in range(R)})
-        per_batch[str(T)] = {"us_per_layer": round(us, 2), "unique_MB": round(U / 1e6, 2),
-                             "GBps": round(U / us / 1e3, 1), "stage_us": stage_us,
-                             "grouped_routing": f"{W.k_dept} of {shape.n // W.rg} groups of {W.rg}",
-                             "imbalance": round(sum(W.imbalance[(r, T)].item() for r in range(R)) / R, 3),
-                             "ffn_path": "/".join(paths),
-                             "active_experts": round(sum(W.counts[(r, T)][0] for r in range(R)) / R, 2)}
-        if shape.I_sh > 0:
-            per_batch[str(T)]["active_depts"] = round(sum(W.counts[(r, T)][1] for r in range(R)) / R, 2)
+    per_workload = {W.name: measure_batches(W, args, world, device, peak) for W in Ws}
 
-    # roofline of the dominant kernel (the expert FFN): FFN launches alone, same inputs
-    scratch = {key: torch.zeros_like(y) for key, y in W.y.items()}
-    g_ffn = capture(lambda: [W.ffn_only(r, T, scratch[(r, T)]) for r in range(R) for T in batches])
-    time_graphs([g_ffn], [0] * 3, world, device)
-    reps_f = max(3, min(100, args.steps // max(1, R)))
-    t_ffn = time_graphs([g_ffn], [0] * reps_f, world, device)
-    ffn_launches = reps_f * R * len(batches)
-    ffn_bytes = reps_f * sum(W.ffn_bytes.values())
-    peaks = load_peaks()
+    # roofline of the dominant kernel (the expert FFN step): FFN launches
+    # alone over the same inputs, every workload of the step
+    reps_f = max(3, min(50, args.steps // 4))
+    t_ffn, ffn_launches, ffn_bytes = 0.0, 0, 0
+    for W in Ws:
+        scratch = {key: torch.zeros_like(y) for key, y in W.y.items()}
+        g_ffn = capture(lambda W=W, scratch=scratch: [W.ffn_only(r, T, scratch[(r, T)])
+                                                      for r in range(W.R) for T in W.batches])
+        time_graphs([g_ffn], [0] * 3, world, device)
+        t_ffn += time_graphs([g_ffn], [0] * reps_f, world, device)
+        ffn_launches += reps_f * W.R * len(W.batches)
+        ffn_bytes += reps_f * sum(W.ffn_bytes.values())
     achieved = ffn_bytes / t_ffn / 1e9
-    ffn_kernels = (["formp_kernel up / private / down passes"] if shape.form_p else
-                   sorted({"ffn_tc_kernel" if W.choice[key] == 2 else "ffn_stream_kernel" for key in W.ws}))
-    roofline = {"bound": "hbm", "kernel": "expert FFN step (" + ", ".join(ffn_kernels) + ")",
-                "achieved": round(achieved, 1),
-                "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4),
+    kernels = set()
+    for W in Ws:
+        kernels |= ({"formp_kernel up / private / down passes"} if W.shape.form_p else
+                    {"ffn_tc_kernel" if W.choice[key] == 2 else "ffn_stream_kernel" for key in W.ws})
+    fracs = [e["frac"] for pb in per_workload.values() for e in pb.values()]
+    roofline = {"bound": "hbm", "kernel": "expert FFN step (" + ", ".join(sorted(kernels)) + ")",
+                "achieved": round(achieved, 1), "peak": peak, "peak_source": peaks["source"], "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
                 "us_per_launch": round(t_ffn / ffn_launches * 1e6, 2),
-                "algorithmic_bytes_per_launch": int(sum(W.ffn_bytes.values()) / (R * len(batches))),
-                "traffic": load_traffic(args.workload) if not args.batches else None}
+                "algorithmic_bytes_per_launch": int(ffn_bytes / ffn_launches),
+                "traffic": load_traffic(args.workload) if not args.batches else None,
+                "layer_frac_mean": round(sum(fracs) / len(fracs), 4),
+                "layer_frac_min": min(fracs),
+                "per_workload": {name: {T: {"layer": e["frac"], "ffn": e["ffn_frac"]} for T, e in pb.items()}
+                                 for name, pb in per_workload.items()}}
 
     # end to end through the C ABI with host buffers (copies inside the timed region)
     e2e = None
     if not args.no_e2e:
-        hx = {key: x.cpu().pin_memory() for key, x in W.x.items()}
-        hy = {key: torch.empty(y.shape, dtype=y.dtype).pin_memory() for key, y in W.y.items()}
-        dx = {T: torch.empty((T, shape.d), device=device) for T in batches}
+        hx = [{key: x.cpu().pin_memory() for key, x in W.x.items()} for W in Ws]
+        hy = [{key: torch.empty(y.shape, dtype=y.dtype).pin_memory() for key, y in W.y.items()} for W in Ws]
+        dx = [{T: torch.empty((T, W.shape.d), device=device) for T in W.batches} for W in Ws]
+
+        def e2e_step(i):
+            for w, W in enumerate(Ws):
+                r = i % W.R
+                for T in W.batches:
+                    B.moe_input_from_host(dx[w][T], hx[w][(r, T)])
+                    W.layer(r, T, x=dx[w][T])
+                    B.moe_output_to_host(hy[w][(r, T)], W.y[(r, T)])
+
         ke = min(args.steps, 500)
         for i in range(min(args.warmup, 20)):
-            for T in batches:
-                B.moe_input_from_host(dx[T], hx[(i % R, T)])
-                W.layer(i % R, T, x=dx[T])
-                B.moe_output_to_host(hy[(i % R, T)], W.y[(i % R, T)])
+            e2e_step(i)
         barrier(world)
         torch.cuda.synchronize()
         s0 = torch.cuda.Event(enable_timing=True)
         s1 = torch.cuda.Event(enable_timing=True)
         s0.record()
         for i in range(ke):
-            r = i % R
-            for T in batches:
-                B.moe_input_from_host(dx[T], hx[(r, T)])
-                W.layer(r, T, x=dx[T])
-                B.moe_output_to_host(hy[(r, T)], W.y[(r, T)])
+            e2e_step(i)
         s1.record()
         torch.cuda.synchronize()
         barrier(world)
         te = max_over_ranks(s0.elapsed_time(s1) / 1e3, world, device)
-        be = sum_over_ranks(sum(W.unique[(i % R, T)] for i in range(ke) for T in batches), world, device)
-        io = sum(T * shape.d * 4 for T in batches)
+        be = sum_over_ranks(sum(W.unique[(i % W.R, T)] for i in range(ke) for W in Ws for T in W.batches),
+                            world, device)
+        io = sum(T * W.shape.d * 4 for W in Ws for T in W.batches)
         e2e = {"value": round(be / te / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": io,
                "d2h_bytes_per_step": io, "steps": ke, "ms_per_step": round(te / ke * 1e3, 4)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(W, shape, batches, args.cpu_seconds)
+        cpu = cpu_baseline(Ws, args.cpu_seconds)
 
+    # the NEXT rows (matrix form P at its Table 1 shapes beside its baseline,
+    # FP8 weights), timed per batch size alone: not part of the step above
+    next_rows = None
+    if args.workload == "suite" and not args.no_next:
+        next_rows = {}
+        for name in NEXT:
+            shape = WORKLOADS[name]
+            W = Workload(B, shape, override or shape.batches, replicas_for(shape, args.replicas),
+                         args.seed + 17 * rank, device)
+            W.name = name
+            for r in range(W.R):
+                for T in W.batches:
+                    W.layer(r, T)
+            torch.cuda.synchronize()
+            W.account()
+            next_rows[name] = measure_batches(W, args, world, device, peak)
+            del W
+            torch.cuda.empty_cache()
+
+    launches = sum(W.launches((i % W.R, T), args.tc_min_tokens) for i in range(args.steps) for W in Ws
+                   for T in W.batches)
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "weights_dtype": shape.dtype, "data": "synthetic",
-        "config": {**workload_config(shape, batches), "replicas": R,
-                   "tc_min_tokens": args.tc_min_tokens or "default",
-                   "l2": "inputs larger than L2: consecutive steps use distinct layer replicas "
-                         f"({R} replicas, >=4x L2 between reuses)",
+        "weights_dtype": "/".join(sorted({W.shape.dtype for W in Ws})), "data": "synthetic",
+        "config": {**suite_config(Ws), "tc_min_tokens": args.tc_min_tokens or "default",
+                   "l2": "inputs larger than L2: consecutive steps use distinct layer replicas of each "
+                         "workload (>=4x L2 between reuses of a replica)",
                    "parallelism": f"replicas x{world}"},
-        "per_batch": per_batch,
+        "per_batch": per_workload,
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": sum(W.launches((i % R, T), args.tc_min_tokens) for i in range(args.steps) for T in batches),
+        "gpu_launches": launches,
         "clocks": clock_info,
         "cpu_baseline": cpu,
     }
+    if next_rows is not None:
+        out["next_rows"] = next_rows
     if rank == 0:
         print(json.dumps(out))
+
+
+def suite_config(Ws):
+    """The `config` of a step over one or more workloads."""
+    if len(Ws) == 1:
+        W = Ws[0]
+        return {**workload_config(W.shape, W.batches), "replicas": W.R}
+    return {"workload": "; ".join(f"{W.shape.name} T={'/'.join(map(str, W.batches))}" for W in Ws),
+            "layers": {W.name: {**workload_config(W.shape, W.batches), "replicas": W.R} for W in Ws}}
 
 
 def workload_config(shape, batches):
@@ -546,67 +650,96 @@ def load_peaks():
 # --------------------------------------------------------------------------- oracle arms
 
 
-def cpu_baseline(W, shape, batches, budget_s):
-    """The oracle (as it stands) on a bounded sample of the same workload:
-    whole layer passes of replicas 0-1 at every batch size, repeated until the
-    budget is spent."""
+class _HostUnits:
+    """Host copies of the units of one [units, rows, d] device tensor, made
+    on request (outside the oracle's timed sections); FP8 units are decoded
+    exactly with their row scales.  Indexing returns the host copy."""
+
+    def __init__(self, O, dev, scales=None):
+        self.O, self.dev, self.scales, self.cache = O, dev, scales, {}
+
+    def fetch(self, u):
+        if u not in self.cache:
+            w = self.dev[u].cpu()
+            self.cache[u] = (w if self.scales is None else
+                             self.O.dequant_rows_e4m3(w, self.scales[u].cpu()))
+        return self.cache[u]
+
+    def __getitem__(self, u):
+        return self.cache[u]
+
+
+class _HostLayer(dict):
+    """The oracle's view of one device layer: router, bias and shared expert
+    copied whole, every other tensor per unit, only for the units a pass
+    touches (a DeepSeek-V3-shaped layer is tens of GB)."""
+
+    UNIT_KEYS = ("gate", "up", "down", "dgate", "dup", "ddown", "pgate", "pup", "pdown", "agate", "aup", "adown")
+
+    def __init__(self, O, shape, L):
+        super().__init__()
+        self.shape = shape
+        self["router"] = L["router"].cpu()
+        self["bias"] = None if L["bias"] is None else L["bias"].cpu()
+        for key in ("sgate", "sup", "sdown"):
+            v = L.get(key)
+            if v is not None and shape.dtype == "fp8":
+                v = O.dequant_rows_e4m3(v.cpu(), L[key + "_sc"].cpu())
+            self[key] = None if v is None else v.cpu() if torch.is_tensor(v) else v
+        for key in self.UNIT_KEYS:
+            if key in L:
+                self[key] = _HostUnits(O, L[key], L.get(key + "_sc"))
+
+    def prefetch(self, idx):
+        s = self.shape
+        for e in {int(e) for e in idx.ravel()}:
+            for key, u in (("gate", e), ("up", e), ("down", e), ("dgate", e // s.g), ("dup", e // s.g),
+                           ("ddown", e // s.g), ("pgate", e), ("pup", e), ("pdown", e), ("agate", e),
+                           ("aup", e), ("adown", e)):
+                if key in self:
+                    self[key].fetch(u)
+
+
+def oracle_route(O, shape, L, x):
+    if shape.k_dept:
+        return O.route_grouped(x, L["router"], shape.k, shape.g, shape.k_dept, bias=L["bias"])
+    return O.route(x, L["router"], shape.k, bias=L["bias"])
+
+
+def cpu_baseline(Ws, budget_s, max_T=8):
+    """The oracle (as it stands) on a bounded sample of the same step: whole
+    layer passes of replica 0 of every workload at its batch sizes up to
+    max_T, smallest first, repeated until the budget is spent.  Host copies
+    of the touched weights are made outside the timed sections."""
     from oracle import moe_oracle as O
-    import numpy as np  # noqa: F401
+    keys = sorted(((T, w) for w, W in enumerate(Ws) for T in W.batches if T <= max_T), key=lambda k: k)
+    if not keys:
+        keys = [(min(W.batches), w) for w, W in enumerate(Ws)]
+    host = {}
     done_bytes = 0
     t_total = 0.0
     passes = 0
-    keys = [(r, T) for r in range(min(2, W.R)) for T in sorted(batches)]   # host copies of <= 2 layers
-    host = {}
     while t_total <= budget_s and passes < 100 * len(keys):
-        r, T = keys[passes % len(keys)]
-        if shape.form_p:
-            # form P: host copies of the units this pass touches only (a
-            # whole layer can be tens of GB)
-            L = W.layers[r]
-            Wl = host.setdefault(r, {"router": L["router"].cpu(), "bias": None if L["bias"] is None else L["bias"].cpu()})
-            sel, _, _ = O.route_grouped(W.x[(r, T)].cpu(), Wl["router"], shape.k, shape.g, shape.k_dept or
-                                        shape.n // shape.g, bias=Wl["bias"])          # untimed: units to copy
-            for e in set(sel.ravel().tolist()):
-                for key_, src, u in (("dgate", "dgate", e // shape.g), ("dup", "dup", e // shape.g),
-                                     ("ddown", "ddown", e // shape.g), ("agate", "agate", e),
-                                     ("aup", "aup", e), ("adown", "adown", e)):
-                    Wl.setdefault(key_, {})
-                    if u not in Wl[key_]:
-                        Wl[key_][u] = L[src][u].cpu()
-        else:
-            if r not in host:
-                L = W.layers[r]
-                host[r] = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in L.items()}
-                if shape.dtype == "fp8":
-                    # the oracle decodes each unit it reads (codes and row scales)
-                    for k_ in [k_ for k_ in host[r] if k_ + "_sc" in host[r]]:
-                        host[r][k_] = _Fp8Units(O, host[r][k_], host[r][k_ + "_sc"])
-        L = host[r]
-        x = W.x[(r, T)].cpu()
+        T, w = keys[passes % len(keys)]
+        W = Ws[w]
+        if w not in host:
+            host[w] = _HostLayer(O, W.shape, W.layers[0])
+        L = host[w]
+        x = W.x[(0, T)].cpu()
+        idx, _, _ = oracle_route(O, W.shape, L, x)      # untimed: which units to copy
+        L.prefetch(idx)
         t0 = time.perf_counter()
-        if shape.k_dept:
-            idx, p, _ = O.route_grouped(x, L["router"], shape.k, shape.g, shape.k_dept, bias=L["bias"])
-        else:
-            idx, p, _ = O.route(x, L["router"], shape.k, bias=L["bias"])
-        oracle_forward(O, shape, L, x, idx, p)
+        idx, p, _ = oracle_route(O, W.shape, L, x)
+        oracle_forward(O, W.shape, L, x, idx, p)
         t_total += time.perf_counter() - t0
-        done_bytes += W.unique[(r, T)]
+        done_bytes += W.unique[(0, T)]
         passes += 1
     return {"value": round(done_bytes / t_total / 1e9, 4), "unit": "GB/s",
             "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-            "sample": f"{passes} full layer passes cycling over (replica, T) for T in "
-                      f"{sorted(batches)}, {min(passes, len(keys))} distinct, in {t_total:.1f} s "
-                      "(host copies of the weights made outside the timed sections)"}
-
-
-class _Fp8Units:
-    """FP8 unit tensor for the oracle: indexing a unit decodes it exactly."""
-
-    def __init__(self, O, codes, scales):
-        self.O, self.codes, self.scales = O, codes, scales
-
-    def __getitem__(self, u):
-        return self.O.dequant_rows_e4m3(self.codes[u], self.scales[u])
+            "sample": f"{passes} whole layer passes (routing + every selected expert of every token) of "
+                      f"replica 0, cycling over {len(keys)} (workload, T <= {max_T}) pairs smallest T first, "
+                      f"in {t_total:.1f} s (host copies of the touched weights made outside the timed "
+                      "sections)"}
 
 
 def oracle_forward(O, shape, L, x, idx, p):
@@ -620,91 +753,112 @@ def oracle_forward(O, shape, L, x, idx, p):
     return O.vanilla_layer(x, idx, p, L["gate"], L["up"], L["down"], shared=sh)
 
 
-def run_reference(args, rank, world):
-    """Reference arm: the CPU oracle timed on the host cores.  A step is one
-    selected expert of one token (its SwiGLU pass, plus the token's routing
-    and shared expert on its first step).  The weights of every unit the
-    steps touch are generated on the host before the timed region."""
-    if rank != 0:
-        return
-    from oracle import moe_oracle as O
-    s = WORKLOADS[args.workload]
-    batches = tuple(int(b) for b in args.batches.split(",")) if args.batches else s.batches
-    bw = {"bf16": 2, "f32": 4, "fp8": 1}[s.dtype]
-    row_b = 3 * s.d * bw + (12 if s.dtype == "fp8" else 0)    # one intermediate row: weights (+ FP8 scales)
-    seed = args.seed * 1000
-    router = synth.router(s.d, s.n, seed)
-    bias = synth.zipf_bias(s.n, s.zipf_g, s.zipf, seed) if s.zipf > 0 else None
-    ntok = -(-(args.steps + args.warmup) // s.k)
-    xs = synth.hidden(ntok, s.d, seed + 7)
+class _RefStepper:
+    """The reference arm's steps on one workload: step i is selected expert
+    i % k of token i // k (its SwiGLU or eq. (4) pass), with the token's
+    routing and shared expert on its first step.  Weights of the units the
+    steps touch are made on the host before the timed region."""
 
-    def route(x):
+    def __init__(self, O, s, seed, nsteps):
+        self.O, self.s = O, s
+        self.router = synth.router(s.d, s.n, seed)
+        self.bias = synth.zipf_bias(s.n, s.zipf_g, s.zipf, seed) if s.zipf > 0 else None
+        ntok = -(-nsteps // s.k)
+        self.xs = synth.hidden(ntok, s.d, seed + 7)
+        self.seed = seed
+        self.units = {}
+        self.row_b = 3 * s.d * {"bf16": 2, "f32": 4, "fp8": 1}[s.dtype] + (12 if s.dtype == "fp8" else 0)
+        idx_all, _, _ = self.route(self.xs)      # untimed: the units the steps touch
+        self.W = {int(e): self.weights(int(e)) for e in set(idx_all.ravel()[:nsteps].tolist())}
+        self.SH = ([self.unit(t, 0, s.I_s) for t in (synth.TID_SGATE, synth.TID_SUP, synth.TID_SDOWN)]
+                   if s.I_s else None)
+        self.state = {}
+
+    def route(self, x):
+        s = self.s
         if s.k_dept:
-            return O.route_grouped(x, router, s.k, s.g, s.k_dept, bias=bias)
-        return O.route(x, router, s.k, bias=bias)
+            return self.O.route_grouped(x, self.router, s.k, s.g, s.k_dept, bias=self.bias)
+        return self.O.route(x, self.router, s.k, bias=self.bias)
 
-    idx_all, _, _ = route(xs)       # untimed: which units to make
-    units = {}
-
-    def unit(tid, u, rows):
-        if (tid, u) not in units:
+    def unit(self, tid, u, rows):
+        s = self.s
+        if (tid, u) not in self.units:
             if s.dtype == "fp8":
-                w = synth.normal((rows, s.d), seed, tid, synth.WEIGHT_STD, "cpu", salt=u + 1)
-                units[(tid, u)] = torch.from_numpy(O.dequant_rows_e4m3(*synth.quantize_rows_e4m3(w)))
+                w = synth.normal((rows, s.d), self.seed, tid, synth.WEIGHT_STD, "cpu", salt=u + 1)
+                self.units[(tid, u)] = torch.from_numpy(self.O.dequant_rows_e4m3(*synth.quantize_rows_e4m3(w)))
             else:
-                units[(tid, u)] = synth.normal((rows, s.d), seed, tid, synth.WEIGHT_STD, "cpu",
-                                               synth.storage_dtype(s.dtype), salt=u + 1)
-        return units[(tid, u)]
+                self.units[(tid, u)] = synth.normal((rows, s.d), self.seed, tid, synth.WEIGHT_STD, "cpu",
+                                                    synth.storage_dtype(s.dtype), salt=u + 1)
+        return self.units[(tid, u)]
 
-    def amat(tid, e):
-        if (tid, e) not in units:
-            units[(tid, e)] = synth.near_identity_unit(e, s.I_sh, seed, tid, s.dtype)
-        return units[(tid, e)]
+    def amat(self, tid, e):
+        if (tid, e) not in self.units:
+            self.units[(tid, e)] = synth.near_identity_unit(e, self.s.I_sh, self.seed, tid, self.s.dtype)
+        return self.units[(tid, e)]
 
-    def weights(e):
+    def weights(self, e):
+        s = self.s
         if s.form_p:
             j = e // s.g
-            return ([unit(t, j, s.I_sh) for t in (synth.TID_DGATE, synth.TID_DUP, synth.TID_DDOWN)] +
-                    [amat(t, e) for t in (synth.TID_AGATE, synth.TID_AUP, synth.TID_ADOWN)])
+            return ([self.unit(t, j, s.I_sh) for t in (synth.TID_DGATE, synth.TID_DUP, synth.TID_DDOWN)] +
+                    [self.amat(t, e) for t in (synth.TID_AGATE, synth.TID_AUP, synth.TID_ADOWN)])
         if s.I_sh > 0:
             j = e // s.g
-            return [torch.cat([unit(t1, j, s.I_sh)] + ([unit(t2, e, s.I_pr)] if s.I_pr else []))
+            return [torch.cat([self.unit(t1, j, s.I_sh)] + ([self.unit(t2, e, s.I_pr)] if s.I_pr else []))
                     for t1, t2 in ((synth.TID_DGATE, synth.TID_PGATE), (synth.TID_DUP, synth.TID_PUP),
                                    (synth.TID_DDOWN, synth.TID_PDOWN))]
-        return [unit(t, e, s.I) for t in (synth.TID_GATE, synth.TID_UP, synth.TID_DOWN)]
+        return [self.unit(t, e, s.I) for t in (synth.TID_GATE, synth.TID_UP, synth.TID_DOWN)]
 
-    W = {int(e): weights(int(e)) for e in set(idx_all.ravel().tolist())}
-    SH = ([unit(t, 0, s.I_s) for t in (synth.TID_SGATE, synth.TID_SUP, synth.TID_SDOWN)]
-          if s.I_s else None)
-    state = {}
-
-    def step(i):
+    def step(self, i):
+        O, s, st = self.O, self.s, self.state
         tok, q = divmod(i, s.k)
         nbytes = 0
         if q == 0:
-            x = xs[tok:tok + 1]
-            idx, p, _ = route(x)
-            state.update(x=x, idx=idx, p=p, depts=set())
+            x = self.xs[tok:tok + 1]
+            idx, p, _ = self.route(x)
+            st.update(x=x, idx=idx, p=p, depts=set())
             nbytes += 4 * s.d * s.n
-            if SH is not None:
-                O.swiglu_expert(x[0], *SH)
-                nbytes += row_b * s.I_s
-        x, idx, p = state["x"], state["idx"], state["p"]
+            if self.SH is not None:
+                O.swiglu_expert(x[0], *self.SH)
+                nbytes += self.row_b * s.I_s
+        x, idx, p = st["x"], st["idx"], st["p"]
         e = int(idx[0, q])
         if s.form_p:
-            p[0, q] * O.deamoe_expert_p(x[0], *W[e])
+            p[0, q] * O.deamoe_expert_p(x[0], *self.W[e])
             j = e // s.g
-            nbytes += 2 * (3 * s.d * s.I_sh * (j not in state["depts"]) + 3 * s.I_sh * s.I_sh)
-            state["depts"].add(j)
+            nbytes += 2 * (3 * s.d * s.I_sh * (j not in st["depts"]) + 3 * s.I_sh * s.I_sh)
+            st["depts"].add(j)
         elif s.I_sh > 0:
-            p[0, q] * O.swiglu_expert(x[0], *W[e])
+            p[0, q] * O.swiglu_expert(x[0], *self.W[e])
             j = e // s.g
-            nbytes += row_b * (s.I_pr + (s.I_sh if j not in state["depts"] else 0))
-            state["depts"].add(j)
+            nbytes += self.row_b * (s.I_pr + (s.I_sh if j not in st["depts"] else 0))
+            st["depts"].add(j)
         else:
-            p[0, q] * O.swiglu_expert(x[0], *W[e])
-            nbytes += row_b * s.I
+            p[0, q] * O.swiglu_expert(x[0], *self.W[e])
+            nbytes += self.row_b * s.I
         return nbytes
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle timed on the host cores.  A step is one
+    selected expert of one token (its SwiGLU pass, plus the token's routing
+    and shared expert on its first step); over the suite, step i runs on
+    workload i % (number of workloads)."""
+    if rank != 0:
+        return
+    from oracle import moe_oracle as O
+    names = SUITE if args.workload == "suite" else (args.workload,)
+    override = tuple(int(b) for b in args.batches.split(",")) if args.batches else None
+    total_steps = args.steps + args.warmup
+    per = -(-total_steps // len(names))
+    steppers = [_RefStepper(O, WORKLOADS[n], args.seed * 1000, per) for n in names]
+    counters = [0] * len(names)
+
+    def step(i):
+        w = i % len(names)
+        j = counters[w]
+        counters[w] += 1
+        return steppers[w].step(j)
 
     for i in range(args.warmup):
         step(i)
@@ -714,12 +868,19 @@ def run_reference(args, rank, world):
         total += step(args.warmup + i)
     dt = time.perf_counter() - t0
     value = total / dt / 1e9
+
+    class _S:     # the configs of the workloads, as our arm reports them
+        def __init__(self, name):
+            self.name, self.shape = name, WORKLOADS[name]
+            self.batches = override or self.shape.batches
+            self.R = replicas_for(self.shape, args.replicas)
+    config = suite_config([_S(n) for n in names])
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {**workload_config(s, batches),
-                      "sample": "one selected expert of one token per step"},
+           "config": {**config, "sample": "one selected expert of one token per step"
+                                          + (", workloads in turn" if len(names) > 1 else "")},
            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "kind": "oracle",
                             "cores": len(os.sched_getaffinity(0)),
                             "sample": "one (token, expert) SwiGLU pass per step; routing and "

@@ -20,12 +20,17 @@ def run_reference(*extra):
     return json.loads(lines[0])
 
 
-@pytest.mark.parametrize("workload", ["vanilla-128e", "deamoe-7b"])
+@pytest.mark.parametrize("workload", ["vanilla-128e", "deamoe-7b", "suite"])
 def test_reference_arm_prints_the_contract_line(workload):
     sys.path.insert(0, ROOT)
     import bench
 
     d = run_reference("--workload", workload)
+    if workload == "suite":
+        # the default step: every layer of the five configurations but the tiny one
+        assert set(d["config"]["layers"]) == set(bench.SUITE)
+        assert all(name in d["config"]["workload"] for name in
+                   (bench.WORKLOADS[w].name for w in bench.SUITE))
     assert d["impl"] == "reference"
     assert d["metric"] == bench.METRIC and d["unit"] == "GB/s" and d["higher_is_better"] is True
     assert d["value"] > 0 and d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 1
