@@ -93,6 +93,22 @@ const char* moe_last_error(void);
  */
 int moe_set_tc_min_tokens(int min_tokens);
 
+/*
+ * Test hook for the FFN kernels' bounded waits (failure detection without a
+ * GPU fault; the paper has no counterpart).  wait_ns > 0: every FFN step
+ * launched while it is set (moe_ffn_vanilla, deamoe_ffn, the *_layer_forward
+ * calls and their FP8 variants) runs with its weight producers issuing no
+ * copy, and each consumer wait on a weight stage gives up after wait_ns
+ * nanoseconds instead of the normal two seconds.  The kernels then write
+ * MOE_ERR_TIMEOUT into the workspace status word (moe_read_status), drain
+ * what they started (no copy or MMA is left in flight), free their tensor
+ * memory and return; the routing of the step still runs and the output is
+ * left incomplete.  wait_ns = 0 turns it off (the default).  Process-wide,
+ * read when a step is launched; returns the previous setting, or
+ * MOE_ERR_INVALID_ARG for a negative value.
+ */
+int64_t moe_test_stall_weight_copies(int64_t wait_ns);
+
 /* ------------------------------------------------------------------------- */
 /* Workspace                                                                 */
 /* ------------------------------------------------------------------------- */

@@ -48,6 +48,7 @@ _P, _I, _F, _SZ, _I64 = C.c_void_p, C.c_int, C.c_float, C.c_size_t, C.c_int64
 _SIGS = {
     "moe_version": (_I, []),
     "moe_set_tc_min_tokens": (_I, [_I]),
+    "moe_test_stall_weight_copies": (C.c_int64, [C.c_int64]),
     "moe_last_error": (C.c_char_p, []),
     "moe_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "moe_workspace_layout": (_I, [_I, _I, _I, _I, C.POINTER(WsLayout)]),
@@ -149,6 +150,16 @@ def moe_set_tc_min_tokens(min_tokens: int) -> int:
     if r < 0:
         raise MoeError("moe_set_tc_min_tokens", r, lib().moe_last_error().decode())
     return r
+
+
+def moe_test_stall_weight_copies(wait_ns: int) -> int:
+    """Test hook: FFN steps launched while wait_ns > 0 issue no weight copy
+    and give up their waits after wait_ns ns (MOE_ERR_TIMEOUT in the
+    workspace status).  Returns the previous setting."""
+    r = lib().moe_test_stall_weight_copies(int(wait_ns))
+    if r < 0:
+        raise MoeError("moe_test_stall_weight_copies", r, lib().moe_last_error().decode())
+    return int(r)
 
 
 # ---------------------------------------------------------------- workspace

@@ -170,6 +170,9 @@ long long rows_count(int T, int n, int k, int g, int has_shared) {
 
 // Minimum gathered tokens for a unit to run on the tensor cores (0 = default).
 std::atomic<int> g_tc_min_tokens{0};
+// Timeout test (moe_test_stall_weight_copies): 0 = off, else the consumer
+// wait limit in ns of the FFN steps launched while it is set.
+std::atomic<long long> g_stall_wait_ns{0};
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -360,6 +363,11 @@ int route_scratch(void** out, const char* who) {
 extern "C" {
 
 int moe_version(void) { return 100; }
+
+int64_t moe_test_stall_weight_copies(int64_t wait_ns) {
+    if (wait_ns < 0) return fail(MOE_ERR_INVALID_ARG, "moe_test_stall_weight_copies: negative limit");
+    return g_stall_wait_ns.exchange(wait_ns);
+}
 
 int moe_set_tc_min_tokens(int min_tokens) {
     if (min_tokens < 0) return fail(MOE_ERR_INVALID_ARG, "moe_set_tc_min_tokens: negative");
@@ -632,6 +640,9 @@ static int setup_vanilla(moe::FfnArgs& a, const float* x, int T, int d, int n, i
     a.out = out;
     a.out_mode = out_mode;
     a.pdl = 1;
+    const long long stall = g_stall_wait_ns.load();
+    a.stall_copies = stall > 0 ? 1 : 0;
+    a.wait_ns = stall > 0 ? (unsigned long long)stall : 0ull;
     return MOE_OK;
 }
 
@@ -677,6 +688,9 @@ static int setup_deamoe(moe::FfnArgs& a, const float* x, int T, int d, int n, in
     a.out = out;
     a.out_mode = out_mode;
     a.pdl = 1;
+    const long long stall = g_stall_wait_ns.load();
+    a.stall_copies = stall > 0 ? 1 : 0;
+    a.wait_ns = stall > 0 ? (unsigned long long)stall : 0ull;
     return MOE_OK;
 }
 

@@ -390,7 +390,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
                 ++it;
                 return true;
             };
-            while (ok && next_seg(a, sm, r, r_end, s)) {
+            while (ok && !a.stall_copies && next_seg(a, sm, r, r_end, s)) {
                 const UnitClass& uc = a.cls[s.cls];
                 const size_t ubase = ((size_t)sm.units[sm.cls_off[s.cls] + s.q].x * uc.rows + s.row0) *
                                      (size_t)row_bytes;
@@ -429,7 +429,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
     bool ok = true;
     auto wait_full = [&](int slot, uint32_t i) -> bool {
         if (!ok) return false;
-        if (!mbar_wait_bounded(&sm.full[slot], (i / NS) & 1u)) {
+        if (!mbar_wait_bounded(&sm.full[slot], (i / NS) & 1u, ffn_wait_limit(a))) {
             ok = false;
             set_status(a.ws.status, kDevErrTimeout);
         }

@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
     bool ok = true;
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
         if (!ok) return false;
-        if (!mbar_wait_bounded(bar, parity)) {
+        if (!mbar_wait_bounded(bar, parity, ffn_wait_limit(a.f))) {
             ok = false;
             set_status(a.f.ws.status, kDevErrTimeout);
         }
@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                 ++it;
                 return true;
             };
-            while (ok && next_tile(a, sm, r, r_end, s)) {
+            while (ok && !a.f.stall_copies && next_tile(a, sm, r, r_end, s)) {
                 const int4 rec = sm.units[sm.cls_off[s.cls] + s.q];
                 const int y = rec.x * a.f.cls[s.cls].rows + s.row0;
                 const CUtensorMap* maps = a.maps[s.cls];

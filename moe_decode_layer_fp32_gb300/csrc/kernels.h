@@ -88,7 +88,17 @@ struct FfnArgs {
     float scale;
     int32_t* topk_idx;    // [T, k] routing outputs (written by CTA 0)
     float* topk_w;
+    // Timeout test (moe_test_stall_weight_copies): the weight producers issue
+    // no copy, and the consumers' waits give up after wait_ns (the drains
+    // keep the normal limit).  0 in every other call.
+    int stall_copies;
+    unsigned long long wait_ns;
 };
+
+// Limit of a consumer wait in an FFN kernel.
+__host__ __device__ __forceinline__ unsigned long long ffn_wait_limit(const FfnArgs& a) {
+    return a.wait_ns ? a.wait_ns : kWaitLimitNs;
+}
 
 // ceil(2^64 / g) for g >= 2 (2^64 / g when g divides it); grid_share() divides
 // by g with it.
