@@ -29,6 +29,7 @@ __global__ void __launch_bounds__(kBalanceThreads)
     const int c = tid < n ? __ldg(counts + tid) : 0;
     long long sum = c;
     int mx = tid < n ? c : INT_MIN;
+    __syncwarp();
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         sum += __shfl_xor_sync(0xffffffffu, sum, o);

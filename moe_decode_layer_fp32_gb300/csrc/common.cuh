@@ -161,6 +161,24 @@ __device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint3
         : "memory");
 }
 
+// Generic-proxy shared-memory writes -> visible to the async proxy (bulk
+// copies, tensor core).
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Shared -> global element-wise fp32 add of `bytes` (multiple of 16, both
+// addresses 16-byte aligned), performed by the bulk-copy unit at L2 as one
+// operation; the shared source must be made visible to the async proxy
+// first (fence_async_smem).  bulk_wait_all() returns once every reduction
+// this thread committed has completed.
+__device__ __forceinline__ void bulk_reduce_add_f32(float* dst_global, const void* src_smem, uint32_t bytes) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst_global),
+                 "r"(smem_u32(src_smem)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // ---- cp.async (16-byte global -> shared, L2 only) ---------------------------------
 __device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src)
@@ -227,12 +245,19 @@ __device__ __forceinline__ void unpack_bf16x8_f2(const uint4 v, float2 (&f)[4]) 
         f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
 }
 
+// Warp collectives start from a converged warp (__syncwarp): after a
+// lane-dependent branch the lanes may still run as separate groups, and then
+// every full-mask shuffle waits for the groups to meet.  Measured in the
+// one-token table build: about 720 cycles per round of three shuffles on a
+// split warp, about 33 once converged.
 __device__ __forceinline__ int warp_sum_int(int v) {
+    __syncwarp();
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
 __device__ __forceinline__ float warp_sum(float v) {
+    __syncwarp();
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
@@ -286,6 +311,7 @@ __device__ __forceinline__ bool topk_select_warp(const float* logits_row, const 
     float my_lg = 0.0f;
     bool bad = false;
     for (int r = 0; r < k; ++r) {
+        __syncwarp();
         uint32_t bk = 0u;
         int bj = 0;
 #pragma unroll
@@ -313,6 +339,7 @@ __device__ __forceinline__ bool topk_select_warp(const float* logits_row, const 
             my_lg = v;
         }
     }
+    __syncwarp();
     float mx = lane < k ? my_lg : -INFINITY;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -364,6 +391,7 @@ __device__ __forceinline__ bool topk_select_warp_grouped(const float* logits_row
     // Warp-wide best (key, then lowest index) among the entries whose bit is
     // set in the lane's mask; -1 when there is none.
     auto best = [&](uint32_t mask, uint32_t& top) -> int {
+        __syncwarp();
         uint32_t bk = 0u;
         int bj = 0;
 #pragma unroll
@@ -431,6 +459,7 @@ __device__ __forceinline__ bool topk_select_warp_grouped(const float* logits_row
             my_lg = v;
         }
     }
+    __syncwarp();
     float mx = lane < k ? my_lg : -INFINITY;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -453,6 +482,7 @@ __device__ int block_exclusive_scan(int* data, int len, int* warp_tmp) {
     int s = 0;
     for (int i = b; i < e; ++i) s += data[i];
     int v = s;
+    __syncwarp();
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int t = __shfl_up_sync(0xffffffffu, v, o);
@@ -462,6 +492,7 @@ __device__ int block_exclusive_scan(int* data, int len, int* warp_tmp) {
     __syncthreads();
     if (warp == 0) {
         int x = lane < NT / 32 ? warp_tmp[lane] : 0;
+        __syncwarp();
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int t = __shfl_up_sync(0xffffffffu, x, o);
@@ -485,6 +516,7 @@ __device__ int block_exclusive_scan(int* data, int len, int* warp_tmp) {
 // (5 - log2 V) bits are zero hold the full sum of value index `vi`.
 template <int V>
 __device__ __forceinline__ float warp_reduce_spread(float (&v)[V], int lane, int& vi) {
+    __syncwarp();
     int cnt = V;
     vi = 0;
 #pragma unroll
@@ -524,6 +556,7 @@ __device__ int3 block_exclusive_scan3(int* a0, int* a1, int* a2, int len, int3* 
         s.z += a2[i];
     }
     int3 v = s;
+    __syncwarp();
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int tx = __shfl_up_sync(0xffffffffu, v.x, o);
@@ -539,6 +572,7 @@ __device__ int3 block_exclusive_scan3(int* a0, int* a1, int* a2, int len, int3* 
     __syncthreads();
     if (warp == 0) {
         int3 x = lane < NT / 32 ? warp_tmp[lane] : make_int3(0, 0, 0);
+        __syncwarp();
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int tx = __shfl_up_sync(0xffffffffu, x.x, o);
@@ -584,6 +618,7 @@ __device__ __forceinline__ int filter_units_warp(const int4* src, int A, int lo,
     int kept = 0, gsum = 0;
     for (int b = 0; b < A; b += 32) {
         const int q = b + lane;
+        __syncwarp();
         const int4 r = q < A ? src[q] : make_int4(0, 0, 0, 0);
         const bool keep = q < A && r.z >= lo && r.z <= hi;
         int gi = keep ? (r.z + gsize - 1) / gsize : 0;

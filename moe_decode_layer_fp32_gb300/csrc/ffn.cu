@@ -110,6 +110,7 @@ __device__ __forceinline__ int class_cost_prefix_warp(const int4* u, int nu, int
         const int q = b + lane;
         const int c = q < nu ? unit_cost(u[q].z, rows) : 0;
         int inc = c;
+        __syncwarp();
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int t = __shfl_up_sync(0xffffffffu, inc, o);
@@ -427,6 +428,17 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
     long long r = r_begin;
     Seg s;
     bool ok = true;
+    bool aborted = false;
+    // Down-projection accumulators.  A one-token step keeps them across its
+    // segments (every unit adds into the same output row, the routing weight
+    // is already in h) and adds them into the output once, at the end.
+    float2 yacc[CH][kMT][4];
+#pragma unroll
+    for (int j = 0; j < CH; ++j)
+#pragma unroll
+        for (int m = 0; m < kMT; ++m)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) yacc[j][m][e] = make_float2(0.0f, 0.0f);
     auto wait_full = [&](int slot, uint32_t i) -> bool {
         if (!ok) return false;
         if (!mbar_wait_bounded(&sm.full[slot], (i / NS) & 1u, ffn_wait_limit(a))) {
@@ -489,7 +501,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
             }
         }
         // every consumer leaves the barrier with the same abort decision
-        if (named_bar_or(1, K::kNC, !ok)) break;
+        if (named_bar_or(1, K::kNC, !ok)) {
+            aborted = true;
+            break;
+        }
 
         // ---- SwiGLU: h = SiLU(g) * u (times the token's weight when accumulating) ----
         for (int i = tid; i < s.nrows * kMT; i += K::kNC) {
@@ -516,13 +531,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
         named_bar_sync(1, K::kNC);
 
         // ---- phase B: down projection into per-thread column accumulators ----
-        float2 yacc[CH][kMT][4];
+        if constexpr (!ONE) {
 #pragma unroll
-        for (int j = 0; j < CH; ++j)
+            for (int j = 0; j < CH; ++j)
 #pragma unroll
-            for (int m = 0; m < kMT; ++m)
+                for (int m = 0; m < kMT; ++m)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) yacc[j][m][e] = make_float2(0.0f, 0.0f);
+                    for (int e = 0; e < 4; ++e) yacc[j][m][e] = make_float2(0.0f, 0.0f);
+        }
         for (int rb = 0; rb < s.nrows; rb += rps) {
             const int nr = min(rps, s.nrows - rb);
             const int slot = it % NS;
@@ -539,7 +555,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
             }
             ++it;
         }
-        if (named_bar_or(1, K::kNC, !ok)) break;
+        if (named_bar_or(1, K::kNC, !ok)) {
+            aborted = true;
+            break;
+        }
+        if constexpr (ONE) continue;
         // ---- add this CTA's partial rows into the output ----
 #pragma unroll
         for (int j = 0; j < CH; ++j) {
@@ -554,6 +574,40 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
                         atomicAdd(dst + 1, make_float4(yacc[j][m][2].x, yacc[j][m][2].y,
                                                        yacc[j][m][3].x, yacc[j][m][3].y));
                     }
+                }
+            }
+        }
+    }
+    if constexpr (ONE) {
+        // One token: the CTA's partial output row goes through shared memory
+        // (the ring, idle once every stage was consumed) and is added into
+        // the output by one bulk reduction.  Every CTA adds into the same row,
+        // and hundreds of CTAs' per-element atomics on it queue at L2 for
+        // microseconds; a bulk reduction per CTA does not.
+        if (!aborted && r_begin < r_end && (size_t)a.d * 4 <= (size_t)NS * kStageBytes) {
+            float* stg = reinterpret_cast<float*>(ring);
+#pragma unroll
+            for (int j = 0; j < CH; ++j) {
+                if (cval[j]) {
+                    float4* p = reinterpret_cast<float4*>(stg + (tid + j * K::kNC) * 8);
+                    p[0] = make_float4(yacc[j][0][0].x, yacc[j][0][0].y, yacc[j][0][1].x, yacc[j][0][1].y);
+                    p[1] = make_float4(yacc[j][0][2].x, yacc[j][0][2].y, yacc[j][0][3].x, yacc[j][0][3].y);
+                }
+            }
+            fence_async_smem();
+            named_bar_sync(1, K::kNC);
+            if (tid == 0) {
+                bulk_reduce_add_f32(a.out, stg, (uint32_t)a.d * 4u);
+                bulk_commit();
+                bulk_wait_all();
+            }
+        } else if (!aborted && r_begin < r_end) {
+#pragma unroll
+            for (int j = 0; j < CH; ++j) {
+                if (cval[j]) {
+                    float4* dst = reinterpret_cast<float4*>(a.out + (tid + j * K::kNC) * 8);
+                    atomicAdd(dst, make_float4(yacc[j][0][0].x, yacc[j][0][0].y, yacc[j][0][1].x, yacc[j][0][1].y));
+                    atomicAdd(dst + 1, make_float4(yacc[j][0][2].x, yacc[j][0][2].y, yacc[j][0][3].x, yacc[j][0][3].y));
                 }
             }
         }

@@ -171,6 +171,7 @@ __device__ __forceinline__ void local_topk(const FfnArgs& a, const LocalRoute& l
 // Inclusive warp scan of four counters.
 __device__ __forceinline__ int4 warp_inclusive_scan4(int4 v) {
     const int lane = threadIdx.x & 31;
+    __syncwarp();
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int tx = __shfl_up_sync(0xffffffffu, v.x, o);
@@ -354,6 +355,9 @@ __device__ void local_tables_one_token(const FfnArgs& a, const UnitTableView& sm
         const int dj = act ? lr.didx[lane] : 0;
         const float w = act ? lr.w[lane] : 0.0f;
         const bool dept = lr.m > 0;
+        // the lane-dependent loads above may leave the warp diverged; the
+        // shuffle loops below run at full speed only on a converged warp
+        __syncwarp();
         int p = 0;              // experts selected below e
         uint32_t same = 0u;     // slots on department dj
         float om = 0.0f;
@@ -362,10 +366,11 @@ __device__ void local_tables_one_token(const FfnArgs& a, const UnitTableView& sm
             const int dr = __shfl_sync(0xffffffffu, dj, r);
             const float wr = __shfl_sync(0xffffffffu, w, r);
             p += er < e ? 1 : 0;
-            if (dr == dj) {
-                same |= 1u << r;
-                om += wr;
-            }
+            // selects, not a branch: the warp stays converged for the next
+            // round's shuffles (adding +0 leaves omega's bits unchanged)
+            const bool sd = dr == dj;
+            same |= sd ? 1u << r : 0u;
+            om += sd ? wr : 0.0f;
         }
         // one lane per selected department: its first slot
         const bool first = dept && act && (same & ((1u << lane) - 1u)) == 0u;
