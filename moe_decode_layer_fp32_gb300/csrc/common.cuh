@@ -178,6 +178,8 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* dst_global, const voi
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Returns once every committed reduction has finished reading its shared source.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 // ---- cp.async (16-byte global -> shared, L2 only) ---------------------------------
 __device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
@@ -211,6 +213,10 @@ __device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
 
 // ---- numerics -----------------------------------------------------------------
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+// The same with the hardware exponential and division (a few ulp, about 1e-6
+// relative): for epilogues where one warp per SM sub-partition applies it to
+// a whole tile column and the precise forms are its critical path.
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // 8 bf16 (one 16-byte word) -> 8 fp32, exact.
 __device__ __forceinline__ void unpack_bf16x8(const uint4 v, float (&f)[8]) {

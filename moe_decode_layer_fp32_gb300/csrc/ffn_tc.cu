@@ -67,6 +67,7 @@ constexpr int kBPair = 2 * kBBlock;               // ... of one K-pair
 constexpr int kTcBPairs = MOE_TC_BPAIRS;         // activation ring (K-pairs)
 constexpr int kHChunk = kTcMaxN * 128;            // H: [K chunk][N rows][128 B]
 constexpr int kHTile = 2 * kHChunk;               // K = 128 tile rows
+constexpr int kYStage = kTcTokens * 128 * 4;      // down output of one M-tile: [token][128 fp32]
 constexpr int kTmemCols = 512;
 constexpr uint32_t kColG = 0, kColU = 64, kColY = 128;
 constexpr int kYBufs = 6;                         // down accumulators, 64 columns each
@@ -163,7 +164,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
     unsigned char* aring = base;
     unsigned char* bring = aring + kTcStages * kAStage;
     unsigned char* htile = bring + kTcBPairs * kBPair;
-    TcSmem& sm = *reinterpret_cast<TcSmem*>(htile + kHTile);
+    float* ystage = reinterpret_cast<float*>(htile + kHTile);
+    TcSmem& sm = *reinterpret_cast<TcSmem*>(htile + kHTile + kYStage);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d = a.f.d;
@@ -415,17 +417,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
             if (!wait(&sm.acc_full, ti & 1u)) break;
             tc_fence_after_sync();
             for (int c0 = 0; c0 < Mp; c0 += 16) {
-                float ghi[16], glo[16], uhi[16], ulo[16];
-                tmem_ld16(tmem + lanes + kColG + c0, ghi);
-                tmem_ld16(tmem + lanes + kColG + Mp + c0, glo);
-                tmem_ld16(tmem + lanes + kColU + c0, uhi);
-                tmem_ld16(tmem + lanes + kColU + Mp + c0, ulo);
+                // the four loads of a column block share one completion wait
+                uint32_t ghi[16], glo[16], uhi[16], ulo[16];
+                tmem_ld16_async(tmem + lanes + kColG + c0, ghi);
+                tmem_ld16_async(tmem + lanes + kColG + Mp + c0, glo);
+                tmem_ld16_async(tmem + lanes + kColU + c0, uhi);
+                tmem_ld16_async(tmem + lanes + kColU + Mp + c0, ulo);
+                tmem_wait_ld();
+                tmem_regs_ready(ghi);
+                tmem_regs_ready(glo);
+                tmem_regs_ready(uhi);
+                tmem_regs_ready(ulo);
+                // every column of the block is computed (the unused ones from
+                // whatever TMEM holds) and only the stores are guarded, so the
+                // sixteen chains interleave
+                float hv[16];
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    hv[jj] = silu_fast(__uint_as_float(ghi[jj]) + __uint_as_float(glo[jj])) *
+                             (__uint_as_float(uhi[jj]) + __uint_as_float(ulo[jj]));
+                    if (a.f.out_mode == MOE_OUT_ACCUM) hv[jj] *= sm.ep_w[quarter][c0 + jj];
+                }
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
                     const int j = c0 + jj;
                     if (j < mg) {
-                        float h = silu_f(ghi[jj] + glo[jj]) * (uhi[jj] + ulo[jj]);
-                        if (a.f.out_mode == MOE_OUT_ACCUM) h *= sm.ep_w[quarter][j];
+                        const float h = hv[jj];
                         const __nv_bfloat16 hh = __float2bfloat16_rn(h);
                         const __nv_bfloat16 hl = __float2bfloat16_rn(h - __bfloat162float(hh));
                         const int jl = Mp + j;
@@ -441,27 +458,40 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                 mbar_arrive(&sm.acc_empty);
                 mbar_arrive(&sm.h_full);
             }
+            // Down outputs: each warp transposes its 32 columns of the M-tile
+            // through its own shared-memory block, so that a lane adds four
+            // consecutive columns of one token per vector atomic (a quarter
+            // of the atomic instructions of one per element and token).
+            float* wst = ystage + quarter * (kTcTokens * 32);
             for (int dt = 0; ok && dt < DT; ++dt, ++dtc) {
                 const uint32_t yb = dtc % kYBufs;
                 if (!wait(&sm.y_full[yb], (dtc / kYBufs) & 1u)) break;
                 tc_fence_after_sync();
                 const uint32_t ycol = kColY + yb * 64;
-                float* orow = a.f.out + dt * 128 + m;
                 for (int c0 = 0; c0 < Mp; c0 += 16) {
-                    float yhi[16], ylo[16];
-                    tmem_ld16(tmem + lanes + ycol + c0, yhi);
-                    tmem_ld16(tmem + lanes + ycol + Mp + c0, ylo);
+                    uint32_t yhi[16], ylo[16];
+                    tmem_ld16_async(tmem + lanes + ycol + c0, yhi);
+                    tmem_ld16_async(tmem + lanes + ycol + Mp + c0, ylo);
+                    tmem_wait_ld();
+                    tmem_regs_ready(yhi);
+                    tmem_regs_ready(ylo);
                     if (c0 + 16 >= Mp) {
                         tc_fence_before_sync();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&sm.y_empty[yb]);
                     }
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int j = c0 + jj;
-                        if (j < mg) atomicAdd(orow + (size_t)sm.ep_row[quarter][j] * d, yhi[jj] + ylo[jj]);
-                    }
+                    for (int jj = 0; jj < 16; ++jj)
+                        wst[(c0 + jj) * 32 + lane] = __uint_as_float(yhi[jj]) + __uint_as_float(ylo[jj]);
                 }
+                __syncwarp();
+                float* ybase = a.f.out + dt * 128 + quarter * 32;
+                for (int q = lane; q < mg * 8; q += 32) {
+                    const int j = q >> 3, c4 = (q & 7) * 4;
+                    const float4 v = *reinterpret_cast<const float4*>(wst + j * 32 + c4);
+                    atomicAdd(reinterpret_cast<float4*>(ybase + (size_t)sm.ep_row[quarter][j] * d + c4), v);
+                }
+                __syncwarp();
             }
             __syncwarp();
             ++ti;
@@ -555,7 +585,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
 }  // namespace
 
 size_t ffn_tc_smem_bytes(int units, const FfnArgs* local) {
-    return 1024 + (size_t)kTcStages * kAStage + (size_t)kTcBPairs * kBPair + kHTile + sizeof(TcSmem) +
+    return 1024 + (size_t)kTcStages * kAStage + (size_t)kTcBPairs * kBPair + kHTile + kYStage + sizeof(TcSmem) +
            (size_t)units * sizeof(int4) +
            (local ? local_route_bytes(local->T, local->n, local->k, local->g, kTcWarps) : 0);
 }
