@@ -559,10 +559,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, CPS) ffn_stream_kernel(FfnArgs
             aborted = true;
             break;
         }
-        if constexpr (ONE) continue;
-        // ---- add this CTA's partial rows into the output ----
+        // ---- add this CTA's partial rows into the output (one token: once,
+        // after the loop) ----
 #pragma unroll
-        for (int j = 0; j < CH; ++j) {
+        for (int j = 0; j < (ONE ? 0 : CH); ++j) {
             if (cval[j]) {
                 const int col = (tid + j * K::kNC) * 8;
 #pragma unroll
