@@ -313,39 +313,38 @@ __device__ __forceinline__ bool topk_select_warp(const float* logits_row, const 
             key[j] = (kv == kv && kv != -INFINITY) ? ordered_key(kv) : kLowest;
         }
     }
+    // A round is two warp reductions and selects: the picked index is
+    // warp-uniform, its owner clears the entry, and lane r keeps the r-th
+    // index; the picked logits are fetched once after the rounds.
     int my_idx = 0;
-    float my_lg = 0.0f;
     bool bad = false;
+    __syncwarp();
     for (int r = 0; r < k; ++r) {
-        __syncwarp();
         uint32_t bk = 0u;
         int bj = 0;
 #pragma unroll
-        for (int j = 0; j < J; ++j)
-            if (key[j] > bk) {
-                bk = key[j];
-                bj = j;
-            }
+        for (int j = 0; j < J; ++j) {
+            const bool gt = key[j] > bk;
+            bk = gt ? key[j] : bk;
+            bj = gt ? j : bj;
+        }
         const uint32_t top = __reduce_max_sync(0xffffffffu, bk);
         const uint32_t cand = (bk == top && top != 0u) ? (uint32_t)(lane + 32 * bj) : 0xffffffffu;
         const uint32_t bi = __reduce_min_sync(0xffffffffu, cand);
-        if (top <= kLowest) bad = true;   // a non-finite key (or none) was selected
+        bad = bad || top <= kLowest;   // a non-finite key (or none) was selected
         const int e = bi == 0xffffffffu ? 0 : (int)bi;
-        const int owner = e & 31, jb = e >> 5;
-        float v = 0.0f;
+        const bool mine = (e & 31) == lane;
 #pragma unroll
-        for (int j = 0; j < J; ++j)
-            if (j == jb) {
-                v = lg[j];
-                if (lane == owner) key[j] = 0u;
-            }
-        v = __shfl_sync(0xffffffffu, v, owner);
-        if (lane == r) {
-            my_idx = e;
-            my_lg = v;
-        }
+        for (int j = 0; j < J; ++j) key[j] = (mine && j == (e >> 5)) ? 0u : key[j];
+        my_idx = lane == r ? e : my_idx;
     }
-    __syncwarp();
+    // lane r < k: the logit of its pick, from the owning lane (one shuffle per slot)
+    float my_lg = 0.0f;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const float v = __shfl_sync(0xffffffffu, lg[j], my_idx & 31);
+        my_lg = (my_idx >> 5) == j ? v : my_lg;
+    }
     float mx = lane < k ? my_lg : -INFINITY;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
