@@ -2,6 +2,7 @@
 // kernel launches.  See include/moe_decode.h for the contract of each call.
 #include <atomic>
 #include <climits>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -997,9 +998,47 @@ static int formp_checks(const float* x, int T, int d, int n, int k, int g, int r
     return MOE_OK;
 }
 
+// Whether the matrix form's department passes (up, down) run on the tensor
+// cores: bf16 rows of d and r both multiples of 128 and d within the
+// activation split; with a fixed threshold (moe_set_tc_min_tokens) when T
+// reaches it; otherwise when the department rows streamed by the busiest SM
+// are fewer, estimated from the expected occupancy of the departments (a
+// token reaches a department with probability k_dept / m under group-limited
+// routing, else 1 - C(n - g, k) / C(n, k)): the CUDA-core passes read a
+// department's rows once per group of 4 tokens spread over every SM, the
+// tensor-core passes once per 32 tokens in 128-row tiles, one SM per tile.
+// As for the form-C FFN, the CUDA-core rows are weighted 4/3 on rows wider
+// than 4096; on narrower rows the tensor cores must win by half again (their
+// tiles are few there and the kernel's fixed costs weigh more: measured on
+// the 7B match, h = 1024, r = 384).  The private pass (A matrices, about one
+// token per expert) stays on the CUDA cores.
+static bool formp_tc(int T, int d, int n, int k, int g, int k_dept, int r) {
+    if (d % moe::kTcHiddenQuantum != 0 || r % moe::kTcBoxRows != 0 || d > moe::kMaxXbHidden) return false;
+    const int thr = tc_min_tokens();
+    if (thr > 0) return T >= thr;
+    const int m = n / g;
+    double p = 1.0;
+    if (k_dept > 0) {
+        p = (double)k_dept / m;
+    } else {
+        double miss = 1.0;
+        for (int i = 0; i < k; ++i) miss *= n - g - i > 0 ? (double)(n - g - i) / (n - i) : 0.0;
+        p = 1.0 - miss;
+    }
+    p = p < 1.0 ? p : 1.0;
+    const double hit = 1.0 - std::pow(1.0 - p, T);        // a department is active
+    const double active = m * hit;
+    const double tokens = hit > 0.0 ? T * p / hit : 0.0;   // tokens of an active department
+    const double sms = moe::device_sm_count();
+    const double cc = active * r * std::ceil(tokens / moe::kGroupTokens) / sms * (d > moe::kTcWideHidden ? 4.0 : 3.0);
+    const double tiles = active * (r / moe::kTcBoxRows) * std::ceil(tokens / moe::kTcGroupTokens);
+    const double tc = std::ceil(tiles / sms) * moe::kTcBoxRows * 3.0 * (d > moe::kTcWideHidden ? 1.0 : 1.5);
+    return tc < cc;
+}
+
 static int formp_launch(const float* x, int T, int d, int n, int k, int g, int r, const void* const (&wts)[6],
                         const int32_t* topk_idx, void* ws, const moe_ws_layout& L, size_t og, size_t ou,
-                        size_t oz, float* y, bool zero_y, cudaStream_t s, const char* who) {
+                        size_t oz, float* y, bool zero_y, bool tc, cudaStream_t s, const char* who) {
     char* b = static_cast<char*>(ws);
     const int m = n / g;
     moe::FormPArgs a = {};
@@ -1016,7 +1055,47 @@ static int formp_launch(const float* x, int T, int d, int n, int k, int g, int r
     a.y = y;
     a.zero_y = zero_y ? 1 : 0;
     a.ws = resolve(ws, L);
-    cudaError_t e = moe::launch_formp(a, moe::device_sm_count(), s);
+    const int sms = moe::device_sm_count();
+    if (!tc) {
+        cudaError_t e = moe::launch_formp(a, sms, s);
+        if (e != cudaSuccess) return cuda_fail(e, who);
+        return MOE_OK;
+    }
+    // department passes on the tensor cores, the private pass between them on
+    // the CUDA cores; each a programmatic dependent of the one before
+    moe::TcArgs t = {};
+    moe::FfnArgs& f = t.f;
+    f.x = x;
+    f.T = T; f.d = d; f.n = n; f.k = k; f.g = g;
+    f.dtype = MOE_DTYPE_BF16;
+    f.cls[0].w_gate = wts[0];
+    f.cls[0].w_up = wts[1];
+    f.cls[0].w_down = wts[2];
+    f.cls[0].rows = r;
+    f.cls[0].kind = moe::kUnitDept;
+    f.ncls = 1;
+    f.ws = a.ws;
+    f.out = y;
+    f.out_mode = MOE_OUT_ACCUM;
+    f.pdl = 1;
+    f.sms = sms;
+    f.max_tokens = INT_MAX;
+    t.min_tokens = 1;
+    for (int mat = 0; mat < 3; ++mat)
+        if (!encode_weight_map(&t.maps[0][mat], wts[mat], n / g, r, d))
+            return fail(MOE_ERR_CUDA, "%s: tensor map encoding failed", who);
+    t.gbuf = a.gbuf;
+    t.ubuf = a.ubuf;
+    t.zbuf = a.zbuf;
+    t.topk_idx = topk_idx;
+    t.zero_y = zero_y ? 1 : 0;
+    t.pmode = moe::kTcFormPUp;
+    cudaError_t e = moe::launch_ffn_tc(t, s);
+    if (e == cudaSuccess) e = moe::launch_formp_pass(a, moe::kFormPPriv, sms, s);
+    if (e == cudaSuccess) {
+        t.pmode = moe::kTcFormPDown;
+        e = moe::launch_ffn_tc(t, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e, who);
     return MOE_OK;
 }
@@ -1054,10 +1133,12 @@ int deamoe_p_layer_forward(const float* x, int T, int d, int n, int k, float sca
     ra.fuse_dispatch = 1;
     ra.route_g = g;
     ra.k_dept = k_dept;
+    const bool tc = formp_tc(T, d, n, k, g, k_dept, r);
+    ra.split_x = tc ? 1 : 0;
     cudaStream_t s = as_stream(stream);
     cudaError_t e = moe::launch_route(ra, s);
     if (e != cudaSuccess) return cuda_fail(e, who);
-    return formp_launch(x, T, d, n, k, g, r, wts, topk_idx, ws, L, og, ou, oz, y, false, s, who);
+    return formp_launch(x, T, d, n, k, g, r, wts, topk_idx, ws, L, og, ou, oz, y, false, tc, s, who);
 }
 
 int deamoe_p_ffn(const float* x, int T, int d, int n, int k, int experts_per_dept, int r, int dtype,
@@ -1072,7 +1153,14 @@ int deamoe_p_ffn(const float* x, int T, int d, int n, int k, int experts_per_dep
     int rc = formp_checks(x, T, d, n, k, g, r, dtype, wts, ws, ws_bytes, y, &L, &og, &ou, &oz, who);
     if (rc) return rc;
     if (!topk_idx) return fail(MOE_ERR_INVALID_ARG, "%s: topk_idx is null", who);
-    return formp_launch(x, T, d, n, k, g, r, wts, topk_idx, ws, L, og, ou, oz, y, true, as_stream(stream), who);
+    // the standalone step takes no k_dept: the plain top-k's occupancy
+    const bool tc = formp_tc(T, d, n, k, g, 0, r);
+    cudaStream_t s = as_stream(stream);
+    if (tc) {
+        cudaError_t e = moe::launch_split_x(x, (long long)T * d, resolve(ws, L).xb, s);
+        if (e != cudaSuccess) return cuda_fail(e, who);
+    }
+    return formp_launch(x, T, d, n, k, g, r, wts, topk_idx, ws, L, og, ou, oz, y, true, tc, s, who);
 }
 
 int64_t moe_unique_weight_bytes_formp(int d, int n, int r, int A_d, int A_e) {

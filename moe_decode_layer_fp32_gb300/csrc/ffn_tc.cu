@@ -87,6 +87,11 @@ struct TcSmem {
     int cls_off[3];
     int ep_row[4][kTcTokens];     // epilogue warps: output row of each tile token
     float ep_w[4][kTcTokens];     // ... and its routing weight
+    // form-P down pass: each tile token's assignments in the department
+    // (zbuf row and routing weight)
+    int pd_cnt[kTcTokens];
+    int pd_pos[kTcTokens][kMaxK];
+    float pd_w[kTcTokens][kMaxK];
     int4 units[1];                // per class: {unit, first entry, tokens, group prefix}
 };
 
@@ -224,6 +229,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
     if (MOE_ROUTE_PDL) pdl_allow_dependents();
     // Everything below reads what the routing / dispatch kernel wrote.
     pdl_wait_primary();
+    if (a.pmode == kTcFormPUp) {
+        // the private pass adds into the assignment rows, the down pass into
+        // y (when no routing kernel cleared it): clear them here
+        const long long z4 = (long long)a.f.T * a.f.k * a.f.cls[0].rows / 4;
+        for (long long i = blockIdx.x * (long long)kTcThreads + tid; i < z4; i += (long long)gridDim.x * kTcThreads)
+            reinterpret_cast<float4*>(a.zbuf)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (a.zero_y) {
+            const long long y4 = (long long)a.f.T * a.f.d / 4;
+            for (long long i = blockIdx.x * (long long)kTcThreads + tid; i < y4; i += (long long)gridDim.x * kTcThreads)
+                reinterpret_cast<float4*>(a.f.out)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    const bool has_gu = a.pmode != kTcFormPDown;    // gate / up rows of each tile
+    const bool has_dn = a.pmode != kTcFormPUp;      // down rows of each tile
 
     // ---- unit table: on the in-CTA routing path every unit, built here from
     // the router logits (CTA 0 also stores the routing and the dispatch).
@@ -309,11 +328,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                 const int4 rec = sm.units[sm.cls_off[s.cls] + s.q];
                 const int y = rec.x * a.f.cls[s.cls].rows + s.row0;
                 const CUtensorMap* maps = a.maps[s.cls];
-                for (int p = 0; ok && p < KP; ++p) {
+                for (int p = 0; ok && has_gu && p < KP; ++p) {
                     if (!load(&maps[0], y, 2 * p)) break;
                     if (!load(&maps[1], y, 2 * p)) break;
                 }
-                for (int mt = 0; ok && mt < DT; ++mt)
+                for (int mt = 0; ok && has_dn && mt < DT; ++mt)
                     if (!load(&maps[2], y, 2 * mt)) break;
             }
             // every issued copy must land before the CTA may exit
@@ -338,6 +357,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                 const int N = 2 * ((mg + 7) & ~7);
                 const uint32_t id_gu = idesc_bf16_f32(128, N, false, false);
                 const uint32_t id_dn = idesc_bf16_f32(128, N, true, false);
+                if (has_gu) {
                 if (!wait(&sm.acc_empty, (ti & 1u) ^ 1u)) break;
                 tc_fence_after_sync();
                 for (int p = 0; ok && p < KP; ++p, ++bp) {
@@ -364,6 +384,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                 }
                 if (!ok) break;
                 umma_commit(&sm.acc_full);
+                }
+                if (!has_dn) {
+                    ++ti;
+                    continue;
+                }
                 if (!wait(&sm.h_full, ti & 1u)) break;
                 tc_fence_after_sync();
                 // down: M-tile mt = 128 hidden columns; A is W_down read MN-major
@@ -414,8 +439,83 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                 sm.ep_w[quarter][lane] = w;
             }
             __syncwarp();
+            if (a.pmode == kTcFormPDown) {
+                // H[row, token] = sum over the token's experts i in the
+                // department of p_i SiLU(Z_i[row]).  Warp 2 collects each tile
+                // token's assignments (zbuf row, routing weight) and the four
+                // epilogue warps meet at named barrier 1 after that; they also
+                // meet at the end of every tile (below), where they agree on
+                // their waits' outcomes, so that all of them reach this barrier
+                // or none does.
+                if (warp == 2 && lane < mg) {
+                    const int t = sm.ep_row[2][lane];
+                    int c = 0;
+                    for (int sl = 0; sl < a.f.k; ++sl) {
+                        const int e = a.topk_idx[t * a.f.k + sl];
+                        if (e / a.f.g == rec.x && c < kMaxK) {
+                            const int p = a.f.ws.tok_asg[t * a.f.k + sl];
+                            sm.pd_pos[lane][c] = p;
+                            sm.pd_w[lane][c] = a.f.ws.asg_w[p];
+                            ++c;
+                        }
+                    }
+                    sm.pd_cnt[lane] = c;
+                }
+                named_bar_sync(1, 128);
+                const int rws = a.f.cls[0].rows;
+                for (int c0 = 0; c0 < Mp; c0 += 16) {
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int j = c0 + jj;
+                        if (j < mg) {
+                            float h = 0.0f;
+                            for (int c = 0; c < sm.pd_cnt[j]; ++c)
+                                h += sm.pd_w[j][c] *
+                                     silu_f(__ldcg(a.zbuf + (size_t)sm.pd_pos[j][c] * rws + s.row0 + m));
+                            const __nv_bfloat16 hh = __float2bfloat16_rn(h);
+                            const __nv_bfloat16 hl = __float2bfloat16_rn(h - __bfloat162float(hh));
+                            const int jl = Mp + j;
+                            *reinterpret_cast<__nv_bfloat16*>(hcol + j * 128 + ((hchunk ^ (j & 7)) << 4)) = hh;
+                            *reinterpret_cast<__nv_bfloat16*>(hcol + jl * 128 + ((hchunk ^ (jl & 7)) << 4)) = hl;
+                        }
+                    }
+                }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.h_full);
+            } else {
             if (!wait(&sm.acc_full, ti & 1u)) break;
             tc_fence_after_sync();
+            if (a.pmode == kTcFormPUp) {
+                // G = SiLU(W_g x), U = SiLU(W_u x) of each department entry
+                const int rws = a.f.cls[0].rows;
+                for (int c0 = 0; c0 < Mp; c0 += 16) {
+                    uint32_t ghi[16], glo[16], uhi[16], ulo[16];
+                    tmem_ld16_async(tmem + lanes + kColG + c0, ghi);
+                    tmem_ld16_async(tmem + lanes + kColG + Mp + c0, glo);
+                    tmem_ld16_async(tmem + lanes + kColU + c0, uhi);
+                    tmem_ld16_async(tmem + lanes + kColU + Mp + c0, ulo);
+                    tmem_wait_ld();
+                    tmem_regs_ready(ghi);
+                    tmem_regs_ready(glo);
+                    tmem_regs_ready(uhi);
+                    tmem_regs_ready(ulo);
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int j = c0 + jj;
+                        if (j < mg) {
+                            const size_t o = (size_t)(first + j) * rws + s.row0 + m;
+                            a.gbuf[o] = silu_f(__uint_as_float(ghi[jj]) + __uint_as_float(glo[jj]));
+                            a.ubuf[o] = silu_f(__uint_as_float(uhi[jj]) + __uint_as_float(ulo[jj]));
+                        }
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.acc_empty);
+                ++ti;
+                continue;
+            }
             for (int c0 = 0; c0 < Mp; c0 += 16) {
                 // the four loads of a column block share one completion wait
                 uint32_t ghi[16], glo[16], uhi[16], ulo[16];
@@ -458,6 +558,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                 mbar_arrive(&sm.acc_empty);
                 mbar_arrive(&sm.h_full);
             }
+            }
             // Down outputs: each warp transposes its 32 columns of the M-tile
             // through its own shared-memory block, so that a lane adds four
             // consecutive columns of one token per vector atomic (a quarter
@@ -495,6 +596,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
             }
             __syncwarp();
             ++ti;
+            if (a.pmode == kTcFormPDown && named_bar_or(1, 128, !ok)) ok = false;
         }
     } else {
         // ===================== activation gather =====================
@@ -507,7 +609,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
         uint32_t bp = 0;
         int r = r_begin;
         TSeg s;
-        while (ok && next_tile(a, sm, r, r_end, s)) {
+        while (ok && has_gu && next_tile(a, sm, r, r_end, s)) {
             const int4 rec = sm.units[sm.cls_off[s.cls] + s.q];
             const int kind = a.f.cls[s.cls].kind;
             const int first = rec.y + s.grp * kTcTokens;

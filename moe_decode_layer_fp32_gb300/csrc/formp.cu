@@ -443,4 +443,10 @@ cudaError_t launch_formp(const FormPArgs& a, int sms, cudaStream_t s) {
     return e;
 }
 
+cudaError_t launch_formp_pass(const FormPArgs& a, int stage, int sms, cudaStream_t s) {
+    if (stage == kFormPUp) return launch_formp_stage<kFormPUp>(a, a.d, sms, s);
+    if (stage == kFormPPriv) return launch_formp_stage<kFormPPriv>(a, a.r, sms, s);
+    return launch_formp_stage<kFormPDown>(a, a.d, sms, s);
+}
+
 }  // namespace moe

@@ -126,7 +126,21 @@ struct TcArgs {
     FfnArgs f;
     CUtensorMap maps[3][3];
     int min_tokens;       // units with at least this many tokens
+    // Matrix-form department passes of "DeaMoE" §3.1 eq. (4) on one class of
+    // department units (rows = r): 0 = the SwiGLU FFN step; kTcFormPUp =
+    // G = SiLU(W_g x) and U = SiLU(W_u x) of each department entry into gbuf
+    // / ubuf (no down rows; also clears zbuf, and y with zero_y);
+    // kTcFormPDown = H = sum_i p_i SiLU(Z_i) of each department entry from
+    // the assignment rows of zbuf, then W_d^T H into y (no gate / up rows).
+    int pmode;
+    float* gbuf;          // [T * min(k, m), r] per department entry
+    float* ubuf;
+    float* zbuf;          // [T * k, r] per assignment: A_d^T Y (before SiLU)
+    const int32_t* topk_idx;
+    int zero_y;
 };
+constexpr int kTcFormPUp = 1;
+constexpr int kTcFormPDown = 2;
 
 // Rows of one tensor-core weight tile / TMA box (unit rows must be a multiple),
 // the hidden-size granularity of its stages, and its tokens per group.
@@ -189,6 +203,8 @@ struct FormPArgs {
     WsPtrs ws;
 };
 cudaError_t launch_formp(const FormPArgs& a, int sms, cudaStream_t s);
+// One of the three passes (FormPStage) on the CUDA cores.
+cudaError_t launch_formp_pass(const FormPArgs& a, int stage, int sms, cudaStream_t s);
 int formp_max_hidden();   // widest h the up / down passes take
 int formp_max_width();    // widest r the private pass takes
 

@@ -99,6 +99,32 @@ def test_formp_dsv3_shapes_sampled(B, T):
     assert check_formp(B, s, T, seed=6, k_dept=s.k_dept, sample=sample) <= 1
 
 
+# department rows 256, hidden 512: both department-pass paths apply
+TC_FORMP = synth.LayerShape("formp-tc-small", d=512, n=32, k=4, dtype="bf16", g=8, I_sh=256, form_p=True,
+                            k_dept=2)
+
+
+@pytest.fixture
+def threshold(B):
+    prev = B.moe_set_tc_min_tokens(0)
+
+    def set_(v):
+        B.moe_set_tc_min_tokens(v)
+    yield set_
+    B.moe_set_tc_min_tokens(prev)
+
+
+@pytest.mark.parametrize("T", [1, 7, 40])
+@pytest.mark.parametrize("mode", ["tc", "cc"])
+def test_formp_department_passes_each_path(B, threshold, mode, T):
+    """The up and down passes on the tensor cores (threshold 1 token) and on
+    the CUDA cores (threshold above every batch), the private pass between
+    them on the CUDA cores: the same oracle output either way (T = 40 puts
+    more than 32 tokens on a department: two token groups per tile)."""
+    threshold(1 if mode == "tc" else 10 ** 6)
+    assert check_formp(B, TC_FORMP, T, seed=21, k_dept=TC_FORMP.k_dept) <= 1
+
+
 def test_formp_identity_matrices_reduce_to_the_closed_form(B):
     """With A = I for every expert, eq. (4) gives W_d^T SiLU(SiLU(SiLU(W_g x)) * SiLU(W_u x))
     for each expert, so a token's output is (sum of its weights) times that
