@@ -256,6 +256,7 @@ bool prepare_tc(const moe::FfnArgs& a, int T, moe::TcArgs* t) {
         return false;
     for (int c = 0; c < a.ncls; ++c)
         if (a.cls[c].rows % moe::kTcBoxRows != 0) return false;
+    *t = moe::TcArgs{};   // the form-C FFN step: no matrix-form pass mode or buffers
     t->f = a;
     t->min_tokens = thr > 0 ? thr : 1;
     for (int c = 0; c < a.ncls; ++c) {
@@ -656,7 +657,7 @@ static int ffn_vanilla_impl(const float* const* sc, const char* who, const float
                            s_down, ws, ws_bytes, out_mode, out, who);
     if (rc) return rc;
     if ((rc = attach_row_scales(a, sc, 2, who))) return rc;
-    moe::TcArgs t;
+    moe::TcArgs t = {};
     const bool tc = prepare_tc(a, T, &t);
     return run_ffn(a, T, n, k, 1, I_s > 0, tc, t, false, stream, who);
 }
@@ -707,7 +708,7 @@ static int deamoe_ffn_impl(const float* const* sc, const char* who, const float*
                           ws_bytes, out_mode, out, who);
     if (rc) return rc;
     if ((rc = attach_row_scales(a, sc, 3, who))) return rc;
-    moe::TcArgs t;
+    moe::TcArgs t = {};
     const bool tc = prepare_tc(a, T, &t);
     return run_ffn(a, T, n, k, experts_per_dept, I_s > 0, tc, t, false, stream, who);
 }
@@ -825,7 +826,7 @@ static int layer_forward_impl(const float* const* sc, const char* who, const flo
     if ((rc = attach_row_scales(a, sc, 2, who))) return rc;
     moe_ws_layout L;
     layout_of(T, n, k, 1, &L);
-    moe::TcArgs t;
+    moe::TcArgs t = {};
     const bool tc = prepare_tc(a, T, &t);
     const int path = layer_path(a, tc, t);
     if ((rc = layer_route(x, T, d, n, k, scale, w_router, bias, 1, L, ws, topk_idx, topk_w, y, tc,
@@ -849,7 +850,7 @@ static int deamoe_layer_forward_impl(const float* const* sc, const char* who, co
     if ((rc = attach_row_scales(a, sc, 3, who))) return rc;
     moe_ws_layout L;
     layout_of(T, n, k, experts_per_dept, &L);
-    moe::TcArgs t;
+    moe::TcArgs t = {};
     const bool tc = prepare_tc(a, T, &t);
     const int path = layer_path(a, tc, t);
     if ((rc = layer_route(x, T, d, n, k, scale, w_router, bias, experts_per_dept, L, ws, topk_idx,
