@@ -703,6 +703,9 @@ bool ffn_tc_local_route_fits(const FfnArgs& a) {
 }
 
 cudaError_t launch_ffn_tc(const TcArgs& a, cudaStream_t s) {
+    // a matrix-form pass needs its buffers; anything else is the FFN step
+    if (a.pmode != 0 && (a.pmode != kTcFormPUp && a.pmode != kTcFormPDown)) return cudaErrorInvalidValue;
+    if (a.pmode != 0 && (!a.gbuf || !a.ubuf || !a.zbuf || !a.topk_idx || a.f.ncls != 1)) return cudaErrorInvalidValue;
     int units = 0;
     for (int c = 0; c < a.f.ncls; ++c) units += class_capacity(a.f.cls[c], a.f.n, a.f.g);
     const size_t smem = ffn_tc_smem_bytes(units, a.f.local_route ? &a.f : nullptr);
