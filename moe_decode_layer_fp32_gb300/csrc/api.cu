@@ -210,11 +210,26 @@ bool encode_weight_map(CUtensorMap* map, const void* base, int units, int rows, 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// TMA descriptor of one [units * rows, d] E4M3 weight tensor (one byte per
+// code): boxes of 128 columns x kTcBoxRows rows (16 KB), unswizzled; the
+// kernel's converter warps lay the values out for the MMA.
+bool encode_weight_map_f8(CUtensorMap* map, const void* base, int units, int rows, int d) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)units * rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)d};
+    const cuuint32_t box[2] = {128, (cuuint32_t)moe::kTcBoxRows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 0 (default): automatic per-call choice on the device; > 0: fixed threshold.
 int tc_min_tokens() { return g_tc_min_tokens.load(); }
 
 // Whether the tensor-core kernel takes part in this FFN step, and its TMA
-// descriptors: bf16 weights, d a multiple of 128, and a batch large enough for
+// descriptors: bf16 or E4M3 weights, d a multiple of 128, and a batch large enough for
 // some unit to reach the token threshold.
 // Expected tokens per active unit of the busiest class under uniform routing:
 // T*k/n per expert, T*P(department chosen) per department, T for the shared
@@ -251,8 +266,9 @@ bool prepare_tc(const moe::FfnArgs& a, int T, moe::TcArgs* t) {
     const int mt = thr > 0 ? thr : 1;
     int units = 0;
     for (int c = 0; c < a.ncls; ++c) units += moe::class_capacity(a.cls[c], a.n, a.g);
-    if (a.dtype != MOE_DTYPE_BF16 || a.d % moe::kTcHiddenQuantum != 0 || a.d > moe::kMaxXbHidden || T < mt ||
-        moe::ffn_tc_smem_bytes(units, nullptr) > 227 * 1024)
+    const bool f8 = a.dtype == MOE_DTYPE_FP8_E4M3;
+    if ((a.dtype != MOE_DTYPE_BF16 && !f8) || a.d % moe::kTcHiddenQuantum != 0 || a.d > moe::kMaxXbHidden ||
+        T < mt || moe::ffn_tc_smem_bytes(units, nullptr, f8) > 227 * 1024)
         return false;
     for (int c = 0; c < a.ncls; ++c)
         if (a.cls[c].rows % moe::kTcBoxRows != 0) return false;
@@ -262,9 +278,9 @@ bool prepare_tc(const moe::FfnArgs& a, int T, moe::TcArgs* t) {
     for (int c = 0; c < a.ncls; ++c) {
         const moe::UnitClass& uc = a.cls[c];
         const int nu = moe::class_capacity(uc, a.n, a.g);
-        if (!encode_weight_map(&t->maps[c][0], uc.w_gate, nu, uc.rows, a.d) ||
-            !encode_weight_map(&t->maps[c][1], uc.w_up, nu, uc.rows, a.d) ||
-            !encode_weight_map(&t->maps[c][2], uc.w_down, nu, uc.rows, a.d))
+        auto enc = f8 ? encode_weight_map_f8 : encode_weight_map;
+        if (!enc(&t->maps[c][0], uc.w_gate, nu, uc.rows, a.d) || !enc(&t->maps[c][1], uc.w_up, nu, uc.rows, a.d) ||
+            !enc(&t->maps[c][2], uc.w_down, nu, uc.rows, a.d))
             return false;
     }
     return true;

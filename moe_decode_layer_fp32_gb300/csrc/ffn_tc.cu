@@ -27,6 +27,15 @@
 // allocation; warps 2-5 are the epilogue (TMEM -> registers, SwiGLU, H tile,
 // output atomics); warps 6-9 gather the bf16 hi/lo activations (split once per
 // layer) into swizzled B tiles with cp.async.
+//
+// FP8 (E4M3 codes, one fp32 scale per weight row): TMA lands 16 KB boxes of
+// codes (128 rows x 128 columns) in a 5-stage ring, and four more warps
+// (10-13) expand each box into the bf16 layout above, in a 3-stage ring the
+// MMAs read.  Every E4M3 value is exact in bf16, so the products are those of
+// the bf16 path on the codes; the epilogue multiplies the gate and up results
+// by their row scales and folds the down row scale into H (a down row is a K
+// index of the down MMA).  Groups hold 16 tokens here, which frees the shared
+// memory for the deeper code ring.
 // Every wait is bounded; on a timeout the kernel records an error status,
 // drains its copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -53,55 +62,102 @@ namespace {
 constexpr int kTcRows = kTcBoxRows;               // 128
 constexpr int kChunkBytes = kTcRows * 128;        // 16 KB: one 64-column chunk
 constexpr int kAStage = 2 * kChunkBytes;          // 32 KB
+constexpr int kF8Box = kTcRows * 128;             // 16 KB: 128 rows x 128 E4M3 codes
 #ifndef MOE_TC_STAGES
 #define MOE_TC_STAGES 4
 #endif
 #ifndef MOE_TC_BPAIRS
 #define MOE_TC_BPAIRS 3
 #endif
-constexpr int kTcStages = MOE_TC_STAGES;          // weight ring
-constexpr int kTcTokens = kTcGroupTokens;         // tokens per group (hi + lo rows: N <= 64)
-constexpr int kTcMaxN = 2 * kTcTokens;
-constexpr int kBBlock = kTcMaxN * 128;            // activations of one K-block: N rows x 128 B
-constexpr int kBPair = 2 * kBBlock;               // ... of one K-pair
-constexpr int kTcBPairs = MOE_TC_BPAIRS;         // activation ring (K-pairs)
-constexpr int kHChunk = kTcMaxN * 128;            // H: [K chunk][N rows][128 B]
-constexpr int kHTile = 2 * kHChunk;               // K = 128 tile rows
-constexpr int kYStage = kTcTokens * 128 * 4;      // down output of one M-tile: [token][128 fp32]
+#ifndef MOE_TC_F8_STAGES
+#define MOE_TC_F8_STAGES 5
+#endif
+#ifndef MOE_TC_F8_CSTAGES
+#define MOE_TC_F8_CSTAGES 3
+#endif
 constexpr int kTmemCols = 512;
 constexpr uint32_t kColG = 0, kColU = 64, kColY = 128;
 constexpr int kYBufs = 6;                         // down accumulators, 64 columns each
-constexpr int kTcWarps = 10;
-constexpr int kTcThreads = kTcWarps * 32;
 
+// Per weight type: bf16 (F8 = false) or E4M3 codes with row scales.
+template <bool F8>
+struct TcGeo {
+    static constexpr int kTok = F8 ? 16 : kTcGroupTokens;   // tokens per group (hi + lo rows: N <= 2 kTok)
+    static constexpr int kMaxN = 2 * kTok;
+    static constexpr int kAStages = F8 ? MOE_TC_F8_CSTAGES : MOE_TC_STAGES;   // ring the MMAs read (bf16 boxes)
+    static constexpr int kF8Stages = F8 ? MOE_TC_F8_STAGES : 0;   // ring of code boxes
+    static constexpr int kBPairs = MOE_TC_BPAIRS;            // activation ring (K-pairs)
+    static constexpr int kBBlock = kMaxN * 128;              // activations of one K-block: N rows x 128 B
+    static constexpr int kBPair = 2 * kBBlock;               // ... of one K-pair
+    static constexpr int kHChunk = kMaxN * 128;              // H: [K chunk][N rows][128 B]
+    static constexpr int kHTile = 2 * kHChunk;               // K = 128 tile rows
+    static constexpr int kYStage = kTok * 128 * 4;           // down output of one M-tile: [token][128 fp32]
+    static constexpr int kCvtWarps = F8 ? 4 : 0;
+    static constexpr int kWarps = 10 + kCvtWarps;
+    static constexpr int kThreads = kWarps * 32;
+    static constexpr int kPdTok = F8 ? 1 : kTok;             // form-P down lists (bf16 only)
+};
+
+template <class G>
 struct TcSmem {
-    uint64_t full[kTcStages];     // producer TMA bytes landed (weight ring)
-    uint64_t empty[kTcStages];    // MMAs reading the weight stage are done
-    uint64_t bx_full[kTcBPairs];  // activation K-pair gathered
-    uint64_t bx_empty[kTcBPairs]; // MMAs reading the activation K-pair are done
+    uint64_t full[G::kAStages];   // weight stage ready: TMA bytes landed (bf16) / converted (FP8)
+    uint64_t empty[G::kAStages];  // MMAs reading the weight stage are done
+    uint64_t full8[G::kF8Stages > 0 ? G::kF8Stages : 1];   // code box landed
+    uint64_t empty8[G::kF8Stages > 0 ? G::kF8Stages : 1];  // code box converted
+    uint64_t bx_full[G::kBPairs];  // activation K-pair gathered
+    uint64_t bx_empty[G::kBPairs]; // MMAs reading the activation K-pair are done
     uint64_t acc_full, acc_empty, h_full, mma_done;
     uint64_t y_full[kYBufs], y_empty[kYBufs];
     uint32_t tmem_base;
     int cls_units[3];
     int cls_groups[3];
     int cls_off[3];
-    int ep_row[4][kTcTokens];     // epilogue warps: output row of each tile token
-    float ep_w[4][kTcTokens];     // ... and its routing weight
+    int ep_row[4][G::kTok];       // epilogue warps: output row of each tile token
+    float ep_w[4][G::kTok];       // ... and its routing weight
     // form-P down pass: each tile token's assignments in the department
     // (zbuf row and routing weight)
-    int pd_cnt[kTcTokens];
-    int pd_pos[kTcTokens][kMaxK];
-    float pd_w[kTcTokens][kMaxK];
+    int pd_cnt[G::kPdTok];
+    int pd_pos[G::kPdTok][kMaxK];
+    float pd_w[G::kPdTok][kMaxK];
     int4 units[1];                // per class: {unit, first entry, tokens, group prefix}
 };
+
+// E4M3 -> bf16 on the integer and FMA pipes (the conversion instructions
+// issue at a quarter of their rate and bound the converter warps).  A code
+// s eeee mmm and the bf16 pattern s 0000eeee mmm0000 have the same sign and
+// significand, and the pattern's value is the code's times 2^-120 (exponent
+// bias 127 against 7); codes with eeee = 0 (E4M3 subnormals) land on bf16
+// subnormals with the same scaling.  So each code of a pair goes to its own
+// 16-bit half, the magnitude bits move up by 4, the sign from bit 11 to bit 15
+// (t + 15 (t & m) moves a set bit 11 to bit 15, bits 12-15 being clear), and
+// one bf16 multiply by 2^120 restores the value; it is exact, every code
+// value being a bf16 normal.  sel picks the pair: 0x4140 codes 0 and 1 of the
+// word, 0x4342 codes 2 and 3; code 2i+0 lands in the low half.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t w, uint32_t sel) {
+    const uint32_t t = __byte_perm(w, 0u, sel) << 4;
+    const uint32_t r = t + 15u * (t & 0x08000800u);
+    const __nv_bfloat162 v = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&r),
+                                     __halves2bfloat162(__ushort_as_bfloat16((unsigned short)0x7B80u),
+                                                        __ushort_as_bfloat16((unsigned short)0x7B80u)));
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// 16 E4M3 codes (one 16-byte load, code 0 in the low byte) -> 16 bf16 values
+// in two 16-byte units, in order.
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 w, uint4& o0, uint4& o1) {
+    o0 = make_uint4(e4m3x2_to_bf16x2(w.x, 0x4140u), e4m3x2_to_bf16x2(w.x, 0x4342u),
+                    e4m3x2_to_bf16x2(w.y, 0x4140u), e4m3x2_to_bf16x2(w.y, 0x4342u));
+    o1 = make_uint4(e4m3x2_to_bf16x2(w.z, 0x4140u), e4m3x2_to_bf16x2(w.z, 0x4342u),
+                    e4m3x2_to_bf16x2(w.w, 0x4140u), e4m3x2_to_bf16x2(w.w, 0x4342u));
+}
 
 struct TSeg {
     int cls, q, grp, row0;
 };
 
 // Next tile (kTcRows rows) of the CTA's row range [r, r_end).
-__device__ __forceinline__ bool next_tile(const TcArgs& a, const TcSmem& sm, int& r, int r_end,
-                                          TSeg& s) {
+template <class S>
+__device__ __forceinline__ bool next_tile(const TcArgs& a, const S& sm, int& r, int r_end, TSeg& s) {
     if (r >= r_end) return false;
     int base = 0, c = 0;
     while (c < a.f.ncls - 1 && r >= base + a.f.cls[c].rows * sm.cls_groups[c]) {
@@ -160,17 +216,27 @@ __device__ __forceinline__ void tile_token(const TcArgs& a, const LocalRoute& lr
 
 // LOCAL: the in-CTA routing path (a.f.local_route); a separate instantiation
 // so that the path reading the dispatch from global memory keeps its code.
-template <bool LOCAL>
-__global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_constant__ TcArgs a) {
+// F8: E4M3 weights with row scales (converter warps, TcGeo<true>).
+template <bool LOCAL, bool F8>
+__global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __grid_constant__ TcArgs a) {
+    using G = TcGeo<F8>;
+    constexpr int kTcTokens = G::kTok;
+    constexpr int kTcStages = G::kAStages;
+    constexpr int kF8Stages = G::kF8Stages;
+    constexpr int kTcBPairs = G::kBPairs;
+    constexpr int kBBlock = G::kBBlock, kBPair = G::kBPair, kHChunk = G::kHChunk, kHTile = G::kHTile;
+    constexpr int kYStage = G::kYStage;
+    constexpr int kTcWarps = G::kWarps, kTcThreads = G::kThreads;
     extern __shared__ unsigned char smem_dyn[];
     // 1024-byte aligned tile regions (128 B swizzle atoms)
     unsigned char* base = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
-    unsigned char* aring = base;
+    unsigned char* f8ring = base;                    // FP8: code boxes (empty for bf16)
+    unsigned char* aring = f8ring + kF8Stages * kF8Box;
     unsigned char* bring = aring + kTcStages * kAStage;
     unsigned char* htile = bring + kTcBPairs * kBPair;
     float* ystage = reinterpret_cast<float*>(htile + kHTile);
-    TcSmem& sm = *reinterpret_cast<TcSmem*>(htile + kHTile + kYStage);
+    TcSmem<G>& sm = *reinterpret_cast<TcSmem<G>*>(htile + kHTile + kYStage);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d = a.f.d;
@@ -178,8 +244,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
 
     if (tid == 0) {
         for (int i = 0; i < kTcStages; ++i) {
-            mbar_init(&sm.full[i], 1);
+            mbar_init(&sm.full[i], F8 ? G::kCvtWarps : 1);
             mbar_init(&sm.empty[i], 1);
+        }
+        for (int i = 0; i < kF8Stages; ++i) {
+            mbar_init(&sm.full8[i], 1);
+            mbar_init(&sm.empty8[i], G::kCvtWarps);
         }
         for (int i = 0; i < kTcBPairs; ++i) {
             mbar_init(&sm.bx_full[i], 4);
@@ -316,11 +386,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
             uint32_t it = 0;
             int r = r_begin;
             TSeg s;
-            auto load = [&](const CUtensorMap* m, int y, int z) -> bool {
-                const int slot = it % kTcStages;
-                if (!wait(&sm.empty[slot], ((it / kTcStages) & 1u) ^ 1u)) return false;
-                mbar_arrive_expect_tx(&sm.full[slot], kAStage);
-                tma_load_3d(aring + slot * kAStage, m, 0, y, z, &sm.full[slot], pol);
+            // the ring TMA writes: the MMAs' (bf16) or the converters' (FP8)
+            constexpr int NS = F8 ? kF8Stages : kTcStages;
+            constexpr int SB = F8 ? kF8Box : kAStage;
+            unsigned char* ring = F8 ? f8ring : aring;
+            uint64_t* fullb = F8 ? sm.full8 : sm.full;
+            uint64_t* emptyb = F8 ? sm.empty8 : sm.empty;
+            // columns [128 cb, 128 cb + 128) of weight rows [y, y + 128)
+            auto load = [&](const CUtensorMap* m, int y, int cb) -> bool {
+                const int slot = it % NS;
+                if (!wait(&emptyb[slot], ((it / NS) & 1u) ^ 1u)) return false;
+                mbar_arrive_expect_tx(&fullb[slot], SB);
+                if (F8) tma_load_2d(ring + slot * SB, m, 128 * cb, y, &fullb[slot], pol);
+                else tma_load_3d(ring + slot * SB, m, 0, y, 2 * cb, &fullb[slot], pol);
                 ++it;
                 return true;
             };
@@ -329,16 +407,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                 const int y = rec.x * a.f.cls[s.cls].rows + s.row0;
                 const CUtensorMap* maps = a.maps[s.cls];
                 for (int p = 0; ok && has_gu && p < KP; ++p) {
-                    if (!load(&maps[0], y, 2 * p)) break;
-                    if (!load(&maps[1], y, 2 * p)) break;
+                    if (!load(&maps[0], y, p)) break;
+                    if (!load(&maps[1], y, p)) break;
                 }
                 for (int mt = 0; ok && has_dn && mt < DT; ++mt)
-                    if (!load(&maps[2], y, 2 * mt)) break;
+                    if (!load(&maps[2], y, mt)) break;
             }
             // every issued copy must land before the CTA may exit
-            const uint32_t first = it > (uint32_t)kTcStages ? it - kTcStages : 0u;
+            const uint32_t first = it > (uint32_t)NS ? it - NS : 0u;
             for (uint32_t i = first; i < it; ++i)
-                mbar_wait_bounded(&sm.full[i % kTcStages], (i / kTcStages) & 1u);
+                mbar_wait_bounded(&fullb[i % NS], (i / NS) & 1u);
         }
     } else if (warp == 1) {
         // ===================== MMA issuer =====================
@@ -438,6 +516,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                 sm.ep_row[quarter][lane] = row;
                 sm.ep_w[quarter][lane] = w;
             }
+            // FP8: this thread's weight row's scales (gate, up, down)
+            float sg = 1.0f, su = 1.0f, sdn = 1.0f;
+            if constexpr (F8) {
+                const UnitClass& uc = a.f.cls[s.cls];
+                const size_t ur = (size_t)rec.x * uc.rows + s.row0 + m;
+                sg = __ldg(uc.sc_gate + ur);
+                su = __ldg(uc.sc_up + ur);
+                sdn = __ldg(uc.sc_down + ur);
+            }
             __syncwarp();
             if (a.pmode == kTcFormPDown) {
                 // H[row, token] = sum over the token's experts i in the
@@ -534,9 +621,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                 float hv[16];
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
-                    hv[jj] = silu_fast(__uint_as_float(ghi[jj]) + __uint_as_float(glo[jj])) *
-                             (__uint_as_float(uhi[jj]) + __uint_as_float(ulo[jj]));
+                    float g = __uint_as_float(ghi[jj]) + __uint_as_float(glo[jj]);
+                    float u = __uint_as_float(uhi[jj]) + __uint_as_float(ulo[jj]);
+                    if constexpr (F8) {
+                        g *= sg;
+                        u *= su;
+                    }
+                    hv[jj] = silu_fast(g) * u;
                     if (a.f.out_mode == MOE_OUT_ACCUM) hv[jj] *= sm.ep_w[quarter][c0 + jj];
+                    if constexpr (F8) hv[jj] *= sdn;
                 }
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
@@ -598,7 +691,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
             ++ti;
             if (a.pmode == kTcFormPDown && named_bar_or(1, 128, !ok)) ok = false;
         }
-    } else {
+    } else if (warp < 10) {
         // ===================== activation gather =====================
         // B tiles (one K-pair per slot) are copied with cp.async from the bf16
         // hi / lo activations (split once per layer), kPre pairs ahead of the MMA.
@@ -652,7 +745,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                 return true;
             };
             // exactly kPre groups in flight before the first wait (empty ones
-            // when the tile has fewer pairs), one more per pair after
+            // when the tile has fewer pairs), one more per pair after.  Pair
+            // p is handed to the MMA as soon as it lands, before the copies of
+            // pair p + kPre wait for the MMA to release a slot, so that the
+            // MMAs of pair p never wait on those of pair p - 1.
             for (int p = 0; ok && p < kPre; ++p) {
                 if (p < KP) {
                     if (!issue(p)) break;
@@ -661,19 +757,67 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
                 }
             }
             for (int p = 0; ok && p < KP; ++p) {
+                cp_async_wait<kPre - 1>();              // pair p has landed
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.bx_full[(bp + p) % kTcBPairs]);
                 if (p + kPre < KP) {
                     if (!issue(p + kPre)) break;
                 } else {
                     cp_async_commit();                  // keep one group per pair
                 }
-                cp_async_wait<kPre>();                  // pair p has landed
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.bx_full[(bp + p) % kTcBPairs]);
             }
             bp += KP;
         }
         cp_async_wait<0>();
+    } else if constexpr (F8) {
+        // ===================== FP8 converters =====================
+        // Warp cw expands rows [32 cw, 32 cw + 32) of each code box, four rows
+        // a step (eight steps).  Within a step, the eight lanes of each shared-memory phase
+        // read half a row each of two adjacent rows (128 distinct bytes) and
+        // write their bf16 units to one chunk's even and the other chunk's odd
+        // swizzled positions, so neither the loads nor the stores conflict.
+        constexpr int kRowsPerCvt = kTcRows / G::kCvtWarps;   // 32
+        const int cw = warp - 10;
+        const int pr = lane >> 4, ph = (lane >> 3) & 1, sub = (lane >> 2) & 1;
+        const int q = ((sub ^ ph) << 2) | (lane & 3);   // 16-code unit of the row
+        const int rsub = 2 * pr + sub;                   // row within the step
+        const int u0 = 2 * (q & 3);                      // first bf16 unit in the chunk
+        const int per_tile = 2 * KP + DT;                // boxes per tile
+        uint32_t it = 0;
+        int r = r_begin;
+        TSeg s;
+        while (ok && next_tile(a, sm, r, r_end, s)) {
+            for (int st = 0; st < per_tile; ++st, ++it) {
+                const uint32_t s8 = it % kF8Stages, sc = it % kTcStages;
+                if (!wait(&sm.full8[s8], (it / kF8Stages) & 1u)) break;
+                if (!wait(&sm.empty[sc], ((it / kTcStages) & 1u) ^ 1u)) break;
+                const unsigned char* src = f8ring + s8 * kF8Box + q * 16;
+                unsigned char* dst = aring + sc * kAStage + (q >> 2) * kChunkBytes;
+                // all loads first: the compiler cannot tell the two rings
+                // apart and would otherwise keep each load behind the
+                // previous step's stores
+                uint4 w[kRowsPerCvt / 4];
+#pragma unroll
+                for (int i = 0; i < kRowsPerCvt / 4; ++i)
+                    w[i] = *reinterpret_cast<const uint4*>(src + (cw * kRowsPerCvt + i * 4 + rsub) * 128);
+#pragma unroll
+                for (int i = 0; i < kRowsPerCvt / 4; ++i) {
+                    const int row = cw * kRowsPerCvt + i * 4 + rsub;
+                    uint4 o0, o1;
+                    e4m3x16_to_bf16(w[i], o0, o1);
+                    unsigned char* drow = dst + row * 128;
+                    *reinterpret_cast<uint4*>(drow + ((u0 ^ (row & 7)) << 4)) = o0;
+                    *reinterpret_cast<uint4*>(drow + (((u0 + 1) ^ (row & 7)) << 4)) = o1;
+                }
+                fence_async_smem();      // the stores are read by the MMA (async proxy)
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&sm.full[sc]);
+                    mbar_arrive(&sm.empty8[s8]);
+                }
+            }
+        }
     }
 
     tc_fence_before_sync();
@@ -686,30 +830,49 @@ __global__ void __launch_bounds__(kTcThreads, 1) ffn_tc_kernel(const __grid_cons
 
 }  // namespace
 
-size_t ffn_tc_smem_bytes(int units, const FfnArgs* local) {
-    return 1024 + (size_t)kTcStages * kAStage + (size_t)kTcBPairs * kBPair + kHTile + kYStage + sizeof(TcSmem) +
-           (size_t)units * sizeof(int4) +
-           (local ? local_route_bytes(local->T, local->n, local->k, local->g, kTcWarps) : 0);
+template <bool F8>
+static size_t tc_smem_bytes(int units, const FfnArgs* local) {
+    using G = TcGeo<F8>;
+    return 1024 + (size_t)G::kF8Stages * kF8Box + (size_t)G::kAStages * kAStage + (size_t)G::kBPairs * G::kBPair +
+           G::kHTile + G::kYStage + sizeof(TcSmem<G>) + (size_t)units * sizeof(int4) +
+           (local ? local_route_bytes(local->T, local->n, local->k, local->g, G::kWarps) : 0);
 }
 
+size_t ffn_tc_smem_bytes(int units, const FfnArgs* local, bool f8) {
+    return f8 ? tc_smem_bytes<true>(units, local) : tc_smem_bytes<false>(units, local);
+}
+
+int ffn_tc_threads(bool f8) { return f8 ? TcGeo<true>::kThreads : TcGeo<false>::kThreads; }
+
 bool ffn_tc_local_route_fits(const FfnArgs& a) {
+    const bool f8 = a.dtype == MOE_DTYPE_FP8_E4M3;
     int units = 0;
     for (int c = 0; c < a.ncls; ++c) units += class_capacity(a.cls[c], a.n, a.g);
     const int m = a.g > 1 ? a.n / a.g : 0;
     // one thread per unit: the experts, then the departments from the next
     // warp on; the top-k's lane-held candidates: n <= 256
-    return a.n <= 256 && ((a.n + 31) / 32) * 32 + m <= kTcThreads &&
-           ffn_tc_smem_bytes(units, &a) <= 227 * 1024;
+    return a.n <= 256 && ((a.n + 31) / 32) * 32 + m <= ffn_tc_threads(f8) &&
+           ffn_tc_smem_bytes(units, &a, f8) <= 227 * 1024;
 }
 
 cudaError_t launch_ffn_tc(const TcArgs& a, cudaStream_t s) {
     // a matrix-form pass needs its buffers; anything else is the FFN step
     if (a.pmode != 0 && (a.pmode != kTcFormPUp && a.pmode != kTcFormPDown)) return cudaErrorInvalidValue;
     if (a.pmode != 0 && (!a.gbuf || !a.ubuf || !a.zbuf || !a.topk_idx || a.f.ncls != 1)) return cudaErrorInvalidValue;
+    // FP8 weights: E4M3 codes with row scales, the FFN step only
+    const bool f8 = a.f.dtype == MOE_DTYPE_FP8_E4M3;
+    if (f8 && a.pmode != 0) return cudaErrorInvalidValue;
+    if (f8) {
+        for (int c = 0; c < a.f.ncls; ++c)
+            if (!a.f.cls[c].sc_gate || !a.f.cls[c].sc_up || !a.f.cls[c].sc_down) return cudaErrorInvalidValue;
+    } else if (a.f.dtype != MOE_DTYPE_BF16) {
+        return cudaErrorInvalidValue;
+    }
     int units = 0;
     for (int c = 0; c < a.f.ncls; ++c) units += class_capacity(a.f.cls[c], a.f.n, a.f.g);
-    const size_t smem = ffn_tc_smem_bytes(units, a.f.local_route ? &a.f : nullptr);
-    auto kern = a.f.local_route ? ffn_tc_kernel<true> : ffn_tc_kernel<false>;
+    const size_t smem = ffn_tc_smem_bytes(units, a.f.local_route ? &a.f : nullptr, f8);
+    auto kern = a.f.local_route ? (f8 ? ffn_tc_kernel<true, true> : ffn_tc_kernel<true, false>)
+                                : (f8 ? ffn_tc_kernel<false, true> : ffn_tc_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)device_sm_count();
@@ -717,7 +880,7 @@ cudaError_t launch_ffn_tc(const TcArgs& a, cudaStream_t s) {
     args.f.grid_magic = grid_magic_of(grid);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(kTcThreads, 1, 1);
+    cfg.blockDim = dim3((unsigned)ffn_tc_threads(f8), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];

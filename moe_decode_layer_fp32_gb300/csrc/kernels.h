@@ -121,7 +121,8 @@ __host__ __device__ __forceinline__ int class_capacity(const UnitClass& c, int n
 }
 
 // Tensor-core FFN: the FFN arguments plus one TMA descriptor per class and
-// matrix (gate, up, down) over the [units * rows, d] bf16 weight tensor.
+// matrix (gate, up, down) over the [units * rows, d] weight tensor (bf16, or
+// E4M3 codes whose row scales the FfnArgs classes carry).
 struct TcArgs {
     FfnArgs f;
     CUtensorMap maps[3][3];
@@ -227,7 +228,10 @@ cudaError_t launch_ffn(const FfnArgs& a, cudaStream_t s);
 // of the local path (a.local_route) at its usual CTAs per SM.
 bool ffn_local_route_fits(const FfnArgs& a);
 cudaError_t launch_ffn_tc(const TcArgs& a, cudaStream_t s);
-size_t ffn_tc_smem_bytes(int units, const FfnArgs* local);
+// Dynamic shared memory of the tensor-core kernel (f8: the E4M3 variant) and
+// its block size.
+size_t ffn_tc_smem_bytes(int units, const FfnArgs* local, bool f8);
+int ffn_tc_threads(bool f8);
 // Whether the tensor-core kernel can route inside its CTAs (a.local_route).
 bool ffn_tc_local_route_fits(const FfnArgs& a);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);

@@ -32,6 +32,23 @@ def B():
     return H.ensure_built()
 
 
+@pytest.fixture
+def threshold(B):
+    prev = B.moe_set_tc_min_tokens(0)
+
+    def set_(v):
+        B.moe_set_tc_min_tokens(v)
+    yield set_
+    B.moe_set_tc_min_tokens(prev)
+
+
+# Small enough for the oracle, with every weight block a multiple of 128 rows
+# so that the tensor-core kernel takes each class, shared expert included.
+TC_DEA_FP8 = synth.LayerShape("tc-deamoe-fp8-shared", d=256, n=16, k=4, dtype="fp8", g=4, I_sh=256, I_pr=128,
+                              I_s=128)
+TC_VAN_FP8 = synth.LayerShape("tc-vanilla-fp8-shared", d=384, n=16, k=4, dtype="fp8", I=128, I_s=128)
+
+
 def scales_of(shape, L):
     sc = lambda key: L.get(key + "_sc")                                       # noqa: E731
     if shape.I_sh > 0:
@@ -67,8 +84,8 @@ def run_layer(B, shape, L, x):
     return ws, idx.cpu().numpy(), w.cpu().numpy(), y.cpu().numpy()
 
 
-def check_fp8_layer(B, shape, T, seed, sample=None):
-    L = synth.make_layer(shape, seed, DEV)
+def check_fp8_layer(B, shape, T, seed, sample=None, L=None):
+    L = synth.make_layer(shape, seed, DEV) if L is None else L
     x = synth.hidden(T, shape.d, seed + 3 * T, DEV)
     ws, gi, gw, y = run_layer(B, shape, L, x)
     assert B.moe_read_status(ws)[0] == 0
@@ -122,6 +139,83 @@ def test_fp8_ffn_step_on_the_oracle_dispatch(B, mode):
     else:
         B.deamoe_ffn(x, shape.k, shape.g, dept, priv, sh, ws, B.MOE_OUT_ACCUM, y, scales=scales_of(shape, L))
     torch.cuda.synchronize()
+    ref = H.oracle_layer(shape, decoded(L), x, oi, op)
+    assert H.rel_err(y.cpu().numpy(), ref) <= 1e-4
+
+
+@pytest.mark.parametrize("mode", ["tc", "cc"])
+@pytest.mark.parametrize("shape,T", [(synth.DEAMOE_7B_FP8, 4), (synth.DEAMOE_7B_FP8, 16), (synth.DEAMOE_7B_FP8, 33),
+                                     (synth.VANILLA_128E_FP8, 16)], ids=lambda v: getattr(v, "name", v))
+def test_fp8_each_path(B, threshold, mode, shape, T):
+    """The E4M3 tensor-core kernel (converter warps, row scales in the
+    epilogue) forced on every unit, and the CUDA-core stream alone, on the
+    7B-class FP8 layers: both within 1e-4 of the oracle on the decoded
+    weights.  T = 33 gives departments three groups of 16 tokens, the last
+    one ragged."""
+    threshold(1 if mode == "tc" else 10 ** 6)
+    sample = None if T <= 16 else [0, 16, 32]
+    assert check_fp8_layer(B, shape, T, seed=27, sample=sample) <= 1
+
+
+@pytest.mark.parametrize("shape", [TC_DEA_FP8, TC_VAN_FP8], ids=lambda s: s.name)
+@pytest.mark.parametrize("T", [1, 5, 17, 33])
+def test_fp8_tc_small_layers(B, threshold, shape, T):
+    """Shared expert, departments and expert blocks on the tensor cores with
+    one token, a partial group, and several groups with a ragged tail."""
+    threshold(1)
+    assert check_fp8_layer(B, shape, T, seed=28) <= 1
+
+
+E4M3_SUBNORMAL = [0x00, 0x80] + list(range(0x01, 0x08)) + list(range(0x81, 0x88))
+E4M3_ALL = [c for c in range(256) if c not in (0x7F, 0xFF)]          # every code but the two NaNs
+
+
+@pytest.mark.parametrize("mode", ["tc", "cc"])
+@pytest.mark.parametrize("pool", ["subnormal", "all"])
+def test_fp8_every_code(B, threshold, mode, pool):
+    """Weights drawn from a set of E4M3 codes, decoded by each path and
+    compared with the oracle's exact decode: the zeros and subnormals alone
+    (a path that flushed or mis-scaled them would be off by the whole output)
+    and every finite code."""
+    threshold(1 if mode == "tc" else 10 ** 6)
+    shape = TC_VAN_FP8
+    L = synth.make_layer(shape, 30, DEV)
+    rng = np.random.default_rng(30 if pool == "all" else 31)
+    codes = np.array(E4M3_SUBNORMAL if pool == "subnormal" else E4M3_ALL, np.uint8)
+    for key in ("gate", "up", "down", "sgate", "sup", "sdown"):
+        draw = rng.choice(codes, size=tuple(L[key].shape))
+        L[key] = torch.tensor(draw, dtype=torch.uint8, device=DEV).view(torch.float8_e4m3fn)
+        if pool == "subnormal":
+            L[key + "_sc"] = L[key + "_sc"] * 256.0
+    for T in (3, 17):
+        assert check_fp8_layer(B, shape, T, seed=30, L=L) <= 1
+
+
+@pytest.mark.parametrize("mode", ["rows", "accum"])
+def test_fp8_tc_ffn_step_on_the_oracle_dispatch(B, threshold, mode):
+    """The FFN step alone on the tensor cores with the oracle's routing:
+    ROWS (each row unweighted, then the combine) and ACCUM."""
+    threshold(1)
+    shape = TC_DEA_FP8
+    T = 21
+    L = synth.make_layer(shape, 29, DEV)
+    x = synth.hidden(T, shape.d, 29, DEV)
+    oi, op, _ = O.route(x, L["router"], shape.k)
+    ws = B.new_workspace(T, shape.n, shape.k, shape.g)
+    B.moe_dispatch(torch.tensor(oi, device=DEV), torch.tensor(op, dtype=torch.float32, device=DEV), shape.n,
+                   shape.g, ws)
+    dept = (L["dgate"], L["dup"], L["ddown"])
+    priv = (L["pgate"], L["pup"], L["pdown"])
+    sh = H.shared_of(L)
+    y = torch.zeros((T, shape.d), device=DEV)
+    if mode == "rows":
+        rows = torch.empty((B.moe_rows_count(T, shape.n, shape.k, shape.g, True), shape.d), device=DEV)
+        B.deamoe_ffn(x, shape.k, shape.g, dept, priv, sh, ws, B.MOE_OUT_ROWS, rows, scales=scales_of(shape, L))
+        B.moe_combine(rows, T, shape.n, shape.k, shape.g, True, ws, y)
+    else:
+        B.deamoe_ffn(x, shape.k, shape.g, dept, priv, sh, ws, B.MOE_OUT_ACCUM, y, scales=scales_of(shape, L))
+    torch.cuda.synchronize()
+    assert B.moe_read_status(ws)[0] == 0
     ref = H.oracle_layer(shape, decoded(L), x, oi, op)
     assert H.rel_err(y.cpu().numpy(), ref) <= 1e-4
 

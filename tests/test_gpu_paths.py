@@ -103,7 +103,7 @@ def expected_auto_choice(shape, T, exp_count, dept_count, sms):
         classes.append((shape.I, exp_count))
     if shape.I_s > 0:
         classes.append((shape.I_s, [T]))
-    if shape.dtype != "bf16" or shape.d % 128 or any(r % 128 for r, _ in classes):
+    if shape.dtype not in ("bf16", "fp8") or shape.d % 128 or any(r % 128 for r, _ in classes):
         return 0
     wide = shape.d > 4096
     if T <= 4 and not wide:
