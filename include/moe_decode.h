@@ -142,8 +142,12 @@ int64_t moe_test_stall_weight_copies(int64_t wait_ns);
  *   exp_units int32[n][4] per active expert q < A_e: {expert, first assignment,
  *                        assignments, inclusive prefix over active experts of
  *                        ceil(assignments / 4)} -- the FFN's work table
- *   xb        bf16[2][T][8192] activations split as x = hi + lo (scratch of the
- *                        tensor-core FFN; rows packed at the call's d)
+ *   xb        4*T*8192 + 4*T bytes of tensor-core FFN scratch: bf16[2][T][d]
+ *                        activations split as x = hi + lo (bf16 weights), or
+ *                        for E4M3 weights four E4M3 terms u8[4][T][d] of the
+ *                        scaled activations and, at byte 4*T*8192, the scale
+ *                        exponent int32[T] of each token (rows packed at the
+ *                        call's d)
  *   dept_count int32[m]  tokens per department (m = n / experts_per_dept)
  *   dept_off  int32[m+1] exclusive prefix sum of dept_count
  *   dept_tok  int32[T*min(k,m)] tokens of each department (X^j), each once

@@ -70,7 +70,8 @@ bool layout_of(int T, int n, int k, int g, moe_ws_layout* L) {
     L->tok_asg = take((size_t)T * k * sizeof(int32_t));
     L->act_exp = take((size_t)n * sizeof(int32_t));
     L->exp_units = take((size_t)n * 4 * sizeof(int32_t));
-    L->xb = take((size_t)2 * T * moe::kMaxXbHidden * 2);
+    // bf16 hi / lo rows, or the E4M3 activation terms and their exponents
+    L->xb = take(moe::xq_exp_offset(T) + (size_t)T * sizeof(int32_t));
     L->dept_count = take((size_t)m * sizeof(int32_t));
     L->dept_off = take((size_t)(m + 1) * sizeof(int32_t));
     L->dept_tok = take((size_t)dk * sizeof(int32_t));
@@ -211,8 +212,8 @@ bool encode_weight_map(CUtensorMap* map, const void* base, int units, int rows, 
 }
 
 // TMA descriptor of one [units * rows, d] E4M3 weight tensor (one byte per
-// code): boxes of 128 columns x kTcBoxRows rows (16 KB), unswizzled; the
-// kernel's converter warps lay the values out for the MMA.
+// code): boxes of 128 columns x kTcBoxRows rows (16 KB) with the 128 B
+// swizzle; the kernel's converter warps lay the values out for the MMA.
 bool encode_weight_map_f8(CUtensorMap* map, const void* base, int units, int rows, int d) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
@@ -221,7 +222,7 @@ bool encode_weight_map_f8(CUtensorMap* map, const void* base, int units, int row
     const cuuint32_t box[2] = {128, (cuuint32_t)moe::kTcBoxRows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -300,7 +301,8 @@ int run_ffn(moe::FfnArgs& a, int T, int n, int k, int g, int has_shared, bool tc
         if (e != cudaSuccess) return cuda_fail(e, who);
     }
     if (tc && !x_split) {
-        e = moe::launch_split_x(a.x, (long long)T * a.d, a.ws.xb, as_stream(stream));
+        e = a.dtype == MOE_DTYPE_FP8_E4M3 ? moe::launch_split_terms(a.x, T, a.d, a.ws.xb, as_stream(stream))
+                                           : moe::launch_split_x(a.x, (long long)T * a.d, a.ws.xb, as_stream(stream));
         if (e != cudaSuccess) return cuda_fail(e, who);
     }
     a.auto_tc = tc && tc_min_tokens() == 0;
@@ -815,7 +817,7 @@ static int layer_route(const float* x, int T, int d, int n, int k, float scale, 
     r.g = g;
     r.y_zero = y;
     r.y_elems = (long long)T * d;
-    r.split_x = split_x ? 1 : 0;
+    r.split_x = split_x ? (a.dtype == MOE_DTYPE_FP8_E4M3 ? 2 : 1) : 0;
     r.fuse_dispatch = local ? 0 : 1;
     r.logits_only = local ? 1 : 0;
     if (local) {

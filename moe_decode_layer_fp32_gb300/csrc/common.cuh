@@ -3,6 +3,8 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 namespace moe {
@@ -69,6 +71,68 @@ __device__ __forceinline__ void split_activations(const float* x, long long elem
         split_bf16x8(x4[2 * i], x4[2 * i + 1], h, l);
         hi[i] = h;
         lo[i] = l;
+    }
+}
+
+// E4M3 activation terms (the tensor-core path for E4M3 weights, whose MMAs
+// take 8-bit operands on both sides).  Row t of x is scaled by 2^e0(t), e0
+// chosen so that max |x_t| 2^e0 lies in [128, 256), and written as kXTerms
+// E4M3 terms: q_0 = e4m3(v), v_1 = 16 (v - q_0), q_1 = e4m3(v_1), ... so that
+//     x_t = 2^-e0 (q_0 + q_1 / 16 + q_2 / 256 + q_3 / 4096) + residual,
+// each residual step exact in fp32 (|v - q_p| is at most half an E4M3 step,
+// at most v / 16, and representable), and the residual at most 2^-16 of
+// |x| per element (plus 2^-30 of max |x_t| from E4M3's subnormal floor).
+// Layout in the xb region: terms [kXTerms][T][d] bytes, then e0 as int32[T]
+// at byte offset xq_exp_offset(T).
+constexpr int kXTerms = 4;
+__host__ __device__ __forceinline__ size_t xq_exp_offset(int T) { return (size_t)4 * T * kMaxXbHidden; }
+
+// One token's row: lanes of one warp.  d % 8 == 0.
+__device__ __forceinline__ void split_e4m3_terms_warp(const float* x, int T, int d, int t, uint8_t* xq, int lane) {
+    const float4* xr = reinterpret_cast<const float4*>(x + (size_t)t * d);
+    float mx = 0.0f;
+    for (int i = lane; i < d / 4; i += 32) {
+        const float4 v = xr[i];
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+    __syncwarp();
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    // mx = f 2^E with f in [0.5, 1): mx 2^(8 - E) in [128, 256); kept within
+    // the range where 2^e0 and 2^(e0 + 4 (kXTerms - 1)) are normal floats
+    int e0 = 0;
+    if (mx > 0.0f) {
+        int E;
+        frexpf(mx, &E);
+        e0 = min(max(8 - E, -120), 126 - 4 * (kXTerms - 1));
+    }
+    if (lane == 0) reinterpret_cast<int32_t*>(xq + xq_exp_offset(T))[t] = e0;
+    const float sc = __int_as_float((e0 + 127) << 23);
+    for (int i = lane; i < d / 8; i += 32) {
+        float v[8];
+        const float4 a = xr[2 * i], b = xr[2 * i + 1];
+        v[0] = a.x * sc; v[1] = a.y * sc; v[2] = a.z * sc; v[3] = a.w * sc;
+        v[4] = b.x * sc; v[5] = b.y * sc; v[6] = b.z * sc; v[7] = b.w * sc;
+#pragma unroll
+        for (int p = 0; p < kXTerms; ++p) {
+            uint32_t w[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t word = 0u;
+#pragma unroll
+                for (int e = 0; e < 4; e += 2) {
+                    const int j = 4 * h + e;
+                    const __nv_fp8x2_storage_t q =
+                        __nv_cvt_float2_to_fp8x2(make_float2(v[j], v[j + 1]), __NV_SATFINITE, __NV_E4M3);
+                    const float2 back = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(q, __NV_E4M3)));
+                    v[j] = 16.0f * (v[j] - back.x);
+                    v[j + 1] = 16.0f * (v[j + 1] - back.y);
+                    word |= (uint32_t)q << (8 * e);
+                }
+                w[h] = word;
+            }
+            *reinterpret_cast<uint2*>(xq + ((size_t)p * T + t) * d + 8 * (size_t)i) = make_uint2(w[0], w[1]);
+        }
     }
 }
 

@@ -708,6 +708,12 @@ __global__ void split_x_kernel(const float* x, long long elems, __nv_bfloat16* x
                       (long long)gridDim.x * blockDim.x);
 }
 
+__global__ void split_terms_kernel(const float* x, int T, int d, uint8_t* xq) {
+    const int lane = threadIdx.x & 31;
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, nw = (gridDim.x * blockDim.x) >> 5;
+    for (int t = gw; t < T; t += nw) split_e4m3_terms_warp(x, T, d, t, xq, lane);
+}
+
 __global__ void zero_kernel(uint4* p, size_t n16) {
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16;
          i += (size_t)gridDim.x * blockDim.x)
@@ -785,6 +791,12 @@ cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t s) {
 }  // namespace moe
 
 namespace moe {
+cudaError_t launch_split_terms(const float* x, int T, int d, __nv_bfloat16* xb, cudaStream_t s) {
+    const int threads = 128;                  // a warp per token
+    split_terms_kernel<<<(T + 3) / 4, threads, 0, s>>>(x, T, d, reinterpret_cast<uint8_t*>(xb));
+    return cudaGetLastError();
+}
+
 cudaError_t launch_split_x(const float* x, long long elems, __nv_bfloat16* xb, cudaStream_t s) {
     const long long n8 = elems / 8;
     const int threads = 256;

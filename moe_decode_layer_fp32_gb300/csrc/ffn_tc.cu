@@ -29,13 +29,20 @@
 // layer) into swizzled B tiles with cp.async.
 //
 // FP8 (E4M3 codes, one fp32 scale per weight row): TMA lands 16 KB boxes of
-// codes (128 rows x 128 columns) in a 5-stage ring, and four more warps
-// (10-13) expand each box into the bf16 layout above, in a 3-stage ring the
-// MMAs read.  Every E4M3 value is exact in bf16, so the products are those of
-// the bf16 path on the codes; the epilogue multiplies the gate and up results
-// by their row scales and folds the down row scale into H (a down row is a K
-// index of the down MMA).  Groups hold 16 tokens here, which frees the shared
-// memory for the deeper code ring.
+// codes (128 rows x 128 columns, 128 B swizzle) in a 6-stage ring.  Gate / up
+// boxes are the A operand of kind::f8f6f4 MMAs as they are (K = 32 per
+// instruction: half the instructions of the bf16 path per weight column, and
+// an MMA instruction, not HBM, is what bounds a tile of few tokens); B holds
+// the activations as four E4M3 terms per token (x = 2^-e0 sum_p 16^-p q_p,
+// split once per layer), so N = 4 Mp and the epilogue sums the four result
+// columns of each token.  Down boxes are expanded to bf16 by four more warps
+// (10-13) into a 2-stage ring that the down MMAs read MN-major as on the bf16
+// path (W_down is read transposed).  E4M3 values are exact in bf16 and the
+// products of two E4M3 values exact in the MMA, so the rounding is that of the
+// fp32 accumulation and of the activation terms (2^-16 of each element); the
+// epilogue multiplies the gate and up results by their row scales and folds the
+// down row scale into H (a down row is a K index of the down MMA).  Groups
+// hold 16 tokens here, which frees the shared memory for the code ring.
 // Every wait is bounded; on a timeout the kernel records an error status,
 // drains its copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -70,25 +77,27 @@ constexpr int kF8Box = kTcRows * 128;             // 16 KB: 128 rows x 128 E4M3 
 #define MOE_TC_BPAIRS 3
 #endif
 #ifndef MOE_TC_F8_STAGES
-#define MOE_TC_F8_STAGES 5
+#define MOE_TC_F8_STAGES 6
 #endif
 #ifndef MOE_TC_F8_CSTAGES
-#define MOE_TC_F8_CSTAGES 3
+#define MOE_TC_F8_CSTAGES 2
 #endif
 constexpr int kTmemCols = 512;
-constexpr uint32_t kColG = 0, kColU = 64, kColY = 128;
-constexpr int kYBufs = 6;                         // down accumulators, 64 columns each
 
 // Per weight type: bf16 (F8 = false) or E4M3 codes with row scales.
 template <bool F8>
 struct TcGeo {
-    static constexpr int kTok = F8 ? 16 : kTcGroupTokens;   // tokens per group (hi + lo rows: N <= 2 kTok)
-    static constexpr int kMaxN = 2 * kTok;
-    static constexpr int kAStages = F8 ? MOE_TC_F8_CSTAGES : MOE_TC_STAGES;   // ring the MMAs read (bf16 boxes)
-    static constexpr int kF8Stages = F8 ? MOE_TC_F8_STAGES : 0;   // ring of code boxes
-    static constexpr int kBPairs = MOE_TC_BPAIRS;            // activation ring (K-pairs)
-    static constexpr int kBBlock = kMaxN * 128;              // activations of one K-block: N rows x 128 B
-    static constexpr int kBPair = 2 * kBBlock;               // ... of one K-pair
+    static constexpr int kTok = F8 ? 16 : kTcGroupTokens;   // tokens per group
+    static constexpr int kMaxN = 2 * kTok;                   // down MMA N: H hi + lo rows
+    // gate / up B operand: rows per token (bf16 hi + lo, or the E4M3 terms)
+    static constexpr int kBTerms = F8 ? kXTerms : 2;
+    static constexpr int kMaxNgu = kBTerms * kTok;           // 64
+    static constexpr int kAStages = F8 ? MOE_TC_F8_CSTAGES : MOE_TC_STAGES;   // bf16 boxes the MMAs read
+    static constexpr int kF8Stages = F8 ? MOE_TC_F8_STAGES : 0;                // code boxes
+    static constexpr int kBPairs = MOE_TC_BPAIRS;            // activation ring (128-column K steps)
+    static constexpr int kBBlock = kMaxNgu * 128;            // one 128-byte K-block of every B row: 8 KB
+    static constexpr int kBBlocks = F8 ? 1 : 2;              // K-blocks per 128-column step
+    static constexpr int kBPair = kBBlocks * kBBlock;
     static constexpr int kHChunk = kMaxN * 128;              // H: [K chunk][N rows][128 B]
     static constexpr int kHTile = 2 * kHChunk;               // K = 128 tile rows
     static constexpr int kYStage = kTok * 128 * 4;           // down output of one M-tile: [token][128 fp32]
@@ -96,24 +105,33 @@ struct TcGeo {
     static constexpr int kWarps = 10 + kCvtWarps;
     static constexpr int kThreads = kWarps * 32;
     static constexpr int kPdTok = F8 ? 1 : kTok;             // form-P down lists (bf16 only)
+    // Tensor memory (512 columns): the G and U accumulators (N = kBTerms Mp
+    // columns each), then the down accumulators (kYBufs of kYCols columns).
+    static constexpr uint32_t kColG = 0;
+    static constexpr uint32_t kColU = kMaxNgu;
+    static constexpr uint32_t kColY = 2 * kMaxNgu;
+    static constexpr uint32_t kYCols = kMaxN;
+    static constexpr int kYBufs = (int)((kTmemCols - kColY) / kYCols);
 };
 
 template <class G>
 struct TcSmem {
     uint64_t full[G::kAStages];   // weight stage ready: TMA bytes landed (bf16) / converted (FP8)
     uint64_t empty[G::kAStages];  // MMAs reading the weight stage are done
-    uint64_t full8[G::kF8Stages > 0 ? G::kF8Stages : 1];   // code box landed
-    uint64_t empty8[G::kF8Stages > 0 ? G::kF8Stages : 1];  // code box converted
+    uint64_t full8[G::kF8Stages > 0 ? G::kF8Stages : 1];   // gate / up code box landed (MMA waits)
+    uint64_t full8d[G::kF8Stages > 0 ? G::kF8Stages : 1];  // down code box landed (converters wait)
+    uint64_t empty8[G::kF8Stages > 0 ? G::kF8Stages : 1];  // code box slot free again
     uint64_t bx_full[G::kBPairs];  // activation K-pair gathered
     uint64_t bx_empty[G::kBPairs]; // MMAs reading the activation K-pair are done
     uint64_t acc_full, acc_empty, h_full, mma_done;
-    uint64_t y_full[kYBufs], y_empty[kYBufs];
+    uint64_t y_full[G::kYBufs], y_empty[G::kYBufs];
     uint32_t tmem_base;
     int cls_units[3];
     int cls_groups[3];
     int cls_off[3];
     int ep_row[4][G::kTok];       // epilogue warps: output row of each tile token
     float ep_w[4][G::kTok];       // ... and its routing weight
+    float ep_xs[4][G::kTok];      // ... and (E4M3 terms) 2^-e0 of its activation row
     // form-P down pass: each tile token's assignments in the department
     // (zbuf row and routing weight)
     int pd_cnt[G::kPdTok];
@@ -123,7 +141,7 @@ struct TcSmem {
 };
 
 // E4M3 -> bf16 on the integer and FMA pipes (the conversion instructions
-// issue at a quarter of their rate and bound the converter warps).  A code
+// issue at a quarter of their rate).  A code
 // s eeee mmm and the bf16 pattern s 0000eeee mmm0000 have the same sign and
 // significand, and the pattern's value is the code's times 2^-120 (exponent
 // bias 127 against 7); codes with eeee = 0 (E4M3 subnormals) land on bf16
@@ -227,6 +245,8 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
     constexpr int kBBlock = G::kBBlock, kBPair = G::kBPair, kHChunk = G::kHChunk, kHTile = G::kHTile;
     constexpr int kYStage = G::kYStage;
     constexpr int kTcWarps = G::kWarps, kTcThreads = G::kThreads;
+    constexpr uint32_t kColG = G::kColG, kColU = G::kColU, kColY = G::kColY, kYCols = G::kYCols;
+    constexpr int kYBufs = G::kYBufs;
     extern __shared__ unsigned char smem_dyn[];
     // 1024-byte aligned tile regions (128 B swizzle atoms)
     unsigned char* base = reinterpret_cast<unsigned char*>(
@@ -249,7 +269,8 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
         }
         for (int i = 0; i < kF8Stages; ++i) {
             mbar_init(&sm.full8[i], 1);
-            mbar_init(&sm.empty8[i], G::kCvtWarps);
+            mbar_init(&sm.full8d[i], 1);
+            mbar_init(&sm.empty8[i], 1);
         }
         for (int i = 0; i < kTcBPairs; ++i) {
             mbar_init(&sm.bx_full[i], 4);
@@ -386,19 +407,31 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
             uint32_t it = 0;
             int r = r_begin;
             TSeg s;
-            // the ring TMA writes: the MMAs' (bf16) or the converters' (FP8)
+            // the ring TMA writes: the MMAs' (bf16) or the code boxes (FP8),
+            // whose gate / up boxes complete on full8 (the MMA reads them)
+            // and down boxes on full8d (the converters read them): each
+            // barrier has one waiter, which takes its phases in order
             constexpr int NS = F8 ? kF8Stages : kTcStages;
             constexpr int SB = F8 ? kF8Box : kAStage;
             unsigned char* ring = F8 ? f8ring : aring;
-            uint64_t* fullb = F8 ? sm.full8 : sm.full;
             uint64_t* emptyb = F8 ? sm.empty8 : sm.empty;
+            uint32_t par_g = 0u, par_d = 0u, last_d = 0u;   // per slot: next phase parity, last box kind
             // columns [128 cb, 128 cb + 128) of weight rows [y, y + 128)
-            auto load = [&](const CUtensorMap* m, int y, int cb) -> bool {
+            auto load = [&](const CUtensorMap* m, int y, int cb, bool down) -> bool {
                 const int slot = it % NS;
                 if (!wait(&emptyb[slot], ((it / NS) & 1u) ^ 1u)) return false;
-                mbar_arrive_expect_tx(&fullb[slot], SB);
-                if (F8) tma_load_2d(ring + slot * SB, m, 128 * cb, y, &fullb[slot], pol);
-                else tma_load_3d(ring + slot * SB, m, 0, y, 2 * cb, &fullb[slot], pol);
+                uint64_t* fb = F8 ? (down ? &sm.full8d[slot] : &sm.full8[slot]) : &sm.full[slot];
+                mbar_arrive_expect_tx(fb, SB);
+                if (F8) tma_load_2d(ring + slot * SB, m, 128 * cb, y, fb, pol);
+                else tma_load_3d(ring + slot * SB, m, 0, y, 2 * cb, fb, pol);
+                const uint32_t bit = 1u << slot;
+                if (down) {
+                    par_d ^= bit;
+                    last_d |= bit;
+                } else {
+                    par_g ^= bit;
+                    last_d &= ~bit;
+                }
                 ++it;
                 return true;
             };
@@ -407,21 +440,26 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
                 const int y = rec.x * a.f.cls[s.cls].rows + s.row0;
                 const CUtensorMap* maps = a.maps[s.cls];
                 for (int p = 0; ok && has_gu && p < KP; ++p) {
-                    if (!load(&maps[0], y, p)) break;
-                    if (!load(&maps[1], y, p)) break;
+                    if (!load(&maps[0], y, p, false)) break;
+                    if (!load(&maps[1], y, p, false)) break;
                 }
                 for (int mt = 0; ok && has_dn && mt < DT; ++mt)
-                    if (!load(&maps[2], y, mt)) break;
+                    if (!load(&maps[2], y, mt, F8)) break;
             }
-            // every issued copy must land before the CTA may exit
-            const uint32_t first = it > (uint32_t)NS ? it - NS : 0u;
-            for (uint32_t i = first; i < it; ++i)
-                mbar_wait_bounded(&fullb[i % NS], (i / NS) & 1u);
+            // every issued copy must land before the CTA may exit: the last
+            // copy into each slot (the earlier ones were waited for before
+            // the slot was refilled), on the barrier it completes
+            for (int slot = 0; slot < NS && slot < (int)it; ++slot) {
+                const bool dn = (last_d >> slot) & 1u;
+                uint64_t* fb = F8 ? (dn ? &sm.full8d[slot] : &sm.full8[slot]) : &sm.full[slot];
+                mbar_wait_bounded(fb, (((dn ? par_d : par_g) >> slot) & 1u) ^ 1u);
+            }
         }
     } else if (warp == 1) {
         // ===================== MMA issuer =====================
         if (lane == 0) {
             uint32_t it = 0, bp = 0, ti = 0, dtc = 0;
+            uint32_t it8 = 0, par_g = 0u;   // FP8: code boxes taken; per slot, next full8 phase parity
             int r = r_begin;
             TSeg s;
             // descriptors: address field += byte offset >> 4 (all of smem < 256 KB)
@@ -429,11 +467,13 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
             const uint64_t a_mn = smem_desc_sw128(smem_u32(aring), kChunkBytes, 1024); // MN-major
             const uint64_t b_k = smem_desc_sw128(smem_u32(bring), 16, 1024);
             const uint64_t h_k = smem_desc_sw128(smem_u32(htile), 16, 1024);
+            const uint64_t a8 = smem_desc_sw128(smem_u32(f8ring), 16, 1024);         // code boxes, K-major
             while (ok && next_tile(a, sm, r, r_end, s)) {
                 const int4 rec = sm.units[sm.cls_off[s.cls] + s.q];
                 const int mg = min(kTcTokens, rec.z - s.grp * kTcTokens);
                 const int N = 2 * ((mg + 7) & ~7);
-                const uint32_t id_gu = idesc_bf16_f32(128, N, false, false);
+                const uint32_t id_gu = F8 ? idesc_e4m3_f32(128, G::kBTerms * (N / 2))
+                                          : idesc_bf16_f32(128, N, false, false);
                 const uint32_t id_dn = idesc_bf16_f32(128, N, true, false);
                 if (has_gu) {
                 if (!wait(&sm.acc_empty, (ti & 1u) ^ 1u)) break;
@@ -442,13 +482,32 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
                     const uint32_t bslot = bp % kTcBPairs;
                     if (!wait(&sm.bx_full[bslot], (bp / kTcBPairs) & 1u)) break;
                     const uint64_t bd = b_k + ((bslot * kBPair) >> 4);
+                    if constexpr (F8) {
+                        // A: the code box itself (128 rows x 128 codes, K-major,
+                        // 128 B swizzle); B: the activation terms; K = 32 a MMA
+#pragma unroll
+                        for (int gu = 0; gu < 2; ++gu, ++it8) {
+                            const uint32_t slot = it8 % kF8Stages;
+                            const uint32_t par = (par_g >> slot) & 1u;
+                            par_g ^= 1u << slot;
+                            if (!wait(&sm.full8[slot], par)) break;
+                            tc_fence_after_sync();
+                            const uint32_t acc_col = tmem + (gu ? kColU : kColG);
+                            const uint64_t ad = a8 + ((slot * kF8Box) >> 4);
+#pragma unroll
+                            for (int ks = 0; ks < 4; ++ks)
+                                umma_e4m3(acc_col, ad + ((ks * 32) >> 4), bd + ((ks * 32) >> 4), id_gu,
+                                          (p | ks) ? 1u : 0u);
+                            umma_commit(&sm.empty8[slot]);
+                        }
+                    } else {
 #pragma unroll
                     for (int gu = 0; gu < 2; ++gu, ++it) {
                         const uint32_t slot = it % kTcStages;
                         if (!wait(&sm.full[slot], (it / kTcStages) & 1u)) break;
                         tc_fence_after_sync();
-                        const uint64_t ad = a_k + ((slot * kAStage) >> 4);
                         const uint32_t acc_col = tmem + (gu ? kColU : kColG);
+                        const uint64_t ad = a_k + ((slot * kAStage) >> 4);
 #pragma unroll
                         for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
@@ -457,6 +516,7 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
                                           bd + ((kb * kBBlock + ks * 32) >> 4), id_gu,
                                           (p | kb | ks) ? 1u : 0u);
                         umma_commit(&sm.empty[slot]);
+                    }
                     }
                     umma_commit(&sm.bx_empty[bslot]);
                 }
@@ -474,11 +534,17 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
                 for (int mt = 0; ok && mt < DT; ++mt, ++it, ++dtc) {
                     const uint32_t slot = it % kTcStages;
                     if (!wait(&sm.full[slot], (it / kTcStages) & 1u)) break;
+                    if constexpr (F8) {
+                        // the converters are done with the code box: its slot
+                        // may be refilled
+                        mbar_arrive(&sm.empty8[it8 % kF8Stages]);
+                        ++it8;
+                    }
                     const uint32_t yb = dtc % kYBufs;
                     if (!wait(&sm.y_empty[yb], ((dtc / kYBufs) & 1u) ^ 1u)) break;
                     tc_fence_after_sync();
                     const uint64_t ad = a_mn + ((slot * kAStage) >> 4);
-                    const uint32_t ycol = tmem + kColY + yb * 64;
+                    const uint32_t ycol = tmem + kColY + yb * kYCols;
 #pragma unroll
                     for (int ks = 0; ks < kTcRows / 16; ++ks)
                         umma_bf16(ycol, ad + ((ks * 2048) >> 4),
@@ -515,6 +581,12 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
                 tile_token<LOCAL>(a, lr, kind, first + lane, t, w, row);
                 sm.ep_row[quarter][lane] = row;
                 sm.ep_w[quarter][lane] = w;
+                if constexpr (F8) {
+                    // 2^-e0 of the token's activation terms (e0 in [-120, 114])
+                    const int e0 = reinterpret_cast<const int32_t*>(
+                        reinterpret_cast<const unsigned char*>(a.f.ws.xb) + xq_exp_offset(a.f.T))[t];
+                    sm.ep_xs[quarter][lane] = __int_as_float((127 - e0) << 23);
+                }
             }
             // FP8: this thread's weight row's scales (gate, up, down)
             float sg = 1.0f, su = 1.0f, sdn = 1.0f;
@@ -604,32 +676,54 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
                 continue;
             }
             for (int c0 = 0; c0 < Mp; c0 += 16) {
-                // the four loads of a column block share one completion wait
-                uint32_t ghi[16], glo[16], uhi[16], ulo[16];
-                tmem_ld16_async(tmem + lanes + kColG + c0, ghi);
-                tmem_ld16_async(tmem + lanes + kColG + Mp + c0, glo);
-                tmem_ld16_async(tmem + lanes + kColU + c0, uhi);
-                tmem_ld16_async(tmem + lanes + kColU + Mp + c0, ulo);
-                tmem_wait_ld();
-                tmem_regs_ready(ghi);
-                tmem_regs_ready(glo);
-                tmem_regs_ready(uhi);
-                tmem_regs_ready(ulo);
                 // every column of the block is computed (the unused ones from
                 // whatever TMEM holds) and only the stores are guarded, so the
                 // sixteen chains interleave
                 float hv[16];
+                if constexpr (F8) {
+                    // g = 2^-e0 sum_p 16^-p G_p, the same for u; then the rows' scales
+                    float gs[16], us[16];
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    float g = __uint_as_float(ghi[jj]) + __uint_as_float(glo[jj]);
-                    float u = __uint_as_float(uhi[jj]) + __uint_as_float(ulo[jj]);
-                    if constexpr (F8) {
-                        g *= sg;
-                        u *= su;
+                    for (int jj = 0; jj < 16; ++jj) gs[jj] = us[jj] = 0.0f;
+#pragma unroll
+                    for (int p = 0; p < kXTerms; ++p) {
+                        uint32_t gp[16], up[16];
+                        tmem_ld16_async(tmem + lanes + kColG + p * Mp + c0, gp);
+                        tmem_ld16_async(tmem + lanes + kColU + p * Mp + c0, up);
+                        tmem_wait_ld();
+                        tmem_regs_ready(gp);
+                        tmem_regs_ready(up);
+                        const float f = 1.0f / (float)(1 << (4 * p));
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            gs[jj] += __uint_as_float(gp[jj]) * f;
+                            us[jj] += __uint_as_float(up[jj]) * f;
+                        }
                     }
-                    hv[jj] = silu_fast(g) * u;
-                    if (a.f.out_mode == MOE_OUT_ACCUM) hv[jj] *= sm.ep_w[quarter][c0 + jj];
-                    if constexpr (F8) hv[jj] *= sdn;
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const float xs = sm.ep_xs[quarter][(c0 + jj) & (kTcTokens - 1)];
+                        hv[jj] = silu_fast(gs[jj] * xs * sg) * (us[jj] * xs * su) * sdn;
+                        if (a.f.out_mode == MOE_OUT_ACCUM) hv[jj] *= sm.ep_w[quarter][(c0 + jj) & (kTcTokens - 1)];
+                    }
+                } else {
+                    // the four loads of a column block share one completion wait
+                    uint32_t ghi[16], glo[16], uhi[16], ulo[16];
+                    tmem_ld16_async(tmem + lanes + kColG + c0, ghi);
+                    tmem_ld16_async(tmem + lanes + kColG + Mp + c0, glo);
+                    tmem_ld16_async(tmem + lanes + kColU + c0, uhi);
+                    tmem_ld16_async(tmem + lanes + kColU + Mp + c0, ulo);
+                    tmem_wait_ld();
+                    tmem_regs_ready(ghi);
+                    tmem_regs_ready(glo);
+                    tmem_regs_ready(uhi);
+                    tmem_regs_ready(ulo);
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        hv[jj] = silu_fast(__uint_as_float(ghi[jj]) + __uint_as_float(glo[jj])) *
+                                 (__uint_as_float(uhi[jj]) + __uint_as_float(ulo[jj]));
+                        if (a.f.out_mode == MOE_OUT_ACCUM) hv[jj] *= sm.ep_w[quarter][c0 + jj];
+                    }
                 }
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
@@ -661,7 +755,7 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
                 const uint32_t yb = dtc % kYBufs;
                 if (!wait(&sm.y_full[yb], (dtc / kYBufs) & 1u)) break;
                 tc_fence_after_sync();
-                const uint32_t ycol = kColY + yb * 64;
+                const uint32_t ycol = kColY + yb * kYCols;
                 for (int c0 = 0; c0 < Mp; c0 += 16) {
                     uint32_t yhi[16], ylo[16];
                     tmem_ld16_async(tmem + lanes + ycol + c0, yhi);
@@ -693,12 +787,15 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
         }
     } else if (warp < 10) {
         // ===================== activation gather =====================
-        // B tiles (one K-pair per slot) are copied with cp.async from the bf16
-        // hi / lo activations (split once per layer), kPre pairs ahead of the MMA.
+        // B tiles (one 128-column K step per slot) are copied with cp.async
+        // from the split activations (once per layer), kPre steps ahead of
+        // the MMA: B row n = term * Mp + j holds term n / Mp (bf16 hi, lo; or
+        // E4M3 term 0..3) of the tile's token j, 128 bytes per K-block.
         constexpr int kPre = kTcBPairs - 1;
         const int ct = tid - 6 * 32;                    // 0..127
-        const __nv_bfloat16* xh = a.f.ws.xb;
-        const __nv_bfloat16* xl = a.f.ws.xb + (size_t)a.f.T * d;
+        const unsigned char* xs = reinterpret_cast<const unsigned char*>(a.f.ws.xb);
+        // bytes of one term's [T, d] rows, and of one row
+        const size_t term_bytes = (size_t)a.f.T * d * (F8 ? 1 : 2), row_bytes = (size_t)d * (F8 ? 1 : 2);
         uint32_t bp = 0;
         int r = r_begin;
         TSeg s;
@@ -708,22 +805,22 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
             const int first = rec.y + s.grp * kTcTokens;
             const int mg = min(kTcTokens, rec.z - s.grp * kTcTokens);
             const int Mp = (mg + 7) & ~7;
-            const int items = 2 * Mp * 8;               // (B row, 16-byte chunk) pairs per K-block
+            const int items = G::kBTerms * Mp * 8;      // (B row, 16-byte chunk) pairs per K-block
             // this thread's items are fixed for the tile: resolve them once
-            const __nv_bfloat16* src[4];
+            const unsigned char* src[4];
             int dst[4];
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
                 const int item = ct + k4 * 128;
                 const int n = item >> 3, c = item & 7;
-                const int j = n < Mp ? n : n - Mp;
+                const int term = n / Mp, j = n - term * Mp;
                 src[k4] = nullptr;
                 dst[k4] = item < items ? n * 128 + ((c ^ (n & 7)) << 4) : -1;
                 if (item < items && j < mg) {
                     int t, row;
                     float w;
                     tile_token<LOCAL>(a, lr, kind, first + j, t, w, row);
-                    src[k4] = (n < Mp ? xh : xl) + (size_t)t * d + c * 8;
+                    src[k4] = xs + term * term_bytes + (size_t)t * row_bytes + c * 16;
                 }
             }
             auto issue = [&](int p) -> bool {
@@ -732,12 +829,12 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
                 if (!wait(&sm.bx_empty[slot], ((b / kTcBPairs) & 1u) ^ 1u)) return false;
                 unsigned char* Bt = bring + slot * kBPair;
 #pragma unroll
-                for (int kb = 0; kb < 2; ++kb)
+                for (int kb = 0; kb < G::kBBlocks; ++kb)
 #pragma unroll
                     for (int k4 = 0; k4 < 4; ++k4) {
                         if (dst[k4] >= 0) {
                             unsigned char* dp = Bt + kb * kBBlock + dst[k4];
-                            if (src[k4]) cp_async16(dp, src[k4] + (2 * p + kb) * 64);
+                            if (src[k4]) cp_async16(dp, src[k4] + (size_t)(G::kBBlocks * p + kb) * 128);
                             else *reinterpret_cast<uint4*>(dp) = make_uint4(0u, 0u, 0u, 0u);
                         }
                     }
@@ -772,35 +869,42 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
         cp_async_wait<0>();
     } else if constexpr (F8) {
         // ===================== FP8 converters =====================
-        // Warp cw expands rows [32 cw, 32 cw + 32) of each code box, four rows
-        // a step (eight steps).  Within a step, the eight lanes of each shared-memory phase
-        // read half a row each of two adjacent rows (128 distinct bytes) and
-        // write their bf16 units to one chunk's even and the other chunk's odd
-        // swizzled positions, so neither the loads nor the stores conflict.
+        // Down code boxes (128 rows of W_down x 128 hidden columns, landed
+        // with the 128 B swizzle: unit u of row r at u ^ (r & 7)) -> the bf16
+        // shared-memory ring the down MMAs read MN-major.  Warp cw expands
+        // rows [32 cw, 32 cw + 32), four rows a step; within a step the eight
+        // lanes of each shared-memory phase read half a row each of two
+        // adjacent rows and write their bf16 units to one chunk's even and
+        // the other chunk's odd swizzled positions, so neither the loads nor
+        // the stores conflict.  Gate / up boxes go to the MMA as they are.
         constexpr int kRowsPerCvt = kTcRows / G::kCvtWarps;   // 32
         const int cw = warp - 10;
         const int pr = lane >> 4, ph = (lane >> 3) & 1, sub = (lane >> 2) & 1;
         const int q = ((sub ^ ph) << 2) | (lane & 3);   // 16-code unit of the row
         const int rsub = 2 * pr + sub;                   // row within the step
         const int u0 = 2 * (q & 3);                      // first bf16 unit in the chunk
-        const int per_tile = 2 * KP + DT;                // boxes per tile
-        uint32_t it = 0;
+        uint32_t it8 = 0, itc = 0, par_d = 0u;           // boxes, down boxes, per-slot full8d parity
         int r = r_begin;
         TSeg s;
         while (ok && next_tile(a, sm, r, r_end, s)) {
-            for (int st = 0; st < per_tile; ++st, ++it) {
-                const uint32_t s8 = it % kF8Stages, sc = it % kTcStages;
-                if (!wait(&sm.full8[s8], (it / kF8Stages) & 1u)) break;
-                if (!wait(&sm.empty[sc], ((it / kTcStages) & 1u) ^ 1u)) break;
-                const unsigned char* src = f8ring + s8 * kF8Box + q * 16;
+            it8 += 2 * KP;                               // the tile's gate / up boxes
+            for (int mt = 0; mt < DT; ++mt, ++it8, ++itc) {
+                const uint32_t s8 = it8 % kF8Stages, sc = itc % kTcStages;
+                const uint32_t par = (par_d >> s8) & 1u;
+                par_d ^= 1u << s8;
+                if (!wait(&sm.full8d[s8], par)) break;
+                if (!wait(&sm.empty[sc], ((itc / kTcStages) & 1u) ^ 1u)) break;
+                const unsigned char* box = f8ring + s8 * kF8Box;
                 unsigned char* dst = aring + sc * kAStage + (q >> 2) * kChunkBytes;
                 // all loads first: the compiler cannot tell the two rings
                 // apart and would otherwise keep each load behind the
                 // previous step's stores
                 uint4 w[kRowsPerCvt / 4];
 #pragma unroll
-                for (int i = 0; i < kRowsPerCvt / 4; ++i)
-                    w[i] = *reinterpret_cast<const uint4*>(src + (cw * kRowsPerCvt + i * 4 + rsub) * 128);
+                for (int i = 0; i < kRowsPerCvt / 4; ++i) {
+                    const int row = cw * kRowsPerCvt + i * 4 + rsub;
+                    w[i] = *reinterpret_cast<const uint4*>(box + row * 128 + ((q ^ (row & 7)) << 4));
+                }
 #pragma unroll
                 for (int i = 0; i < kRowsPerCvt / 4; ++i) {
                     const int row = cw * kRowsPerCvt + i * 4 + rsub;
@@ -812,10 +916,7 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
                 }
                 fence_async_smem();      // the stores are read by the MMA (async proxy)
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&sm.full[sc]);
-                    mbar_arrive(&sm.empty8[s8]);
-                }
+                if (lane == 0) mbar_arrive(&sm.full[sc]);
             }
         }
     }

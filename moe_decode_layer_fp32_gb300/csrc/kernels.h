@@ -27,7 +27,8 @@ struct RouteArgs {
     int g;                   // experts per department
     float* y_zero;           // zeroed by the route grid when non-null
     long long y_elems;
-    int split_x;             // also write the bf16 hi/lo activations (ws.xb)
+    int split_x;             // also write the activations into ws.xb: 1 bf16 hi/lo,
+                             // 2 E4M3 terms (split_e4m3_terms_warp)
     // Whole-layer path with routing in the FFN kernel: write the logits only
     // (no top-k, no dispatch); the FFN CTAs take it from there.
     int logits_only;
@@ -237,6 +238,8 @@ bool ffn_tc_local_route_fits(const FfnArgs& a);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
 cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t s);
 cudaError_t launch_split_x(const float* x, long long elems, __nv_bfloat16* xb, cudaStream_t s);
+// x [T, d] -> the E4M3 activation terms and exponents in the xb region.
+cudaError_t launch_split_terms(const float* x, int T, int d, __nv_bfloat16* xb, cudaStream_t s);
 
 int device_sm_count();
 

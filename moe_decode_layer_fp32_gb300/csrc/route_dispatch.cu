@@ -272,9 +272,15 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
     // that kernel's completion here.
     pdl_wait_primary();
 
-    if (a.split_x)
+    if (a.split_x == 1)
         split_activations(a.x, (long long)a.T * a.d, a.ws.xb, blockIdx.x * (long long)kRouteThreads + tid,
                           (long long)gridDim.x * kRouteThreads);
+    if (a.split_x == 2) {
+        // a warp per token
+        const int gw = (blockIdx.x * kRouteThreads + tid) >> 5, nw = (gridDim.x * kRouteThreads) >> 5;
+        for (int t = gw; t < a.T; t += nw)
+            split_e4m3_terms_warp(a.x, a.T, a.d, t, reinterpret_cast<uint8_t*>(a.ws.xb), tid & 31);
+    }
     if (a.y_zero) {
         float4* y4 = reinterpret_cast<float4*>(a.y_zero);
         const long long n4 = a.y_elems >> 2;
