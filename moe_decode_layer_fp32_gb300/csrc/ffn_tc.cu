@@ -68,7 +68,6 @@ namespace {
 // stage, then the up stage, of the same two K-blocks.
 constexpr int kTcRows = kTcBoxRows;               // 128
 constexpr int kChunkBytes = kTcRows * 128;        // 16 KB: one 64-column chunk
-constexpr int kAStage = 2 * kChunkBytes;          // 32 KB
 constexpr int kF8Box = kTcRows * 128;             // 16 KB: 128 rows x 128 E4M3 codes
 #ifndef MOE_TC_STAGES
 #define MOE_TC_STAGES 4
@@ -82,6 +81,9 @@ constexpr int kF8Box = kTcRows * 128;             // 16 KB: 128 rows x 128 E4M3 
 #ifndef MOE_TC_F8_CSTAGES
 #define MOE_TC_F8_CSTAGES 2
 #endif
+#ifndef MOE_TC_F8_CROWS
+#define MOE_TC_F8_CROWS 128
+#endif
 constexpr int kTmemCols = 512;
 
 // Per weight type: bf16 (F8 = false) or E4M3 codes with row scales.
@@ -92,7 +94,13 @@ struct TcGeo {
     // gate / up B operand: rows per token (bf16 hi + lo, or the E4M3 terms)
     static constexpr int kBTerms = F8 ? kXTerms : 2;
     static constexpr int kMaxNgu = kBTerms * kTok;           // 64
-    static constexpr int kAStages = F8 ? MOE_TC_F8_CSTAGES : MOE_TC_STAGES;   // bf16 boxes the MMAs read
+    static constexpr int kAStages = F8 ? MOE_TC_F8_CSTAGES : MOE_TC_STAGES;   // bf16 slots the MMAs read
+    // rows (down: K) of a bf16 slot: whole boxes (half boxes, which let the
+    // down MMAs of one half run while the converters fill the next, measured
+    // slower: twice the hand-offs)
+    static constexpr int kCRows = F8 ? MOE_TC_F8_CROWS : kTcRows;
+    static constexpr int kAChunk = kCRows * 128;             // one 64-column chunk of a slot
+    static constexpr int kASlot = 2 * kAChunk;
     static constexpr int kF8Stages = F8 ? MOE_TC_F8_STAGES : 0;                // code boxes
     static constexpr int kBPairs = MOE_TC_BPAIRS;            // activation ring (128-column K steps)
     static constexpr int kBBlock = kMaxNgu * 128;            // one 128-byte K-block of every B row: 8 KB
@@ -253,7 +261,7 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
         (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
     unsigned char* f8ring = base;                    // FP8: code boxes (empty for bf16)
     unsigned char* aring = f8ring + kF8Stages * kF8Box;
-    unsigned char* bring = aring + kTcStages * kAStage;
+    unsigned char* bring = aring + kTcStages * G::kASlot;
     unsigned char* htile = bring + kTcBPairs * kBPair;
     float* ystage = reinterpret_cast<float*>(htile + kHTile);
     TcSmem<G>& sm = *reinterpret_cast<TcSmem<G>*>(htile + kHTile + kYStage);
@@ -412,7 +420,7 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
             // and down boxes on full8d (the converters read them): each
             // barrier has one waiter, which takes its phases in order
             constexpr int NS = F8 ? kF8Stages : kTcStages;
-            constexpr int SB = F8 ? kF8Box : kAStage;
+            constexpr int SB = F8 ? kF8Box : G::kASlot;
             unsigned char* ring = F8 ? f8ring : aring;
             uint64_t* emptyb = F8 ? sm.empty8 : sm.empty;
             uint32_t par_g = 0u, par_d = 0u, last_d = 0u;   // per slot: next phase parity, last box kind
@@ -464,7 +472,7 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
             TSeg s;
             // descriptors: address field += byte offset >> 4 (all of smem < 256 KB)
             const uint64_t a_k = smem_desc_sw128(smem_u32(aring), 16, 1024);          // K-major
-            const uint64_t a_mn = smem_desc_sw128(smem_u32(aring), kChunkBytes, 1024); // MN-major
+            const uint64_t a_mn = smem_desc_sw128(smem_u32(aring), G::kAChunk, 1024);  // MN-major
             const uint64_t b_k = smem_desc_sw128(smem_u32(bring), 16, 1024);
             const uint64_t h_k = smem_desc_sw128(smem_u32(htile), 16, 1024);
             const uint64_t a8 = smem_desc_sw128(smem_u32(f8ring), 16, 1024);         // code boxes, K-major
@@ -507,7 +515,7 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
                         if (!wait(&sm.full[slot], (it / kTcStages) & 1u)) break;
                         tc_fence_after_sync();
                         const uint32_t acc_col = tmem + (gu ? kColU : kColG);
-                        const uint64_t ad = a_k + ((slot * kAStage) >> 4);
+                        const uint64_t ad = a_k + ((slot * G::kASlot) >> 4);
 #pragma unroll
                         for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
@@ -530,28 +538,35 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
                 if (!wait(&sm.h_full, ti & 1u)) break;
                 tc_fence_after_sync();
                 // down: M-tile mt = 128 hidden columns; A is W_down read MN-major
-                // (chunk slabs kChunkBytes apart), K = the tile's 128 rows
-                for (int mt = 0; ok && mt < DT; ++mt, ++it, ++dtc) {
-                    const uint32_t slot = it % kTcStages;
-                    if (!wait(&sm.full[slot], (it / kTcStages) & 1u)) break;
-                    if constexpr (F8) {
-                        // the converters are done with the code box: its slot
-                        // may be refilled
-                        mbar_arrive(&sm.empty8[it8 % kF8Stages]);
-                        ++it8;
-                    }
+                // (chunk slabs kAChunk apart), K = the tile's 128 rows, in
+                // slots of kCRows rows
+                constexpr int kSlotsPerTile = kTcRows / G::kCRows;
+                for (int mt = 0; ok && mt < DT; ++mt, ++dtc) {
                     const uint32_t yb = dtc % kYBufs;
                     if (!wait(&sm.y_empty[yb], ((dtc / kYBufs) & 1u) ^ 1u)) break;
-                    tc_fence_after_sync();
-                    const uint64_t ad = a_mn + ((slot * kAStage) >> 4);
                     const uint32_t ycol = tmem + kColY + yb * kYCols;
+                    for (int h = 0; h < kSlotsPerTile; ++h, ++it) {
+                        const uint32_t slot = it % kTcStages;
+                        if (!wait(&sm.full[slot], (it / kTcStages) & 1u)) break;
+                        if (F8 && h == kSlotsPerTile - 1) {
+                            // the converters are done with the code box: its
+                            // slot may be refilled
+                            mbar_arrive(&sm.empty8[it8 % kF8Stages]);
+                            ++it8;
+                        }
+                        tc_fence_after_sync();
+                        const uint64_t ad = a_mn + ((slot * G::kASlot) >> 4);
 #pragma unroll
-                    for (int ks = 0; ks < kTcRows / 16; ++ks)
-                        umma_bf16(ycol, ad + ((ks * 2048) >> 4),
-                                  h_k + (((ks >> 2) * kHChunk + (ks & 3) * 32) >> 4), id_dn,
-                                  ks ? 1u : 0u);
+                        for (int ks = 0; ks < G::kCRows / 16; ++ks) {
+                            const int kg = h * (G::kCRows / 16) + ks;   // K step in the tile
+                            umma_bf16(ycol, ad + ((ks * 2048) >> 4),
+                                      h_k + (((kg >> 2) * kHChunk + (kg & 3) * 32) >> 4), id_dn,
+                                      kg ? 1u : 0u);
+                        }
+                        umma_commit(&sm.empty[slot]);
+                    }
+                    if (!ok) break;
                     umma_commit(&sm.y_full[yb]);
-                    umma_commit(&sm.empty[slot]);
                 }
                 ++ti;
             }
@@ -685,19 +700,24 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
                     float gs[16], us[16];
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) gs[jj] = us[jj] = 0.0f;
+                    // two terms per TMEM round trip
 #pragma unroll
-                    for (int p = 0; p < kXTerms; ++p) {
-                        uint32_t gp[16], up[16];
-                        tmem_ld16_async(tmem + lanes + kColG + p * Mp + c0, gp);
-                        tmem_ld16_async(tmem + lanes + kColU + p * Mp + c0, up);
+                    for (int p = 0; p < kXTerms; p += 2) {
+                        uint32_t g0[16], u0[16], g1[16], u1[16];
+                        tmem_ld16_async(tmem + lanes + kColG + p * Mp + c0, g0);
+                        tmem_ld16_async(tmem + lanes + kColU + p * Mp + c0, u0);
+                        tmem_ld16_async(tmem + lanes + kColG + (p + 1) * Mp + c0, g1);
+                        tmem_ld16_async(tmem + lanes + kColU + (p + 1) * Mp + c0, u1);
                         tmem_wait_ld();
-                        tmem_regs_ready(gp);
-                        tmem_regs_ready(up);
-                        const float f = 1.0f / (float)(1 << (4 * p));
+                        tmem_regs_ready(g0);
+                        tmem_regs_ready(u0);
+                        tmem_regs_ready(g1);
+                        tmem_regs_ready(u1);
+                        const float f0 = 1.0f / (float)(1 << (4 * p)), f1 = f0 * (1.0f / 16.0f);
 #pragma unroll
                         for (int jj = 0; jj < 16; ++jj) {
-                            gs[jj] += __uint_as_float(gp[jj]) * f;
-                            us[jj] += __uint_as_float(up[jj]) * f;
+                            gs[jj] += __uint_as_float(g0[jj]) * f0 + __uint_as_float(g1[jj]) * f1;
+                            us[jj] += __uint_as_float(u0[jj]) * f0 + __uint_as_float(u1[jj]) * f1;
                         }
                     }
 #pragma unroll
@@ -877,46 +897,49 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
         // adjacent rows and write their bf16 units to one chunk's even and
         // the other chunk's odd swizzled positions, so neither the loads nor
         // the stores conflict.  Gate / up boxes go to the MMA as they are.
-        constexpr int kRowsPerCvt = kTcRows / G::kCvtWarps;   // 32
+        constexpr int kRowsPerCvt = G::kCRows / G::kCvtWarps;   // rows of each slot per warp
         const int cw = warp - 10;
         const int pr = lane >> 4, ph = (lane >> 3) & 1, sub = (lane >> 2) & 1;
         const int q = ((sub ^ ph) << 2) | (lane & 3);   // 16-code unit of the row
         const int rsub = 2 * pr + sub;                   // row within the step
         const int u0 = 2 * (q & 3);                      // first bf16 unit in the chunk
-        uint32_t it8 = 0, itc = 0, par_d = 0u;           // boxes, down boxes, per-slot full8d parity
+        uint32_t it8 = 0, itc = 0, par_d = 0u;           // boxes, bf16 slots, per-slot full8d parity
         int r = r_begin;
         TSeg s;
         while (ok && next_tile(a, sm, r, r_end, s)) {
             it8 += 2 * KP;                               // the tile's gate / up boxes
-            for (int mt = 0; mt < DT; ++mt, ++it8, ++itc) {
-                const uint32_t s8 = it8 % kF8Stages, sc = itc % kTcStages;
+            for (int mt = 0; ok && mt < DT; ++mt, ++it8) {
+                const uint32_t s8 = it8 % kF8Stages;
                 const uint32_t par = (par_d >> s8) & 1u;
                 par_d ^= 1u << s8;
                 if (!wait(&sm.full8d[s8], par)) break;
-                if (!wait(&sm.empty[sc], ((itc / kTcStages) & 1u) ^ 1u)) break;
                 const unsigned char* box = f8ring + s8 * kF8Box;
-                unsigned char* dst = aring + sc * kAStage + (q >> 2) * kChunkBytes;
-                // all loads first: the compiler cannot tell the two rings
-                // apart and would otherwise keep each load behind the
-                // previous step's stores
-                uint4 w[kRowsPerCvt / 4];
+                for (int h = 0; h < kTcRows / G::kCRows; ++h, ++itc) {
+                    const uint32_t sc = itc % kTcStages;
+                    if (!wait(&sm.empty[sc], ((itc / kTcStages) & 1u) ^ 1u)) break;
+                    unsigned char* dst = aring + sc * G::kASlot + (q >> 2) * G::kAChunk;
+                    // all loads first: the compiler cannot tell the two rings
+                    // apart and would otherwise keep each load behind the
+                    // previous step's stores
+                    uint4 w[kRowsPerCvt / 4];
 #pragma unroll
-                for (int i = 0; i < kRowsPerCvt / 4; ++i) {
-                    const int row = cw * kRowsPerCvt + i * 4 + rsub;
-                    w[i] = *reinterpret_cast<const uint4*>(box + row * 128 + ((q ^ (row & 7)) << 4));
-                }
+                    for (int i = 0; i < kRowsPerCvt / 4; ++i) {
+                        const int row = h * G::kCRows + cw * kRowsPerCvt + i * 4 + rsub;   // row of the box
+                        w[i] = *reinterpret_cast<const uint4*>(box + row * 128 + ((q ^ (row & 7)) << 4));
+                    }
 #pragma unroll
-                for (int i = 0; i < kRowsPerCvt / 4; ++i) {
-                    const int row = cw * kRowsPerCvt + i * 4 + rsub;
-                    uint4 o0, o1;
-                    e4m3x16_to_bf16(w[i], o0, o1);
-                    unsigned char* drow = dst + row * 128;
-                    *reinterpret_cast<uint4*>(drow + ((u0 ^ (row & 7)) << 4)) = o0;
-                    *reinterpret_cast<uint4*>(drow + (((u0 + 1) ^ (row & 7)) << 4)) = o1;
+                    for (int i = 0; i < kRowsPerCvt / 4; ++i) {
+                        const int row = cw * kRowsPerCvt + i * 4 + rsub;                    // row of the slot
+                        uint4 o0, o1;
+                        e4m3x16_to_bf16(w[i], o0, o1);
+                        unsigned char* drow = dst + row * 128;
+                        *reinterpret_cast<uint4*>(drow + ((u0 ^ (row & 7)) << 4)) = o0;
+                        *reinterpret_cast<uint4*>(drow + (((u0 + 1) ^ (row & 7)) << 4)) = o1;
+                    }
+                    fence_async_smem();      // the stores are read by the MMA (async proxy)
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sm.full[sc]);
                 }
-                fence_async_smem();      // the stores are read by the MMA (async proxy)
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.full[sc]);
             }
         }
     }
@@ -934,7 +957,7 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
 template <bool F8>
 static size_t tc_smem_bytes(int units, const FfnArgs* local) {
     using G = TcGeo<F8>;
-    return 1024 + (size_t)G::kF8Stages * kF8Box + (size_t)G::kAStages * kAStage + (size_t)G::kBPairs * G::kBPair +
+    return 1024 + (size_t)G::kF8Stages * kF8Box + (size_t)G::kAStages * G::kASlot + (size_t)G::kBPairs * G::kBPair +
            G::kHTile + G::kYStage + sizeof(TcSmem<G>) + (size_t)units * sizeof(int4) +
            (local ? local_route_bytes(local->T, local->n, local->k, local->g, G::kWarps) : 0);
 }
