@@ -26,7 +26,9 @@
 // 4-stage ring; warp 1 issues the MMAs (one thread) and owns the TMEM
 // allocation; warps 2-5 are the epilogue (TMEM -> registers, SwiGLU, H tile,
 // output atomics); warps 6-9 gather the bf16 hi/lo activations (split once per
-// layer) into swizzled B tiles with cp.async.
+// layer) into swizzled B tiles with cp.async; the CTA has 16 warps so that the
+// in-CTA top-k (a warp per token) takes up to 16 tokens in one round, and the
+// warps past the roles only take part in that prologue.
 //
 // FP8 (E4M3 codes, one fp32 scale per weight row): TMA lands 16 KB boxes of
 // codes (128 rows x 128 columns, 128 B swizzle) in a 6-stage ring.  Gate / up
@@ -110,7 +112,9 @@ struct TcGeo {
     static constexpr int kHTile = 2 * kHChunk;               // K = 128 tile rows
     static constexpr int kYStage = kTok * 128 * 4;           // down output of one M-tile: [token][128 fp32]
     static constexpr int kCvtWarps = F8 ? 4 : 0;
-    static constexpr int kWarps = 10 + kCvtWarps;
+    // 16 warps: the in-CTA top-k takes one token per warp, so up to 16 tokens
+    // are selected in one round; warps past the roles idle after the prologue
+    static constexpr int kWarps = 16;
     static constexpr int kThreads = kWarps * 32;
     static constexpr int kPdTok = F8 ? 1 : kTok;             // form-P down lists (bf16 only)
     // Tensor memory (512 columns): the G and U accumulators (N = kBTerms Mp
@@ -906,7 +910,7 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
         uint32_t it8 = 0, itc = 0, par_d = 0u;           // boxes, bf16 slots, per-slot full8d parity
         int r = r_begin;
         TSeg s;
-        while (ok && next_tile(a, sm, r, r_end, s)) {
+        while (cw < G::kCvtWarps && ok && next_tile(a, sm, r, r_end, s)) {
             it8 += 2 * KP;                               // the tile's gate / up boxes
             for (int mt = 0; ok && mt < DT; ++mt, ++it8) {
                 const uint32_t s8 = it8 % kF8Stages;
