@@ -30,28 +30,53 @@ def B():
     return H.ensure_built()
 
 
+def scales_of(shape, L):
+    """FP8 row scales in the order of the *_fp8 calls (None for bf16 layers)."""
+    if shape.dtype != "fp8":
+        return None
+    keys = ("dgate", "dup", "ddown", "pgate", "pup", "pdown") if shape.I_sh > 0 else ("gate", "up", "down")
+    return [L[k + "_sc"] for k in keys] + [None, None, None]
+
+
+def decoded(shape, L):
+    """The layer with its FP8 weights decoded exactly (the oracle's weights)."""
+    if shape.dtype != "fp8":
+        return L
+    D = dict(L)
+    for key in ("gate", "up", "down", "dgate", "dup", "ddown", "pgate", "pup", "pdown"):
+        if L.get(key) is not None:
+            D[key] = O.dequant_rows_e4m3(L[key], L[key + "_sc"])
+    return D
+
+
 def layer_once(B, shape, L, x, ws):
     T = x.shape[0]
     idx = torch.empty((T, shape.k), dtype=torch.int32, device=DEV)
     w = torch.empty((T, shape.k), dtype=torch.float32, device=DEV)
     y = torch.empty((T, shape.d), dtype=torch.float32, device=DEV)
+    sc = scales_of(shape, L)
     if shape.I_sh > 0:
         B.deamoe_layer_forward(x, shape.k, 1.0, L["router"], L["bias"], shape.g,
                                (L["dgate"], L["dup"], L["ddown"]), (L["pgate"], L["pup"], L["pdown"]),
-                               None, ws, idx, w, y)
+                               None, ws, idx, w, y, scales=sc)
     else:
         B.moe_layer_forward(x, shape.k, 1.0, L["router"], L["bias"], L["gate"], L["up"], L["down"], None,
-                            ws, idx, w, y)
+                            ws, idx, w, y, scales=sc)
     torch.cuda.synchronize()
     return idx, w, y
 
 
 # (layer, T, tensor-core threshold): the CUDA-core kernel alone with routing
 # in its CTAs; the tensor-core kernel alone with routing in its CTAs; both
-# kernels on the routing kernel's dispatch (units of >= 4 tokens on tcgen05)
+# kernels on the routing kernel's dispatch (units of >= 4 tokens on tcgen05);
+# the same three with E4M3 weights (the tensor-core kernel's converter warps
+# and its two landing barriers per code slot)
 CASES = [(synth.VANILLA_128E, 4, 0, "ffn_stream_kernel"),
          (synth.DEAMOE_7B, 16, 0, "ffn_tc_kernel"),
-         (synth.DEAMOE_7B, 16, 4, "both")]
+         (synth.DEAMOE_7B, 16, 4, "both"),
+         (synth.VANILLA_128E_FP8, 4, 0, "ffn_stream_kernel-fp8"),
+         (synth.DEAMOE_7B_FP8, 16, 0, "ffn_tc_kernel-fp8"),
+         (synth.DEAMOE_7B_FP8, 16, 4, "both-fp8")]
 
 
 @pytest.mark.parametrize("shape,T,thr,kernels", CASES, ids=[c[3] for c in CASES])
@@ -79,7 +104,7 @@ def test_wait_runs_out_and_reports_timeout(B, shape, T, thr, kernels):
         assert B.moe_read_status(ws)[0] == 0
         ties = H.compare_routing(idx.cpu().numpy(), w.cpu().numpy(), oi, op, info, x, L["router"])
         tokens = [t for t in range(T) if t not in ties]
-        ref = H.oracle_layer(shape, L, x, oi, op, tokens)
+        ref = H.oracle_layer(shape, decoded(shape, L), x, oi, op, tokens)
         assert H.rel_err(y.cpu().numpy()[tokens], ref) <= H.KERNEL_TOL
     finally:
         B.moe_set_tc_min_tokens(prev_thr)
