@@ -88,7 +88,7 @@ const char* moe_last_error(void);
  * run on the tcgen05 kernel, the others on the CUDA cores; a value above every
  * batch size keeps everything on the CUDA cores.  Process-wide; returns the
  * previous setting, or MOE_ERR_INVALID_ARG for a negative value.  The
- * tensor-core kernel applies to bf16 weights with d % 128 == 0 and unit row
+ * tensor-core kernel applies to bf16 and E4M3 weights with d % 128 == 0 and unit row
  * counts that are multiples of 128.
  */
 int moe_set_tc_min_tokens(int min_tokens);
@@ -429,9 +429,14 @@ int deamoe_layer_forward(const float* x, int T, int d, int n, int k, float scale
  *     deamoe_*_fp8: [0..2] the departments, [3..5] the private rows
  *     (ignored when I_pr == 0), [6..8] the shared expert (ignored when
  *     I_s == 0).
- * Other arguments, limits and results as for the bf16 calls, except that
- * the CUDA-core kernel always runs (no tensor-core path for FP8).  The
- * bf16 / fp32 calls reject dtype MOE_DTYPE_FP8_E4M3.
+ * Other arguments, limits, kernel choice and results as for the bf16 calls.
+ * On the tensor cores the gate and up products take the codes as they are
+ * (8-bit MMAs) against the activations written as four E4M3 terms per token
+ * with a power-of-two scale (x = 2^-e0 (q0 + q1/16 + q2/256 + q3/4096), within
+ * 2^-16 of each element; the workspace's xb region holds them); the down
+ * product expands the codes to bf16 exactly.  Either kernel's output is
+ * within 1e-4 of the layer on the exactly decoded weights.  The bf16 / fp32
+ * calls reject dtype MOE_DTYPE_FP8_E4M3.
  */
 int moe_ffn_vanilla_fp8(const float* x, int T, int d, int n, int k, int I,
                         const void* w_gate, const void* w_up, const void* w_down, int I_s,
