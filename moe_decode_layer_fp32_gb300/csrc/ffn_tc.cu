@@ -273,6 +273,10 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d = a.f.d;
     const int KP = d / 128, DT = d / 128;          // K-pairs (gate/up), M-tiles (down)
+    // The CTAs take the down M-tiles (128 output columns each) in orders
+    // rotated by the block index, so that their output reductions spread
+    // over the whole row of y instead of all landing on the same columns.
+    const int mt_rot = (int)(blockIdx.x % (unsigned)DT);
 
     if (tid == 0) {
         for (int i = 0; i < kTcStages; ++i) {
@@ -455,8 +459,10 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
                     if (!load(&maps[0], y, p, false)) break;
                     if (!load(&maps[1], y, p, false)) break;
                 }
-                for (int mt = 0; ok && has_dn && mt < DT; ++mt)
-                    if (!load(&maps[2], y, mt, F8)) break;
+                for (int mt = 0; ok && has_dn && mt < DT; ++mt) {
+                    const int mc = mt + mt_rot < DT ? mt + mt_rot : mt + mt_rot - DT;
+                    if (!load(&maps[2], y, mc, F8)) break;
+                }
             }
             // every issued copy must land before the CTA may exit: the last
             // copy into each slot (the earlier ones were waited for before
@@ -797,7 +803,8 @@ __global__ void __launch_bounds__(TcGeo<F8>::kThreads, 1) ffn_tc_kernel(const __
                         wst[(c0 + jj) * 32 + lane] = __uint_as_float(yhi[jj]) + __uint_as_float(ylo[jj]);
                 }
                 __syncwarp();
-                float* ybase = a.f.out + dt * 128 + quarter * 32;
+                const int dc = dt + mt_rot < DT ? dt + mt_rot : dt + mt_rot - DT;   // the producer's order
+                float* ybase = a.f.out + dc * 128 + quarter * 32;
                 for (int q = lane; q < mg * 8; q += 32) {
                     const int j = q >> 3, c4 = (q & 7) * 4;
                     const float4 v = *reinterpret_cast<const float4*>(wst + j * 32 + c4);
