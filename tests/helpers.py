@@ -186,6 +186,14 @@ def oracle_layer(shape, L, x, idx, p, tokens=None):
     return O.vanilla_layer(xs, idx_s, p_s, L["gate"], L["up"], L["down"], shared=sh)
 
 
+def fp8_scales(shape, L):
+    """Row scales of an FP8 layer in the order of the *_fp8 calls (None otherwise)."""
+    if shape.dtype != "fp8":
+        return None
+    keys = ("dgate", "dup", "ddown", "pgate", "pup", "pdown") if shape.I_sh > 0 else ("gate", "up", "down")
+    return [L.get(k + "_sc") for k in keys + ("sgate", "sup", "sdown")]
+
+
 def run_layer_forward(binding, shape, L, x, scale=1.0):
     """Whole-layer path (fused route+dispatch, FFN as its dependent)."""
     T = x.shape[0]
@@ -194,12 +202,13 @@ def run_layer_forward(binding, shape, L, x, scale=1.0):
     idx = torch.empty((T, shape.k), dtype=torch.int32, device=x.device)
     w = torch.empty((T, shape.k), dtype=torch.float32, device=x.device)
     y = torch.empty((T, shape.d), dtype=torch.float32, device=x.device)
+    sc = fp8_scales(shape, L)
     if shape.I_sh > 0:
         priv = (L["pgate"], L["pup"], L["pdown"]) if shape.I_pr > 0 else None
         binding.deamoe_layer_forward(x, shape.k, scale, L["router"], L["bias"], shape.g,
                                      (L["dgate"], L["dup"], L["ddown"]), priv, shared_of(L),
-                                     ws, idx, w, y)
+                                     ws, idx, w, y, scales=sc)
     else:
         binding.moe_layer_forward(x, shape.k, scale, L["router"], L["bias"], L["gate"], L["up"],
-                                  L["down"], shared_of(L), ws, idx, w, y)
+                                  L["down"], shared_of(L), ws, idx, w, y, scales=sc)
     return ws, idx, w, y

@@ -136,7 +136,8 @@ def expected_auto_choice(shape, T, exp_count, dept_count, sms):
 @pytest.mark.parametrize("shape,T", [(synth.VANILLA_128E, 16), (synth.VANILLA_128E, 4),
                                      (synth.DEAMOE_7B, 16), (synth.DEAMOE_7B, 8),
                                      (synth.DEAMOE_7B, 4), (synth.ZIPF_DEAMOE, 64),
-                                     (synth.DSV3_DEAMOE, 32), (synth.DSV3_VANILLA, 1)])
+                                     (synth.DSV3_DEAMOE, 32), (synth.DSV3_VANILLA, 1),
+                                     (synth.DEAMOE_7B_FP8, 16), (synth.DEAMOE_7B_FP8, 4)])
 def test_auto_choice_matches_cost_model(B, threshold, shape, T):
     """Default mode: the FFN kernels pick one path per call on the device;
     the choice they record equals the cost model evaluated on the host from
@@ -158,3 +159,5 @@ def test_auto_choice_matches_cost_model(B, threshold, shape, T):
         assert want == 2          # dense department backbones: tensor cores
     if (shape, T) == (synth.VANILLA_128E, 16):
         assert want == 0          # ~1 token per expert expected: tensor cores not launched
+    if (shape, T) == (synth.DEAMOE_7B_FP8, 16):
+        assert want == 2          # E4M3 weights take the same choice as bf16
